@@ -1,0 +1,246 @@
+"""Seeded synthetic inputs for the MLA decode post-attention stage.
+
+This module only draws inputs: partial latents ``o``, their log-sum-exp
+values ``lse``, the up-projection ``W_V`` (bf16, or MXFP4 codes + E8M0
+scales as a checkpoint would store them) and the ``gate``.  It holds none of
+the stage's own arithmetic (no LSE merge, no latent rounding or quantisation,
+no GEMM), so the CUDA path and the CPU oracle can both take their inputs from
+it without sharing any of the computation under test.
+
+Shapes follow the decode workload of the vLLM page
+"vllm.models.kimi_k3.amd.specialized_decode.mono.attention.mla_back"
+(12 heads per rank, 512-wide latents, 128-wide V heads; up to 96 heads in the
+large multi-token-prediction batch).
+
+The workloads (``WORKLOADS``):
+
+* ``tiny_split``   S=4 (2 requests x q=2), H=2, 2 splits per request, P=4
+                   request-major; lse ~N(4,2) with one -inf and one NaN.
+* ``nosplit``      P=1, S=64, H=12: lse unused, pure up-projection + gate.
+* ``splitkv``      64 requests x q=1, H=12, 16 splits per request, compact
+                   [16, 64, 12, 512]; lse ~N(6,3) with 10% -inf.
+* ``splitkv_rm``   the same splits in request-major layout, P=1024
+                   ([1024, 64, 12, 512]; only 1/64 of it is read, the rest
+                   is NaN so that a wrong read shows).
+* ``stacked_mxfp4`` 8 stacked shard partials, S=256 live of S_out=264, H=12;
+                   lse ~N(4,2) with 5% -inf, 0.1% NaN and 8 (t, h) rows all
+                   -inf; MXFP4 W_V.
+* ``mtp``          1024 requests x q=4 (S=4096), H=96, 4 splits per request
+                   compact; lse ~N(5,2) with 2% -inf; bf16 W_V.
+* ``mtp_mxfp4``    the same with MXFP4 W_V.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+D = 512   # latent width
+V = 128   # V head dim
+BLK = 32  # MX block along K
+
+W_BF16 = 0
+W_MXFP4 = 1
+
+
+@dataclass
+class Workload:
+    name: str
+    S: int
+    H: int
+    P: int
+    q: int
+    spr: int
+    w_fmt: int
+    S_out: int | None = None
+    lse_mean: float = 0.0
+    lse_std: float = 1.0
+    neg_inf_frac: float = 0.0
+    nan_frac: float = 0.0
+    dead_rows: int = 0            # (t, h) rows whose every partial is -inf
+    exact_neg_inf: int = 0        # a fixed count of -inf entries (tiny case)
+    exact_nan: int = 0            # a fixed count of NaN entries (tiny case)
+    lse_unused: bool = False      # P == 1: lse all 0 and ignored
+    seed: int = 0
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def out_rows(self) -> int:
+        return self.S if self.S_out is None else self.S_out
+
+    @property
+    def requests(self) -> int:
+        return self.S // self.q
+
+
+WORKLOADS = {
+    "tiny_split": Workload("tiny_split", S=4, H=2, P=4, q=2, spr=2, w_fmt=W_BF16,
+                           lse_mean=4.0, lse_std=2.0, exact_neg_inf=1, exact_nan=1, seed=0),
+    "nosplit": Workload("nosplit", S=64, H=12, P=1, q=1, spr=0, w_fmt=W_BF16,
+                        lse_unused=True, seed=1),
+    "splitkv": Workload("splitkv", S=64, H=12, P=16, q=1, spr=16, w_fmt=W_BF16,
+                        lse_mean=6.0, lse_std=3.0, neg_inf_frac=0.10, seed=2),
+    "splitkv_rm": Workload("splitkv_rm", S=64, H=12, P=1024, q=1, spr=16, w_fmt=W_BF16,
+                           lse_mean=6.0, lse_std=3.0, neg_inf_frac=0.10, seed=2),
+    "stacked_mxfp4": Workload("stacked_mxfp4", S=256, S_out=264, H=12, P=8, q=1, spr=8,
+                              w_fmt=W_MXFP4, lse_mean=4.0, lse_std=2.0, neg_inf_frac=0.05,
+                              nan_frac=0.001, dead_rows=8, seed=3),
+    "mtp": Workload("mtp", S=4096, H=96, P=4, q=4, spr=4, w_fmt=W_BF16,
+                    lse_mean=5.0, lse_std=2.0, neg_inf_frac=0.02, seed=4),
+    "mtp_mxfp4": Workload("mtp_mxfp4", S=4096, H=96, P=4, q=4, spr=4, w_fmt=W_MXFP4,
+                          lse_mean=5.0, lse_std=2.0, neg_inf_frac=0.02, seed=4),
+}
+
+
+def _gen(device, seed):
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def _normal(shape, std, g, device, dtype=torch.float32):
+    x = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+    if std != 1.0:
+        x.mul_(std)
+    return x.to(dtype)
+
+
+def mxfp4_pack_weights(w: torch.Tensor):
+    """Store float weights [H, 128, 512] in the MXFP4 checkpoint format.
+
+    Data preparation only (it is the weight file's format, not a step of the
+    stage): each 32-wide block along K gets the smallest power-of-two scale
+    that fits its largest magnitude into 6 (so nothing clips), and each
+    element takes the nearest E2M1 magnitude, ties away from zero.  Returns
+    (codes u8 [H, 128, 256], element 2i in the low nibble of byte i;
+    scales u8 [H, 128, 16], E8M0).
+    """
+    H, Vr, K = w.shape
+    blocks = w.float().reshape(H, Vr, K // BLK, BLK)
+    amax = blocks.abs().amax(-1)
+    # smallest e with amax / 2^e <= 6  ->  e = ceil(log2(amax / 6))
+    e = torch.ceil(torch.log2(torch.clamp(amax, min=1e-30) / 6.0))
+    e = torch.clamp(e, -126, 127)
+    e = torch.where(amax > 0, e, torch.full_like(e, -126))
+    scaled = blocks / torch.exp2(e).unsqueeze(-1)
+    # midpoints between neighbouring E2M1 magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6;
+    # a magnitude at or past a midpoint takes the larger neighbour
+    mids = torch.tensor([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], device=w.device)
+    mag = scaled.abs()
+    best = (mag.unsqueeze(-1) >= mids).sum(-1)
+    codes = best.to(torch.uint8) | ((scaled < 0) & (best > 0)).to(torch.uint8) * 8
+    codes = codes.reshape(H, Vr, K)
+    packed = codes[..., 0::2] | (codes[..., 1::2] << 4)
+    scales = (e + 127).to(torch.uint8)
+    return packed.contiguous(), scales.contiguous()
+
+
+def make(wl: Workload | str, device="cpu", seed: int | None = None, w_fmt: int | None = None):
+    """Draw one workload's inputs on ``device``.
+
+    Returns a dict of tensors: o [P, S, H, 512] bf16, lse [P, S, H] f32 (or
+    None when P == 1 and lse is unused), w_v, w_scale (None for bf16 W_V),
+    gate [S, H*128] bf16, plus the integer parameters.
+    """
+    if isinstance(wl, str):
+        wl = WORKLOADS[wl]
+    seed = wl.seed if seed is None else seed
+    w_fmt = wl.w_fmt if w_fmt is None else w_fmt
+    g = _gen(device, seed)
+    S, H, P = wl.S, wl.H, wl.P
+
+    request_major = P > 1 and P != wl.spr
+    if request_major:
+        # only token t's request's splits are ever read; everything else NaN
+        o = torch.full((P, S, H, D), float("nan"), device=device, dtype=torch.bfloat16)
+        lse = torch.full((P, S, H), float("nan"), device=device, dtype=torch.float32)
+        live_o = _normal((wl.spr, S, H, D), 1.0, g, device, torch.bfloat16)
+        live_l = _normal((wl.spr, S, H), wl.lse_std, g, device) + wl.lse_mean
+        t = torch.arange(S, device=device)
+        for j in range(wl.spr):
+            r = (t // wl.q) * wl.spr + j
+            o[r, t] = live_o[j]
+            lse[r, t] = live_l[j]
+        sel_mask = torch.zeros((P, S, H), dtype=torch.bool, device=device)
+        for j in range(wl.spr):
+            sel_mask[(t // wl.q) * wl.spr + j, t] = True
+    else:
+        o = _normal((P, S, H, D), 1.0, g, device, torch.bfloat16)
+        if wl.lse_unused:
+            lse = torch.zeros((P, S, H), device=device, dtype=torch.float32)
+        else:
+            lse = _normal((P, S, H), wl.lse_std, g, device) + wl.lse_mean
+        sel_mask = torch.ones((P, S, H), dtype=torch.bool, device=device)
+
+    if P > 1:
+        live_idx = sel_mask.flatten().nonzero().flatten()
+        n_live = live_idx.numel()
+        flat = lse.view(-1)
+        if wl.neg_inf_frac > 0:
+            u = torch.rand(n_live, generator=g, device=device)
+            flat[live_idx[u < wl.neg_inf_frac]] = float("-inf")
+        if wl.nan_frac > 0:
+            u = torch.rand(n_live, generator=g, device=device)
+            flat[live_idx[u < wl.nan_frac]] = float("nan")
+        if wl.exact_neg_inf or wl.exact_nan:
+            perm = torch.randperm(n_live, generator=g, device=device)
+            k1, k2 = wl.exact_neg_inf, wl.exact_nan
+            flat[live_idx[perm[:k1]]] = float("-inf")
+            flat[live_idx[perm[k1:k1 + k2]]] = float("nan")
+        if wl.dead_rows:
+            perm = torch.randperm(S * H, generator=g, device=device)[: wl.dead_rows]
+            for i in perm.tolist():
+                t, h = divmod(i, H)
+                lse[sel_mask[:, t, h], t, h] = float("-inf")
+    else:
+        lse = None if wl.lse_unused else lse
+
+    w = _normal((H, V, D), 1.0 / math.sqrt(D), g, device)
+    if w_fmt == W_BF16:
+        w_v, w_scale = w.to(torch.bfloat16).contiguous(), None
+    else:
+        w_v, w_scale = mxfp4_pack_weights(w)
+    gate = torch.sigmoid(_normal((S, H * V), 1.0, g, device)).to(torch.bfloat16).contiguous()
+    return dict(o=o, lse=lse, w_v=w_v, w_scale=w_scale, gate=gate, S=S, S_out=wl.out_rows,
+                H=H, P=P, q=wl.q, spr=wl.spr, w_fmt=w_fmt, name=wl.name)
+
+
+def custom(S, H, P, q, spr, w_fmt, S_out=None, seed=0, device="cpu", lse_mean=4.0,
+           lse_std=2.0, neg_inf_frac=0.0, nan_frac=0.0, dead_rows=0, lse_unused=False):
+    """A workload of any shape with the same recipe (for edge-case tests)."""
+    wl = Workload("custom", S=S, H=H, P=P, q=q, spr=spr, w_fmt=w_fmt, S_out=S_out,
+                  lse_mean=lse_mean, lse_std=lse_std, neg_inf_frac=neg_inf_frac,
+                  nan_frac=nan_frac, dead_rows=dead_rows, lse_unused=lse_unused, seed=seed)
+    return make(wl, device=device)
+
+
+def algorithmic_bytes(inp) -> int:
+    """Bytes the stage must move: every partial row with a finite sanitised
+    LSE (the rows whose weight can be non-zero; P == 1 reads every row), all
+    selected LSE values, W_V (and its scales), the gate rows and the output."""
+    S, S_out, H, P, q, spr = (inp[k] for k in ("S", "S_out", "H", "P", "q", "spr"))
+    if P == 1:
+        rows = S * H
+        lse_bytes = 0
+    else:
+        lse = inp["lse"]
+        n_sel = (S * H * spr)
+        fin = torch.isfinite(lse) & (lse < float("inf"))
+        if P != spr:  # request-major: only the selected entries count
+            t = torch.arange(S, device=lse.device)
+            cnt = 0
+            for j in range(spr):
+                cnt += int(fin[(t // q) * spr + j, t].sum())
+            rows = cnt
+        else:
+            rows = int(fin.sum())
+        lse_bytes = 4 * n_sel
+    wv = inp["w_v"].numel() * inp["w_v"].element_size()
+    if inp["w_scale"] is not None:
+        wv += inp["w_scale"].numel()
+    return rows * D * 2 + lse_bytes + wv + S * H * V * 2 + S_out * H * V * 2
+
+
+def flops(inp) -> int:
+    return 2 * inp["S"] * inp["H"] * V * D

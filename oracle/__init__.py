@@ -1,0 +1,214 @@
+"""CPU oracle for the MLA decode post-attention stage (test infrastructure).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never loads it.
+
+The arithmetic lives in ``mla_oracle.c`` (plain single-threaded C, fp32 as
+the vLLM page "vllm.models.kimi_k3.amd.specialized_decode.mono.attention.
+mla_back" fixes it).  This module only compiles it with gcc and marshals
+numpy arrays into it.  bf16 values travel as ``uint16`` bit patterns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mla_oracle.c")
+_HDR = os.path.join(_HERE, "mla_oracle.h")
+_LIB_PATH = os.path.join(_HERE, "libmla_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+D, V, BLK = 512, 128, 32
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no fused multiply-add: one rounding per op)."""
+    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_HDR))
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < newest:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+               "-shared", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True, cwd=_HERE)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class _Args(ctypes.Structure):
+    _fields_ = [
+        ("S", ctypes.c_int), ("S_out", ctypes.c_int), ("H", ctypes.c_int),
+        ("P", ctypes.c_int), ("q", ctypes.c_int), ("spr", ctypes.c_int),
+        ("o", ctypes.c_void_p), ("o_sp", ctypes.c_int64), ("o_st", ctypes.c_int64),
+        ("o_sh", ctypes.c_int64),
+        ("lse", ctypes.c_void_p), ("l_sp", ctypes.c_int64), ("l_st", ctypes.c_int64),
+        ("l_sh", ctypes.c_int64),
+        ("w_v", ctypes.c_void_p), ("w_sh", ctypes.c_int64), ("w_sv", ctypes.c_int64),
+        ("w_scale", ctypes.c_void_p), ("s_sh", ctypes.c_int64), ("s_sv", ctypes.c_int64),
+        ("w_fmt", ctypes.c_int),
+        ("gate", ctypes.c_void_p),
+    ]
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            L = ctypes.CDLL(_LIB_PATH)
+            P = ctypes.POINTER
+            L.orc_bf16_to_f32.restype = ctypes.c_float
+            L.orc_bf16_to_f32.argtypes = [ctypes.c_uint16]
+            L.orc_f32_to_bf16.restype = ctypes.c_uint16
+            L.orc_f32_to_bf16.argtypes = [ctypes.c_float]
+            L.orc_e2m1_value.restype = ctypes.c_float
+            L.orc_e2m1_value.argtypes = [ctypes.c_int]
+            L.orc_e8m0_value.restype = ctypes.c_float
+            L.orc_e8m0_value.argtypes = [ctypes.c_int]
+            L.orc_e2m1_code.restype = ctypes.c_int
+            L.orc_e2m1_code.argtypes = [ctypes.c_float]
+            L.orc_mx_scale_code.restype = ctypes.c_int
+            L.orc_mx_scale_code.argtypes = [ctypes.c_void_p]
+            L.orc_mx_quant_block.restype = None
+            L.orc_mx_quant_block.argtypes = [ctypes.c_void_p, ctypes.c_void_p, P(ctypes.c_int)]
+            L.orc_sane.restype = ctypes.c_float
+            L.orc_sane.argtypes = [ctypes.c_float]
+            L.orc_partial_set.restype = ctypes.c_int
+            L.orc_partial_set.argtypes = [ctypes.c_int] * 5 + [P(ctypes.c_int), P(ctypes.c_int)]
+            for name in ("orc_combine_latent", "orc_latent_bf16", "orc_row"):
+                f = getattr(L, name)
+                f.restype = ctypes.c_int
+                f.argtypes = [P(_Args), ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+            L.orc_rows.restype = ctypes.c_int
+            L.orc_rows.argtypes = [P(_Args), ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                   ctypes.c_void_p]
+            L.orc_mla_combine_uv.restype = ctypes.c_int
+            L.orc_mla_combine_uv.argtypes = [P(_Args), ctypes.c_void_p]
+            _lib = L
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _estrides(a):
+    return [s // a.itemsize for s in a.strides]
+
+
+class Problem:
+    """One call's inputs as numpy arrays (kept alive while the oracle runs).
+
+    o       uint16 [P, S, H, 512] (bf16 bits; any strides, last dim contiguous)
+    lse     float32 [P, S, H] or None (allowed only when P == 1)
+    w_v     uint16 [H, 128, 512] (w_fmt 0) or uint8 [H, 128, 256] (w_fmt 1)
+    w_scale uint8 [H, 128, 16] (w_fmt 1)
+    gate    uint16 [S, H*128] dense
+    """
+
+    def __init__(self, o, lse, q, spr, w_v, w_scale, w_fmt, gate, S_out=None):
+        self.o, self.lse, self.w_v, self.w_scale, self.gate = o, lse, w_v, w_scale, gate
+        P, S, H, d = o.shape
+        assert d == D and o.strides[-1] == o.itemsize and o.dtype == np.uint16
+        assert gate.dtype == np.uint16 and gate.flags.c_contiguous
+        self.S, self.H, self.P = S, H, P
+        self.S_out = S if S_out is None else S_out
+        a = _Args()
+        a.S, a.S_out, a.H, a.P, a.q, a.spr = S, self.S_out, H, P, q, spr
+        a.o = _ptr(o)
+        a.o_sp, a.o_st, a.o_sh, _ = _estrides(o)
+        if lse is not None:
+            assert lse.dtype == np.float32
+            a.lse = _ptr(lse)
+            a.l_sp, a.l_st, a.l_sh = _estrides(lse)
+        a.w_v = _ptr(w_v)
+        a.w_sh, a.w_sv, _ = _estrides(w_v)
+        if w_scale is not None:
+            a.w_scale = _ptr(w_scale)
+            a.s_sh, a.s_sv, _ = _estrides(w_scale)
+        a.w_fmt = w_fmt
+        a.gate = _ptr(gate)
+        self.args = a
+
+    def full(self) -> np.ndarray:
+        out = np.empty((self.S_out, self.H * V), np.uint16)
+        rc = lib().orc_mla_combine_uv(ctypes.byref(self.args), _ptr(out))
+        if rc != 0:
+            raise ValueError("oracle rejected the problem (layout or shape)")
+        return out
+
+    def rows(self, ts, hs) -> np.ndarray:
+        ts = np.ascontiguousarray(ts, np.int32)
+        hs = np.ascontiguousarray(hs, np.int32)
+        segs = np.empty((len(ts), V), np.uint16)
+        rc = lib().orc_rows(ctypes.byref(self.args), len(ts), _ptr(ts), _ptr(hs), _ptr(segs))
+        if rc != 0:
+            raise ValueError("oracle rejected the problem (layout or shape)")
+        return segs
+
+    def latent_f32(self, t, h) -> np.ndarray:
+        lat = np.empty(D, np.float32)
+        if lib().orc_combine_latent(ctypes.byref(self.args), t, h, _ptr(lat)) < 0:
+            raise ValueError("oracle rejected the problem")
+        return lat
+
+    def latent_bf16(self, t, h) -> np.ndarray:
+        lat = np.empty(D, np.uint16)
+        if lib().orc_latent_bf16(ctypes.byref(self.args), t, h, _ptr(lat)) < 0:
+            raise ValueError("oracle rejected the problem")
+        return lat
+
+
+# ---- scalar helpers for the pins ----------------------------------------
+
+def sane(x: float) -> float:
+    return lib().orc_sane(x)
+
+
+def bf16_round(x) -> np.ndarray:
+    x = np.asarray(x, np.float32).ravel()
+    f = lib().orc_f32_to_bf16
+    return np.array([f(float(v)) for v in x], np.uint16)
+
+
+def bf16_value(bits) -> np.ndarray:
+    bits = np.asarray(bits, np.uint16).ravel()
+    f = lib().orc_bf16_to_f32
+    return np.array([f(int(b)) for b in bits], np.float32)
+
+
+def e2m1_code(y: float) -> int:
+    return lib().orc_e2m1_code(y)
+
+
+def e2m1_value(code: int) -> float:
+    return lib().orc_e2m1_value(code)
+
+
+def e8m0_value(code: int) -> float:
+    return lib().orc_e8m0_value(code)
+
+
+def mx_scale_code(blk_bits) -> int:
+    blk = np.ascontiguousarray(blk_bits, np.uint16)
+    assert blk.size == BLK
+    return lib().orc_mx_scale_code(_ptr(blk))
+
+
+def mx_quant_block(blk_bits):
+    blk = np.ascontiguousarray(blk_bits, np.uint16)
+    assert blk.size == BLK
+    codes = np.empty(BLK, np.uint8)
+    sc = ctypes.c_int()
+    lib().orc_mx_quant_block(_ptr(blk), _ptr(codes), ctypes.byref(sc))
+    return codes, sc.value
+
+
+def partial_set(t, S, P, q, spr):
+    r0, n = ctypes.c_int(), ctypes.c_int()
+    lay = lib().orc_partial_set(t, S, P, q, spr, ctypes.byref(r0), ctypes.byref(n))
+    return lay, r0.value, n.value

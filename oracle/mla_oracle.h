@@ -1,0 +1,44 @@
+/*
+ * mla_oracle.h -- interface of the CPU oracle (test infrastructure only; the
+ * CUDA library neither includes nor links it).
+ *
+ * Definition followed: the vLLM API page
+ * "vllm.models.kimi_k3.amd.specialized_decode.mono.attention.mla_back",
+ * functions sane, combine_ranks, combine_splits, stage_combine, stage_uv and
+ * mla_post.  All strides are in elements.
+ */
+#ifndef MLA_ORACLE_H
+#define MLA_ORACLE_H
+#include <stdint.h>
+
+typedef struct {
+  int S, S_out, H;    /* tokens of o, rows of out, heads                    */
+  int P, q, spr;      /* partials, queries per request, splits per request   */
+  const uint16_t *o;  /* bf16 [P, S, H, 512]                                 */
+  int64_t o_sp, o_st, o_sh;
+  const float *lse;   /* f32 [P, S, H]; unused when P == 1                   */
+  int64_t l_sp, l_st, l_sh;
+  const void *w_v;    /* bf16 [H,128,512] (w_fmt 0) or u8 [H,128,256] (1)    */
+  int64_t w_sh, w_sv;
+  const uint8_t *w_scale; /* e8m0 [H,128,16], w_fmt 1 only                   */
+  int64_t s_sh, s_sv;
+  int w_fmt;
+  const uint16_t *gate; /* bf16 [S, H*128] dense                            */
+} orc_args;
+
+float orc_bf16_to_f32(uint16_t b);
+uint16_t orc_f32_to_bf16(float f);
+float orc_e2m1_value(int code);
+float orc_e8m0_value(int code);
+int orc_e2m1_code(float y);
+int orc_mx_scale_code(const uint16_t *blk);
+void orc_mx_quant_block(const uint16_t *blk, uint8_t *codes, int *scale_code);
+float orc_sane(float x);
+int orc_partial_set(int t, int S, int P, int q, int spr, int *r0, int *n);
+int orc_combine_latent(const orc_args *a, int t, int h, float *lat);
+int orc_latent_bf16(const orc_args *a, int t, int h, uint16_t *latb);
+int orc_row(const orc_args *a, int t, int h, uint16_t *seg);
+int orc_rows(const orc_args *a, int n, const int *ts, const int *hs, uint16_t *segs);
+int orc_mla_combine_uv(const orc_args *a, uint16_t *out);
+
+#endif
