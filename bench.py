@@ -1,0 +1,379 @@
+"""Benchmark of the MLA decode post-attention stage on GB300.
+
+One step = one call of the whole stage (LSE combine -> MXFP4 latents -> W_UV
+-> gate) over the large multi-token-prediction batch: 1024 requests x q=4
+(S=4096 tokens), 96 heads, 4 splits per request (compact [4, 4096, 96, 512]
+bf16 partials, lse with 2% -inf), MXFP4 W_V.  It is the largest single-GPU
+workload of the recipe and the one that runs every step of the path.
+
+Prints one JSON line.  ``value`` is tokens/s over all ranks with the inputs
+resident in HBM (device-timed with CUDA events on the launching stream);
+``e2e`` is the same metric through the Python binding with the step's inputs
+copied from pinned host memory and the output copied back inside the timed
+region.  ``--impl reference`` times the CPU oracle instead (bounded samples
+of the same workload).
+
+Multi-GPU: the stage has no exchange step on one GPU's data, so N > 1 runs N
+independent replicas (one per rank, launched by torch.distributed.run) and
+``value`` sums their tokens over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "combine+W_UV tokens/s and achieved HBM GB/s (% of GB300 roofline)"
+DEFAULT_WORKLOAD = "mtp_mxfp4"
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6800.0), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mla_decode_attention_lse_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profile(workload: str, kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(f"{workload}/{kernel}")
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except FileNotFoundError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t_start: float | None = None):
+        rows = []
+        if self.path and os.path.exists(self.path):
+            with open(self.path) as f:
+                for line in f:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws, backend):
+    import torch.distributed as dist
+
+    if ws > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend)
+    return dist
+
+
+def host_copy_inputs(inp):
+    import torch
+
+    pin = {}
+    for k in ("o", "lse", "gate"):
+        if inp[k] is not None:
+            t = torch.empty(inp[k].shape, dtype=inp[k].dtype, pin_memory=True)
+            t.copy_(inp[k])
+            pin[k] = t
+    return pin
+
+
+def oracle_sample_rate(inp, budget_s: float, rows_hint: int | None = None):
+    """Time the oracle (as it stands, one thread) on a bounded sample of the
+    workload's (t, h) rows; returns (tokens/s, rows timed, seconds)."""
+    import numpy as np
+
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle
+    from parity_util import host_inputs, oracle_problem
+
+    host = host_inputs(inp)
+    pr = oracle_problem(oracle, inp, host)
+    rng = np.random.default_rng(0)
+    S, H = inp["S"], inp["H"]
+    # calibrate on a few rows, then size the sample to the budget
+    cal = 8
+    t0 = time.perf_counter()
+    pr.rows(rng.integers(0, S, cal), rng.integers(0, H, cal))
+    per_row = (time.perf_counter() - t0) / cal
+    n = rows_hint or max(H, int(budget_s / max(per_row, 1e-6)))
+    ts = np.repeat(rng.integers(0, S, (n + H - 1) // H), H)[:n]
+    hs = np.tile(np.arange(H), (n + H - 1) // H)[:n]
+    t0 = time.perf_counter()
+    pr.rows(ts, hs)
+    dt = time.perf_counter() - t0
+    return (n / H) / dt, n, dt, pr, per_row
+
+
+def run_reference(args):
+    """The oracle on the host cores, on bounded samples of the workload."""
+    import torch
+
+    ws, rank, _ = dist_env()
+    if ws > 1:
+        dist = init_dist(ws, "gloo")
+        if rank != 0:
+            dist.barrier()
+            return
+    from mla_decode_attention_lse_gb300 import synth
+
+    inp = synth.make(args.workload, device="cpu")
+    S, H = inp["S"], inp["H"]
+    # per-step sample sized so the whole run stays within ~2 minutes
+    _, _, _, pr, per_row = oracle_sample_rate(inp, 0.0, rows_hint=H)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    rows = max(1, int(budget / max(per_row, 1e-6)))
+    import numpy as np
+
+    rng = np.random.default_rng(1)
+    for _ in range(args.warmup):
+        pr.rows(rng.integers(0, S, rows), rng.integers(0, H, rows))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        pr.rows(rng.integers(0, S, rows), rng.integers(0, H, rows))
+    dt = time.perf_counter() - t0
+    value = rows * args.steps / H / dt
+    sample = f"{rows} random (t, h) rows per step of {args.workload} (S={S}, H={H})"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "S": S, "H": H, "P": inp["P"], "w_fmt": inp["w_fmt"]},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def run_gpu(args):
+    import torch
+
+    import mla_decode_attention_lse_gb300 as m
+    from mla_decode_attention_lse_gb300 import synth
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = init_dist(ws, "nccl") if ws > 1 else None
+    dev = torch.device("cuda", local)
+    m.load_library()
+
+    inp = synth.make(args.workload, device=dev, seed=synth.WORKLOADS[args.workload].seed + rank)
+    S, H, S_out = inp["S"], inp["H"], inp["S_out"]
+    out = torch.empty(S_out, H * 128, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    call = lambda: m.mla_combine_uv(inp["o"], inp["lse"], inp["q"], inp["spr"], inp["w_v"],
+                                    inp["w_fmt"], inp["gate"], out, w_scale=inp["w_scale"],
+                                    stream=stream)
+    a = m.make_args(inp["o"], inp["lse"], inp["q"], inp["spr"], inp["w_v"], inp["w_fmt"],
+                    inp["gate"], out, inp["w_scale"])
+    plan = m.mla_combine_uv_plan(a)
+    kname = "tc" if plan["kernel"] == m.MLA_KERNEL_TC else "simt"
+    nbytes = synth.algorithmic_bytes(inp)
+
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    assert m.mla_combine_uv_status(stream) == m.MLA_OK
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall0 = time.perf_counter()
+        for i in range(args.steps):
+            starts[i].record(stream)
+            call()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    if dist:
+        dist.barrier()
+    kern_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = starts[0].elapsed_time(ends[-1])
+    clocks = clk.summary()
+    assert m.mla_combine_uv_status(stream) == m.MLA_OK
+
+    # max over ranks of the timed region
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if dist:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = float(t.item())
+    value = S * args.steps * ws / (total_ms / 1e3)
+    avg_kern_s = statistics.mean(kern_ms) / 1e3
+    peak, peak_kind = load_peaks()
+    achieved = nbytes / avg_kern_s / 1e9
+
+    # end to end: pinned host inputs -> device, the call, output -> host
+    pin = host_copy_inputs(inp)
+    out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    dev_bufs = {k: torch.empty_like(inp[k]) for k in pin}
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        for k in pin:
+            dev_bufs[k].copy_(pin[k], non_blocking=True)
+        m.mla_combine_uv(dev_bufs["o"], dev_bufs.get("lse"), inp["q"], inp["spr"], inp["w_v"],
+                         inp["w_fmt"], dev_bufs["gate"], out, w_scale=inp["w_scale"], stream=stream)
+        out_host.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
+    if dist:
+        dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
+    e2e_value = S * e2e_steps * ws / (float(e2e_ms.item()) / 1e3)
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    line = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and ws == 1:
+            host_inp = {k: (v.cpu() if hasattr(v, "cpu") else v) for k, v in inp.items()}
+            rate, n, dt, _, _ = oracle_sample_rate(host_inp, args.cpu_budget)
+            cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                   "sample": f"{n} (t, h) rows ({n // H} tokens x {H} heads) of the same "
+                             f"workload, single-threaded oracle, {dt:.1f} s"}
+        wl = synth.WORKLOADS[args.workload]
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": f"{args.workload}: {wl.S // wl.q} requests x q={wl.q} "
+                                   f"(S={S}), H={H}, {inp['spr']} splits per request, "
+                                   f"P={inp['P']} compact, "
+                                   f"{'MXFP4' if inp['w_fmt'] else 'bf16'} W_V",
+                       "S": S, "H": H, "P": inp["P"], "w_fmt": ["bf16", "mxfp4"][inp["w_fmt"]],
+                       "parallelism": f"replicas x{ws}", "kernel": kname,
+                       "tile_tokens": plan["tile_tokens"], "grid": plan["grid"],
+                       "l2": "inputs 1.8 GB per step, larger than L2: no flush"},
+            "achieved_gbs": achieved,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": peak_kind,
+                         "traffic": traffic_from_profile(args.workload, kname),
+                         "algorithmic_bytes": nbytes},
+            "tensor": {"tflops": synth.flops(inp) / avg_kern_s / 1e12},
+            "kernel_ms": {"mean": statistics.mean(kern_ms), "min": min(kern_ms),
+                          "max": max(kern_ms)},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "wall_s": t_wall,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,164 @@
+/*
+ * mla_combine_uv.h -- C ABI of the GB300 (sm_103a) MLA decode post-attention
+ * stage: LSE-weighted merge of partial attention outputs, bf16 or MXFP4
+ * rounding of the merged latents, per-head W_UV up-projection, gate.
+ *
+ * The operation is the one the vLLM API page
+ * "vllm.models.kimi_k3.amd.specialized_decode.mono.attention.mla_back"
+ * defines (module docstring; functions sane, combine_ranks, combine_splits,
+ * stage_combine, stage_uv, wv_loads, host_args, mla_post).  For every token
+ * t < S and head h:
+ *
+ *   R(t)  = the partials token t merges (see "Layouts" below)
+ *   l_r   = sane(lse[r, t, h])            NaN and +inf become -inf
+ *   m     = max_r l_r  (0 if that is -inf)
+ *   e_r   = 2^((l_r - m) * log2 e)        (lse is a natural log)
+ *   w_r   = 0 if e_r == 0 or sum e == 0, else e_r / sum e
+ *   lat   = bf16( sum_{r : w_r != 0} w_r * o[r, t, h, :] )   fp32 sum
+ *   x     = lat (bf16 weights) or MXFP4(lat) (MXFP4 weights: per 32-wide
+ *           block an E8M0 scale 2^(floor(log2 amax) - 2), E2M1 elements
+ *           rounded to nearest even, saturating at 6)
+ *   acc_v = sum_k W_V[h][v][k] * x[k]      fp32
+ *   out[t, h*128 + v] = bf16( bf16(acc_v) * gate[t, h*128 + v] )
+ *
+ * and out[t, :] = 0 for S <= t < S_out.
+ *
+ * Layouts (chosen by P):
+ *   P == 1                         passthrough: lat = o[0, t, h, :] as is;
+ *                                  lse is ignored and may be NULL.
+ *   P == splits_per_request        compact / stacked partials: every token
+ *                                  merges partials 0 .. P-1.
+ *   P == (S / q) * splits_per_request, S % q == 0
+ *                                  request-major split-KV partials: token t
+ *                                  merges (t/q)*spr .. (t/q)*spr + spr - 1.
+ *   anything else                  MLA_ERR_LAYOUT.
+ *
+ * Ownership: the caller owns every buffer; the library allocates nothing per
+ * call.  All pointers are DEVICE pointers of the current CUDA device except
+ * where a field says otherwise.  Calls are asynchronous on `stream` (a
+ * cudaStream_t passed as void*; NULL is the legacy default stream).
+ * Validation errors return before anything is launched and leave `out`
+ * untouched.  `out` must not overlap any input.
+ */
+#ifndef MLA_COMBINE_UV_H
+#define MLA_COMBINE_UV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MLA_ABI_VERSION 1
+
+/* W_V storage format. */
+enum {
+  MLA_W_BF16 = 0,  /* w_v: bf16 [H, 128, 512]                                  */
+  MLA_W_MXFP4 = 1  /* w_v: u8 [H, 128, 256] E2M1 pairs (element 2i in the low
+                      nibble of byte i); w_scale: u8 [H, 128, 16] E8M0, one per
+                      32 elements along K                                      */
+};
+
+/* Status codes. */
+enum {
+  MLA_OK = 0,
+  MLA_ERR_NULL = 1,    /* a required pointer is NULL                          */
+  MLA_ERR_SHAPE = 2,   /* S < 0, S_out < S, H < 1, P < 1, q < 1, spr < 0, or a
+                          size too large for 32-bit token / unit indexing     */
+  MLA_ERR_STRIDE = 3,  /* a stride is not a multiple of 8 elements (16 bytes)
+                          where 16-byte vector or TMA access needs it        */
+  MLA_ERR_ALIGN = 4,   /* a base pointer is not 16-byte aligned               */
+  MLA_ERR_FMT = 5,     /* w_fmt is not MLA_W_BF16 / MLA_W_MXFP4               */
+  MLA_ERR_LAYOUT = 6,  /* (P, q, splits_per_request) is not one of the layouts */
+  MLA_ERR_CUDA = 7,    /* a CUDA runtime / driver call failed                 */
+  MLA_ERR_TIMEOUT = 8, /* a kernel gave up a bounded wait (reported by
+                          mla_combine_uv_status)                              */
+  MLA_ERR_KERNEL = 9   /* the requested kernel cannot run this problem        */
+};
+
+/* Kernel selection. */
+enum {
+  MLA_KERNEL_AUTO = 0, /* pick by size (the plan says which)                  */
+  MLA_KERNEL_SIMT = 1, /* CUDA-core kernel: any P; the small-batch path       */
+  MLA_KERNEL_TC = 2    /* fused tcgen05 kernel: partials per token <= 32       */
+};
+
+typedef struct {
+  int32_t S;                  /* token rows of o (and of gate)                */
+  int32_t S_out;              /* rows of out, >= S; rows S.. are zeroed       */
+  int32_t H;                  /* heads; gate / out rows are H*128 wide        */
+  int32_t P;                  /* partials along o's first dimension           */
+  int32_t q_per_request;      /* queries per request (request-major layout)   */
+  int32_t splits_per_request; /* splits each request's tokens merge           */
+
+  const void *o;              /* bf16 [P, S, H, 512]: element (r,t,h,d) at
+                                 r*o_sp + t*o_st + h*o_sh + d; strides in
+                                 elements, multiples of 8; 16-byte aligned     */
+  int64_t o_sp, o_st, o_sh;
+
+  const float *lse;           /* f32 [P, S, H]: (r,t,h) at r*l_sp + t*l_st +
+                                 h*l_sh; natural-log LSE; may be NULL iff P==1 */
+  int64_t l_sp, l_st, l_sh;
+
+  const void *w_v;            /* W_V[h][v][k] at h*w_sh + v*w_sv + k (bf16
+                                 elements) or + k/2 (MXFP4 bytes); strides
+                                 multiples of 8 elements (bf16) / 16 bytes     */
+  int64_t w_sh, w_sv;
+  const uint8_t *w_scale;     /* E8M0 scale of (h, v, k/32) at h*s_sh + v*s_sv
+                                 + k/32 (MXFP4 only; NULL for bf16)           */
+  int64_t s_sh, s_sv;
+  int32_t w_fmt;              /* MLA_W_BF16 or MLA_W_MXFP4                   */
+
+  const void *gate;           /* bf16 [S, H*128], dense row-major            */
+  void *out;                  /* bf16 [S_out, H*128], dense row-major        */
+
+  int32_t kernel;             /* MLA_KERNEL_*; 0 = automatic                  */
+  int32_t tile_tokens;        /* tensor-core token tile (16 or 32); 0 = auto  */
+} mla_combine_uv_args;
+
+/* What a call would launch (host-side planning only). */
+typedef struct {
+  int32_t kernel;        /* MLA_KERNEL_SIMT or MLA_KERNEL_TC                  */
+  int32_t layout;        /* 0 passthrough, 1 compact, 2 request-major         */
+  int32_t n_part;        /* partials each token merges                        */
+  int32_t tile_tokens;   /* tokens per work unit                              */
+  int32_t units;         /* (head, token tile) work units                     */
+  int32_t grid;          /* CTAs launched                                     */
+  int32_t threads;       /* threads per CTA                                   */
+  int32_t smem_bytes;    /* dynamic shared memory per CTA                     */
+} mla_plan;
+
+/*
+ * mla_combine_uv -- run the stage on `stream`.
+ * Returns MLA_OK once the kernel is enqueued, or an MLA_ERR_* code (nothing
+ * launched).  Kernel-side failures (a bounded wait that gave up) are reported
+ * by mla_combine_uv_status.
+ */
+int32_t mla_combine_uv(const mla_combine_uv_args *args, void *stream);
+
+/*
+ * mla_combine_uv_plan -- validate `args` and describe the launch a call would
+ * make on a GPU with `num_sms` SMs (pass 0 to ask the current device).
+ * Pure host logic when num_sms > 0: no CUDA call is made.
+ */
+int32_t mla_combine_uv_plan(const mla_combine_uv_args *args, int32_t num_sms, mla_plan *plan);
+
+/*
+ * mla_combine_uv_status -- synchronise `stream`, then read and clear the
+ * device-side error word of the current device.  Returns MLA_OK,
+ * MLA_ERR_TIMEOUT (a kernel abandoned a bounded wait; its output is
+ * undefined) or MLA_ERR_CUDA.
+ */
+int32_t mla_combine_uv_status(void *stream);
+
+/* A short English description of a status code (static storage). */
+const char *mla_status_str(int32_t status);
+
+/* MLA_ABI_VERSION of the loaded library. */
+int32_t mla_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_COMBINE_UV_H */

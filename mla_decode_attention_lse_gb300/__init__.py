@@ -1,0 +1,198 @@
+"""GB300 (sm_103a) MLA decode post-attention stage: LSE combine -> W_UV -> gate.
+
+A thin ctypes binding of ``libmla_combine_uv.so`` (C ABI in
+``include/mla_combine_uv.h``).  It only marshals arguments: every step of the
+computation runs in the library's CUDA kernels.  PyTorch supplies device
+memory and the current stream.  There is no CPU fallback: if the library is
+missing, importing the binding's functions raises.
+
+The operation is the one of the vLLM page
+"vllm.models.kimi_k3.amd.specialized_decode.mono.attention.mla_back"
+(``mla_post``: dcp_a2a_lse_reduce -> _v_up_proj -> gate).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmla_combine_uv.so")
+
+MLA_W_BF16 = 0
+MLA_W_MXFP4 = 1
+MLA_KERNEL_AUTO = 0
+MLA_KERNEL_SIMT = 1
+MLA_KERNEL_TC = 2
+
+MLA_OK = 0
+MLA_ERR_NULL = 1
+MLA_ERR_SHAPE = 2
+MLA_ERR_STRIDE = 3
+MLA_ERR_ALIGN = 4
+MLA_ERR_FMT = 5
+MLA_ERR_LAYOUT = 6
+MLA_ERR_CUDA = 7
+MLA_ERR_TIMEOUT = 8
+MLA_ERR_KERNEL = 9
+
+EXPORTED_SYMBOLS = ("mla_combine_uv", "mla_combine_uv_plan", "mla_combine_uv_status",
+                    "mla_status_str", "mla_abi_version")
+
+
+class MlaError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: status {status} ({mla_status_str(status)})" if what else
+                         f"status {status} ({mla_status_str(status)})")
+
+
+class Args(ctypes.Structure):
+    """Mirror of ``mla_combine_uv_args``."""
+    _fields_ = [
+        ("S", ctypes.c_int32), ("S_out", ctypes.c_int32), ("H", ctypes.c_int32),
+        ("P", ctypes.c_int32), ("q_per_request", ctypes.c_int32),
+        ("splits_per_request", ctypes.c_int32),
+        ("o", ctypes.c_void_p), ("o_sp", ctypes.c_int64), ("o_st", ctypes.c_int64),
+        ("o_sh", ctypes.c_int64),
+        ("lse", ctypes.c_void_p), ("l_sp", ctypes.c_int64), ("l_st", ctypes.c_int64),
+        ("l_sh", ctypes.c_int64),
+        ("w_v", ctypes.c_void_p), ("w_sh", ctypes.c_int64), ("w_sv", ctypes.c_int64),
+        ("w_scale", ctypes.c_void_p), ("s_sh", ctypes.c_int64), ("s_sv", ctypes.c_int64),
+        ("w_fmt", ctypes.c_int32),
+        ("gate", ctypes.c_void_p), ("out", ctypes.c_void_p),
+        ("kernel", ctypes.c_int32), ("tile_tokens", ctypes.c_int32),
+    ]
+
+
+class Plan(ctypes.Structure):
+    """Mirror of ``mla_plan``."""
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("kernel", "layout", "n_part", "tile_tokens", "units", "grid", "threads",
+                 "smem_bytes")]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+_lib = None
+
+
+def load_library(path: str | None = None):
+    """Load the CUDA library (built in-tree by ``build.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise ImportError(
+            f"{path} is missing: build it with `python -m mla_decode_attention_lse_gb300.build` "
+            "(there is no CPU fallback)")
+    L = ctypes.CDLL(path)
+    L.mla_combine_uv.restype = ctypes.c_int32
+    L.mla_combine_uv.argtypes = [ctypes.POINTER(Args), ctypes.c_void_p]
+    L.mla_combine_uv_plan.restype = ctypes.c_int32
+    L.mla_combine_uv_plan.argtypes = [ctypes.POINTER(Args), ctypes.c_int32, ctypes.POINTER(Plan)]
+    L.mla_combine_uv_status.restype = ctypes.c_int32
+    L.mla_combine_uv_status.argtypes = [ctypes.c_void_p]
+    L.mla_status_str.restype = ctypes.c_char_p
+    L.mla_status_str.argtypes = [ctypes.c_int32]
+    L.mla_abi_version.restype = ctypes.c_int32
+    L.mla_abi_version.argtypes = []
+    _lib = L
+    return L
+
+
+def mla_status_str(status: int) -> str:
+    return load_library().mla_status_str(status).decode()
+
+
+def mla_abi_version() -> int:
+    return load_library().mla_abi_version()
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def make_args(o, lse, q_per_request, splits_per_request, w_v, w_fmt, gate, out, w_scale=None,
+              kernel=MLA_KERNEL_AUTO, tile_tokens=0) -> Args:
+    """Fill ``mla_combine_uv_args`` from tensors (pointers and element strides)."""
+    P, S, H, _ = o.shape
+    a = Args()
+    a.S, a.S_out, a.H, a.P = S, out.shape[0], H, P
+    a.q_per_request, a.splits_per_request = q_per_request, splits_per_request
+    a.o = _ptr(o)
+    a.o_sp, a.o_st, a.o_sh = o.stride(0), o.stride(1), o.stride(2)
+    if lse is not None:
+        a.lse = _ptr(lse)
+        a.l_sp, a.l_st, a.l_sh = lse.stride(0), lse.stride(1), lse.stride(2)
+    a.w_v = _ptr(w_v)
+    a.w_sh, a.w_sv = w_v.stride(0), w_v.stride(1)
+    if w_scale is not None:
+        a.w_scale = _ptr(w_scale)
+        a.s_sh, a.s_sv = w_scale.stride(0), w_scale.stride(1)
+    a.w_fmt = w_fmt
+    a.gate = _ptr(gate)
+    a.out = _ptr(out)
+    a.kernel, a.tile_tokens = kernel, tile_tokens
+    return a
+
+
+def _check_tensors(o, lse, w_v, w_scale, gate, out, w_fmt):
+    import torch
+
+    if o.dtype != torch.bfloat16 or o.dim() != 4 or o.shape[3] != 512 or o.stride(3) != 1:
+        raise ValueError("o must be bf16 [P, S, H, 512] with a unit-stride last dimension")
+    if lse is not None and (lse.dtype != torch.float32 or lse.dim() != 3):
+        raise ValueError("lse must be float32 [P, S, H]")
+    if gate.dtype != torch.bfloat16 or not gate.is_contiguous():
+        raise ValueError("gate must be a dense bf16 [S, H*128] tensor")
+    if out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a dense bf16 [S_out, H*128] tensor")
+    if w_fmt == MLA_W_BF16 and (w_v.dtype != torch.bfloat16 or w_v.stride(-1) != 1):
+        raise ValueError("bf16 W_V must be bf16 [H, 128, 512] with a unit-stride last dimension")
+    if w_fmt == MLA_W_MXFP4 and (w_v.dtype != torch.uint8 or w_scale is None
+                                 or w_scale.dtype != torch.uint8):
+        raise ValueError("MXFP4 W_V must be uint8 [H, 128, 256] with uint8 [H, 128, 16] scales")
+
+
+def mla_combine_uv(o, lse, q_per_request, splits_per_request, w_v, w_fmt, gate, out,
+                   w_scale=None, stream=None, kernel=MLA_KERNEL_AUTO, tile_tokens=0) -> None:
+    """Run the stage on CUDA tensors; writes ``out`` [S_out, H*128] bf16.
+
+    o [P, S, H, 512] bf16; lse [P, S, H] f32 (None allowed when P == 1);
+    w_v bf16 [H, 128, 512] (w_fmt 0) or uint8 [H, 128, 256] + w_scale uint8
+    [H, 128, 16] (w_fmt 1); gate [S, H*128] bf16.  Asynchronous on ``stream``
+    (default: PyTorch's current stream).
+    """
+    import torch
+
+    _check_tensors(o, lse, w_v, w_scale, gate, out, w_fmt)
+    if stream is None:
+        stream = torch.cuda.current_stream(o.device)
+    s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    a = make_args(o, lse, q_per_request, splits_per_request, w_v, w_fmt, gate, out, w_scale,
+                  kernel, tile_tokens)
+    st = load_library().mla_combine_uv(ctypes.byref(a), ctypes.c_void_p(s))
+    if st != MLA_OK:
+        raise MlaError(st, "mla_combine_uv")
+
+
+def mla_combine_uv_plan(args: Args, num_sms: int = 0) -> dict:
+    """Validate ``args`` and return the launch plan (no GPU needed when
+    ``num_sms`` > 0).  Raises ``MlaError`` on a validation error."""
+    pl = Plan()
+    st = load_library().mla_combine_uv_plan(ctypes.byref(args), num_sms, ctypes.byref(pl))
+    if st != MLA_OK:
+        raise MlaError(st, "mla_combine_uv_plan")
+    return pl.as_dict()
+
+
+def mla_combine_uv_status(stream=None) -> int:
+    """Synchronise ``stream`` and return (and clear) the device error status."""
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    return load_library().mla_combine_uv_status(ctypes.c_void_p(s))

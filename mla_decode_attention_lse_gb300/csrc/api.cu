@@ -1,0 +1,265 @@
+// api.cu -- the C ABI of libmla_combine_uv: validation, planning, dispatch.
+//
+// Host-side conventions follow the launcher of the vLLM page
+// "vllm.models.kimi_k3.amd.specialized_decode.mono.attention.mla_back"
+// (host_args / mla_post): strided o / lse rows and heads with a unit-stride
+// last dimension, dense gate / core, launch on the caller's stream, every
+// check done before anything is launched.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "../../include/mla_combine_uv.h"
+#include "kernels.h"
+
+namespace {
+
+using mla::KParams;
+
+// Device-side error word, one per device context (first error wins).
+__device__ int g_mla_err_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int *g_err_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+bool aligned(const void *ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+// Validate and plan.  Pure host logic when num_sms > 0.
+int32_t plan_impl(const mla_combine_uv_args *a, int32_t num_sms, mla_plan *pl, KParams *kp) {
+  if (!a || !pl) return MLA_ERR_NULL;
+  if (a->w_fmt != MLA_W_BF16 && a->w_fmt != MLA_W_MXFP4) return MLA_ERR_FMT;
+  if (a->S < 0 || a->S_out < a->S || a->H < 1 || a->H > 65535 || a->P < 1 || a->q_per_request < 1 ||
+      a->splits_per_request < 0)
+    return MLA_ERR_SHAPE;
+  if ((int64_t)a->S_out * a->H * 128 >= (int64_t)1 << 40) return MLA_ERR_SHAPE;
+
+  // layout, chosen by P
+  int layout, n_part;
+  const int S = a->S, q = a->q_per_request, spr = a->splits_per_request;
+  if (a->P == 1) {
+    layout = mla::kPassthrough;
+    n_part = 1;
+  } else if (spr > 0 && a->P == spr) {
+    layout = mla::kCompact;
+    n_part = spr;
+  } else if (spr > 0 && S % q == 0 && (int64_t)a->P == (int64_t)(S / q) * spr) {
+    layout = mla::kRequestMajor;
+    n_part = spr;
+  } else {
+    return MLA_ERR_LAYOUT;
+  }
+
+  // pointers (only those the call will touch)
+  if (a->S_out > 0 && !a->out) return MLA_ERR_NULL;
+  if (S > 0) {
+    if (!a->o || !a->w_v || !a->gate) return MLA_ERR_NULL;
+    if (a->P > 1 && !a->lse) return MLA_ERR_NULL;
+    if (a->w_fmt == MLA_W_MXFP4 && !a->w_scale) return MLA_ERR_NULL;
+    if (!aligned(a->o, 16) || !aligned(a->w_v, 16) || !aligned(a->gate, 16)) return MLA_ERR_ALIGN;
+    if (a->lse && !aligned(a->lse, 4)) return MLA_ERR_ALIGN;
+    // 16-byte vector rows of o; strides in elements
+    if (a->o_st < 0 || a->o_sh < 0 || a->o_sp < 0) return MLA_ERR_STRIDE;
+    if (a->o_st % 8 || a->o_sh % 8 || (a->P > 1 && a->o_sp % 8)) return MLA_ERR_STRIDE;
+    if (a->P > 1 && (a->l_sp < 0 || a->l_st < 0 || a->l_sh < 0)) return MLA_ERR_STRIDE;
+    if (a->w_sh < 0 || a->w_sv < 0) return MLA_ERR_STRIDE;
+    if (a->w_fmt == MLA_W_BF16 && (a->w_sh % 8 || a->w_sv % 8)) return MLA_ERR_STRIDE;
+    if (a->w_fmt == MLA_W_MXFP4 && (a->w_sh % 16 || a->w_sv % 16)) return MLA_ERR_STRIDE;
+    if (a->w_fmt == MLA_W_MXFP4 && (a->s_sh < 0 || a->s_sv < 0)) return MLA_ERR_STRIDE;
+  }
+  if (a->S_out > 0 && !aligned(a->out, 16)) return MLA_ERR_ALIGN;
+
+  // kernel choice
+  int kernel = a->kernel;
+  if (kernel != MLA_KERNEL_AUTO && kernel != MLA_KERNEL_SIMT && kernel != MLA_KERNEL_TC) return MLA_ERR_KERNEL;
+  if (a->tile_tokens != 0 && a->tile_tokens != 16 && a->tile_tokens != 32) return MLA_ERR_KERNEL;
+  if (kernel == MLA_KERNEL_TC && n_part > mla::kTcMaxPart) return MLA_ERR_KERNEL;
+  if (kernel == MLA_KERNEL_AUTO) kernel = (n_part <= mla::kTcMaxPart && S >= 16) ? MLA_KERNEL_TC : MLA_KERNEL_SIMT;
+  if (S == 0) kernel = MLA_KERNEL_SIMT;  // nothing to merge: zero rows only
+  if (kernel == MLA_KERNEL_SIMT && mla::simt_smem_bytes(n_part) > 200 * 1024) return MLA_ERR_KERNEL;
+
+  std::memset(pl, 0, sizeof *pl);
+  pl->kernel = kernel;
+  pl->layout = layout;
+  pl->n_part = n_part;
+  if (kernel == MLA_KERNEL_SIMT) {
+    pl->tile_tokens = 8;
+    pl->units = a->H * ((a->S_out + 7) / 8);
+    pl->grid = pl->units;
+    pl->threads = 256;
+    pl->smem_bytes = (int32_t)mla::simt_smem_bytes(n_part);
+  } else {
+    if (num_sms <= 0) return MLA_ERR_SHAPE;
+    int tile = a->tile_tokens;
+    if (tile == 0) tile = ((int64_t)a->H * ((S + 31) / 32) >= num_sms) ? 32 : 16;
+    pl->tile_tokens = tile;
+    pl->units = a->H * ((S + tile - 1) / tile);
+    pl->grid = pl->units < num_sms ? pl->units : num_sms;
+    pl->threads = mla::kTcThreads;
+    pl->smem_bytes = (int32_t)mla::tc_smem_bytes(tile);
+  }
+
+  if (kp) {
+    KParams &k = *kp;
+    std::memset(&k, 0, sizeof k);
+    k.S = S;
+    k.S_out = a->S_out;
+    k.H = a->H;
+    k.layout = layout;
+    k.n_part = n_part;
+    k.q = q;
+    k.spr = spr;
+    k.o = static_cast<const uint16_t *>(a->o);
+    k.o_sp = a->o_sp;
+    k.o_st = a->o_st;
+    k.o_sh = a->o_sh;
+    k.lse = a->lse;
+    k.l_sp = a->l_sp;
+    k.l_st = a->l_st;
+    k.l_sh = a->l_sh;
+    k.w_v = a->w_v;
+    k.w_sh = a->w_sh;
+    k.w_sv = a->w_sv;
+    k.w_scale = a->w_scale;
+    k.s_sh = a->s_sh;
+    k.s_sv = a->s_sv;
+    k.w_fmt = a->w_fmt;
+    k.gate = static_cast<const uint16_t *>(a->gate);
+    k.out = static_cast<uint16_t *>(a->out);
+    k.tile = pl->tile_tokens;
+    k.tiles_per_head = (kernel == MLA_KERNEL_SIMT) ? (a->S_out + 7) / 8 : (S + pl->tile_tokens - 1) / pl->tile_tokens;
+    k.units = pl->units;
+  }
+  return MLA_OK;
+}
+
+// Per-device state: SM count and the error word's device address.
+int32_t device_state(int *dev_out, int *sms_out, int **err_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MLA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[dev]) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MLA_ERR_CUDA;
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_mla_err_word) != cudaSuccess) return MLA_ERR_CUDA;
+    g_num_sms[dev] = sms;
+    g_err_ptr[dev] = static_cast<int *>(ptr);
+  }
+  if (!g_encode) {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return MLA_ERR_CUDA;
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  *dev_out = dev;
+  *sms_out = g_num_sms[dev];
+  *err_out = g_err_ptr[dev];
+  return MLA_OK;
+}
+
+// TMA descriptor of bf16 W_V [H, 128, 512]: boxes of 64 K x 128 rows, 128-byte
+// swizzle (the layout the MMA's shared-memory descriptor expects).
+int32_t make_wv_tmap(const KParams &k, CUtensorMap *tm) {
+  cuuint64_t dims[3] = {512, 128, (cuuint64_t)k.H};
+  cuuint64_t strides[2] = {(cuuint64_t)k.w_sv * 2, (cuuint64_t)k.w_sh * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  if (k.H == 1) strides[1] = (cuuint64_t)128 * k.w_sv * 2;  // unused dimension; any legal stride
+  if (strides[1] == 0) strides[1] = 16;
+  CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(k.w_v), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t mla_abi_version(void) { return MLA_ABI_VERSION; }
+
+const char *mla_status_str(int32_t s) {
+  switch (s) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_NULL: return "a required pointer is NULL";
+    case MLA_ERR_SHAPE: return "invalid sizes";
+    case MLA_ERR_STRIDE: return "a stride is not a multiple of 16 bytes or is negative";
+    case MLA_ERR_ALIGN: return "a base pointer is not 16-byte aligned";
+    case MLA_ERR_FMT: return "unknown W_V format";
+    case MLA_ERR_LAYOUT: return "P matches neither passthrough, compact nor request-major layout";
+    case MLA_ERR_CUDA: return "a CUDA call failed";
+    case MLA_ERR_TIMEOUT: return "a kernel abandoned a bounded wait";
+    case MLA_ERR_KERNEL: return "the requested kernel cannot run this problem";
+    default: return "unknown status";
+  }
+}
+
+int32_t mla_combine_uv_plan(const mla_combine_uv_args *args, int32_t num_sms, mla_plan *plan) {
+  if (num_sms <= 0) {
+    int dev, sms;
+    int *err;
+    int32_t st = device_state(&dev, &sms, &err);
+    if (st != MLA_OK) return st;
+    num_sms = sms;
+  }
+  return plan_impl(args, num_sms, plan, nullptr);
+}
+
+int32_t mla_combine_uv(const mla_combine_uv_args *args, void *stream) {
+  int dev, sms;
+  int *err;
+  int32_t st = device_state(&dev, &sms, &err);
+  if (st != MLA_OK) return st;
+  mla_plan pl;
+  KParams kp;
+  st = plan_impl(args, sms, &pl, &kp);
+  if (st != MLA_OK) return st;
+  if (args->S_out == 0) return MLA_OK;
+  kp.err = err;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (pl.kernel == MLA_KERNEL_SIMT) {
+    e = mla::launch_simt(kp, s);
+  } else {
+    alignas(64) CUtensorMap tm;
+    std::memset(&tm, 0, sizeof tm);
+    if (kp.w_fmt == MLA_W_BF16) {
+      st = make_wv_tmap(kp, &tm);
+      if (st != MLA_OK) return st;
+    }
+    e = mla::launch_tc(kp, &tm, pl.grid, s);
+  }
+  return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int32_t mla_combine_uv_status(void *stream) {
+  int dev, sms;
+  int *err;
+  int32_t st = device_state(&dev, &sms, &err);
+  if (st != MLA_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MLA_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, err, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_CUDA;
+  if (word != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return MLA_ERR_CUDA;
+    return MLA_ERR_TIMEOUT;
+  }
+  return MLA_OK;
+}
+
+}  // extern "C"

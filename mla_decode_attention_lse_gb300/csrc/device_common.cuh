@@ -1,0 +1,256 @@
+// device_common.cuh -- shared device helpers of the sm_103a kernels: number
+// formats (bf16, E2M1, E8M0), the LSE weight rule, bounded mbarrier waits and
+// thin inline-PTX wrappers for TMA and tcgen05.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "kparams.h"
+
+namespace mla {
+
+constexpr int kD = 512;    // latent width
+constexpr int kV = 128;    // V head dim
+constexpr int kBlk = 32;   // MX block along K
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Bounded waits give up after this long and report MLA_ERR_TIMEOUT through
+// the error word; a healthy wait here lasts microseconds.
+constexpr unsigned long long kWaitNs = 500ull * 1000ull * 1000ull;
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---- number formats ------------------------------------------------------
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Two fp32 values -> packed bf16 pair (round to nearest even).
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&p);
+}
+
+__device__ __forceinline__ float round_bf16(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// E8M0 code -> 2^(code - 127) as fp32 (code 255 -> NaN; code 0 -> 2^-127, a
+// subnormal).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t code) {
+  if (code == 255u) return __uint_as_float(0x7FC00000u);
+  if (code == 0u) return __uint_as_float(0x00400000u);
+  return __uint_as_float(code << 23);
+}
+
+// Shared MX scale code from the largest sign-cleared bf16 pattern of a block:
+// floor(log2 amax) - 2 + 127 is the exponent field minus 2 for normal values;
+// clamped below at 1 (zero and subnormal blocks); 255 (NaN) when the block
+// holds an Inf or NaN.
+__device__ __forceinline__ uint32_t mx_scale_code(uint32_t amax_bits) {
+  uint32_t ef = (amax_bits >> 7) & 0xFFu;
+  if (ef == 0xFFu) return 255u;
+  int c = (int)ef - 2;
+  return c < 1 ? 1u : (uint32_t)c;
+}
+
+// Magnitude code (0..7) of E2M1 for an already-scaled magnitude a >= 0:
+// round to nearest, ties to the even code, saturate at 6.  The decision
+// points are the midpoints 0.25, 0.75, 1.25, 1.75, 2.5, 3.5 and 5; at a tie
+// the even code wins, so the comparison is strict where the lower neighbour
+// is even and inclusive where the upper one is.
+__device__ __forceinline__ uint32_t e2m1_mag_code(float a) {
+  return (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
+         (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) +
+         (uint32_t)(a > 5.0f);
+}
+
+__device__ __forceinline__ float e2m1_mag_value(uint32_t c) {
+  // 0, .5, 1, 1.5, 2, 3, 4, 6
+  const float m = (c < 4u) ? 0.5f * (float)c : (float)(2u << ((c - 4u) >> 1)) * (1.0f + 0.5f * (float)(c & 1u));
+  return m;
+}
+
+// Quantise one bf16 value x (given as fp32) with block scale code sc and
+// return the dequantised value: +-E2M1(x / 2^(sc-127)) * 2^(sc-127).
+// The scaling by a power of two is exact (no flush-to-zero in this build).
+__device__ __forceinline__ float mx_fake_quant(float x, uint32_t sc, float scale, float inv_scale) {
+  if (sc == 255u) return __uint_as_float(0x7FC00000u);
+  float a = fabsf(x) * inv_scale;
+  uint32_t c = e2m1_mag_code(a);
+  float v = e2m1_mag_value(c) * scale;
+  return (c != 0u && signbit(x)) ? -v : v;
+}
+
+// 2^(127 - sc) for a scale code 1..254, exact (2^-127 is a subnormal).
+__device__ __forceinline__ float e8m0_inverse(uint32_t sc) {
+  int e = 127 - (int)sc;  // -127 .. 126
+  if (e >= -126) return __uint_as_float((uint32_t)(e + 127) << 23);
+  return __uint_as_float(0x00400000u);
+}
+
+// Sanitise an LSE: NaN and +inf become -inf.
+__device__ __forceinline__ float sane(float x) {
+  return (x != x || x == __int_as_float(0x7F800000)) ? __int_as_float(0xFF800000) : x;
+}
+
+// ---- mbarrier ----------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete, for at most kWaitNs.
+// Returns false (and records `code` in the error word) on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *err, int code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer() - t0 > kWaitNs) {
+      if (err) atomicCAS(err, 0, code);
+      return false;
+    }
+  }
+}
+
+// ---- proxies, TMA, tcgen05 --------------------------------------------
+
+// Make this thread's generic-proxy shared-memory writes visible to the async
+// proxy (tensor-core operand reads).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// 3-D tiled TMA load into shared memory, completing on `bar` (tx bytes).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int x, int y, int z,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 in, fp32 accumulate).
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation this thread issued so far is
+// complete.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// 32 lanes x 32 bit, 8 consecutive columns.
+__device__ __forceinline__ void tmem_ld_x8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7])
+      : "r"(taddr)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 format): K-major operand with the
+// 128-byte swizzle, rows of 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);        // start address, 16-byte units
+  d |= (uint64_t)(16u >> 4) << 16;                  // leading byte offset (unused here)
+  d |= (uint64_t)(1024u >> 4) << 32;                // stride byte offset: 8 rows x 128 B
+  d |= (uint64_t)1 << 46;                           // descriptor version (tcgen05)
+  d |= (uint64_t)2 << 61;                           // swizzle mode: 128 B
+  return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4)                      // D format: f32
+         | (1u << 7)                    // A format: bf16
+         | (1u << 10)                   // B format: bf16
+         | ((uint32_t)(N >> 3) << 17)   // N / 8
+         | ((uint32_t)(M >> 4) << 24);  // M / 16
+}
+
+// Byte offset of 16-byte chunk `c` (0..63) of row `r` in a K-major bf16 tile
+// of `rows` rows stored as 8 K-blocks of [rows x 128 B] with the 128-byte
+// swizzle (chunk j of a row lives at j ^ (r % 8)).
+__device__ __forceinline__ uint32_t sw128_offset(int r, int c, int rows) {
+  const int kb = c >> 3, j = c & 7;
+  return (uint32_t)(kb * rows * 128 + r * 128 + ((j ^ (r & 7)) << 4));
+}
+
+}  // namespace mla

@@ -1,0 +1,168 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+function ``include/mla_combine_uv.h`` declares, and its host-side validation
+and planning behave as documented (``mla_combine_uv_plan`` with an explicit
+SM count makes no CUDA call)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from mla_decode_attention_lse_gb300 import (Args, MlaError, build, load_library, make_args,
+                                            mla_combine_uv_plan)
+import mla_decode_attention_lse_gb300 as m
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SMS = 152
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return load_library()
+
+
+def declared_functions():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            src = open(os.path.join(inc, f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(mla_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert set(m.EXPORTED_SYMBOLS) <= set(names)
+    assert len(names) >= 5
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_abi_version_and_status_strings(lib):
+    assert m.mla_abi_version() == 1
+    for s in range(0, 10):
+        assert m.mla_status_str(s) and m.mla_status_str(s) != "unknown status"
+    assert m.mla_status_str(99) == "unknown status"
+
+
+def test_args_struct_layout_matches_header(lib, tmp_path):
+    # compile a probe against the header and compare every field offset
+    fields = [f for f, _ in Args._fields_]
+    prog = ["#include <stdio.h>", "#include <stddef.h>", '#include "mla_combine_uv.h"',
+            "int main(void) {", 'printf("%zu\\n", sizeof(mla_combine_uv_args));']
+    prog += [f'printf("%zu\\n", offsetof(mla_combine_uv_args, {f}));' for f in fields]
+    prog += ['printf("%zu\\n", sizeof(mla_plan));', "return 0; }"]
+    src = tmp_path / "probe.c"
+    src.write_text("\n".join(prog))
+    exe = tmp_path / "probe"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                           check=True).stdout.split()]
+    assert vals[0] == ctypes.sizeof(Args)
+    for f, off in zip(fields, vals[1:-1]):
+        assert getattr(Args, f).offset == off, f
+    assert vals[-1] == ctypes.sizeof(m.Plan)
+
+
+# ---- planning / validation without a GPU ---------------------------------
+
+ALIGNED = 1 << 20  # fake, 16-byte aligned device addresses: never dereferenced
+
+
+def args(S=64, S_out=None, H=12, P=4, q=1, spr=4, w_fmt=0, kernel=0, tile=0, **kw):
+    a = Args()
+    a.S, a.S_out, a.H, a.P = S, S if S_out is None else S_out, H, P
+    a.q_per_request, a.splits_per_request = q, spr
+    a.o, a.o_sp, a.o_st, a.o_sh = ALIGNED, S * H * 512, H * 512, 512
+    a.lse, a.l_sp, a.l_st, a.l_sh = ALIGNED * 2, S * H, H, 1
+    a.w_v = ALIGNED * 3
+    a.w_sh, a.w_sv = (128 * 512, 512) if w_fmt == 0 else (128 * 256, 256)
+    a.w_scale, a.s_sh, a.s_sv = (ALIGNED * 4, 128 * 16, 16) if w_fmt == 1 else (None, 0, 0)
+    a.w_fmt = w_fmt
+    a.gate, a.out = ALIGNED * 5, ALIGNED * 6
+    a.kernel, a.tile_tokens = kernel, tile
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def status_of(a):
+    with pytest.raises(MlaError) as e:
+        mla_combine_uv_plan(a, SMS)
+    return e.value.status
+
+
+def test_layouts(lib):
+    assert mla_combine_uv_plan(args(P=1, spr=0), SMS)["layout"] == 0
+    p = mla_combine_uv_plan(args(P=16, spr=16), SMS)
+    assert (p["layout"], p["n_part"]) == (1, 16)
+    p = mla_combine_uv_plan(args(S=64, P=1024, q=1, spr=16), SMS)
+    assert (p["layout"], p["n_part"]) == (2, 16)
+    p = mla_combine_uv_plan(args(S=8, P=12, q=2, spr=3), SMS)
+    assert (p["layout"], p["n_part"]) == (2, 3)
+    assert status_of(args(S=8, P=7, q=2, spr=3)) == m.MLA_ERR_LAYOUT
+    assert status_of(args(S=7, P=9, q=2, spr=3)) == m.MLA_ERR_LAYOUT  # S % q != 0
+    assert status_of(args(P=4, spr=0)) == m.MLA_ERR_LAYOUT
+
+
+def test_kernel_and_tile_choice(lib):
+    # tiny token counts -> CUDA-core kernel
+    assert mla_combine_uv_plan(args(S=4, H=2, P=4, q=2, spr=2), SMS)["kernel"] == m.MLA_KERNEL_SIMT
+    # decode sizes -> tensor cores, 16-token tiles when 32 would not fill the GPU
+    p = mla_combine_uv_plan(args(S=64, P=16, spr=16), SMS)
+    assert (p["kernel"], p["tile_tokens"], p["units"], p["grid"]) == (m.MLA_KERNEL_TC, 16, 48, 48)
+    # the large batch: 32-token tiles over a persistent grid of SMS CTAs
+    p = mla_combine_uv_plan(args(S=4096, H=96, P=4, q=4, spr=4), SMS)
+    assert (p["tile_tokens"], p["units"], p["grid"]) == (32, 96 * 128, SMS)
+    assert p["smem_bytes"] <= 227 * 1024
+    # more than 32 partials per token: CUDA cores only
+    assert mla_combine_uv_plan(args(P=64, spr=64), SMS)["kernel"] == m.MLA_KERNEL_SIMT
+    assert status_of(args(P=64, spr=64, kernel=m.MLA_KERNEL_TC)) == m.MLA_ERR_KERNEL
+    assert status_of(args(tile=24)) == m.MLA_ERR_KERNEL
+    assert status_of(args(kernel=7)) == m.MLA_ERR_KERNEL
+    p = mla_combine_uv_plan(args(S=0, S_out=5, kernel=m.MLA_KERNEL_TC), SMS)
+    assert p["kernel"] == m.MLA_KERNEL_SIMT  # nothing to merge: zero rows only
+
+
+def test_validation_errors(lib):
+    assert status_of(args(w_fmt=3)) == m.MLA_ERR_FMT
+    assert status_of(args(S=-1)) == m.MLA_ERR_SHAPE
+    assert status_of(args(S=8, S_out=4)) == m.MLA_ERR_SHAPE
+    assert status_of(args(H=0)) == m.MLA_ERR_SHAPE
+    assert status_of(args(q=0)) == m.MLA_ERR_SHAPE
+    assert status_of(args(o=None)) == m.MLA_ERR_NULL
+    assert status_of(args(lse=None)) == m.MLA_ERR_NULL
+    assert status_of(args(out=None)) == m.MLA_ERR_NULL
+    assert status_of(args(w_fmt=1, w_scale=None)) == m.MLA_ERR_NULL
+    assert status_of(args(o=ALIGNED + 8)) == m.MLA_ERR_ALIGN
+    assert status_of(args(out=ALIGNED + 2)) == m.MLA_ERR_ALIGN
+    assert status_of(args(o_st=12 * 512 + 4)) == m.MLA_ERR_STRIDE
+    assert status_of(args(o_sh=-512)) == m.MLA_ERR_STRIDE
+    assert status_of(args(w_sv=500)) == m.MLA_ERR_STRIDE
+    assert status_of(args(w_fmt=1, w_sv=264)) == m.MLA_ERR_STRIDE
+    # lse may be NULL only with one partial
+    mla_combine_uv_plan(args(P=1, spr=0, lse=None), SMS)
+    # nothing to read when S == 0: input pointers are not required
+    mla_combine_uv_plan(args(S=0, S_out=3, o=None, lse=None, w_v=None, gate=None), SMS)
+
+
+def test_make_args_from_strided_views(lib):
+    import torch
+
+    big = torch.zeros(2, 8, 16, 512, dtype=torch.bfloat16)
+    o = big[:, :, 4:10]  # heads strided view
+    lse = torch.zeros(2, 8, 6)
+    w = torch.zeros(6, 128, 512, dtype=torch.bfloat16)
+    gate = torch.zeros(8, 6 * 128, dtype=torch.bfloat16)
+    out = torch.zeros(8, 6 * 128, dtype=torch.bfloat16)
+    a = make_args(o, lse, 1, 2, w, 0, gate, out)
+    assert (a.P, a.S, a.H, a.S_out) == (2, 8, 6, 8)
+    assert (a.o_sp, a.o_st, a.o_sh) == (8 * 16 * 512, 16 * 512, 512)
+    assert a.o == o.data_ptr()
+    p = mla_combine_uv_plan(a, SMS)
+    assert p["layout"] == 1
