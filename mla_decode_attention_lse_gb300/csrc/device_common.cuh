@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "kparams.h"
@@ -99,6 +100,53 @@ __device__ __forceinline__ float sane(float x) {
   return (x != x || x == __int_as_float(0x7F800000)) ? __int_as_float(0xFF800000) : x;
 }
 
+// ---- packed fp32 pairs and hardware E2M1 conversions (sm_100 family) -----
+
+// Round-to-nearest packed fp32 arithmetic on (lo, hi) pairs: one rounding
+// per lane of the pair, exactly like two scalar operations.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// Two fp32 values -> an E2M1 pair (round to nearest even, saturating at +-6),
+// `hi` in the upper nibble.
+__device__ __forceinline__ uint32_t e2m1x2_from_f32(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+// An E2M1 pair (low nibble -> lo) -> two fp16 values packed as (lo, hi).
+__device__ __forceinline__ uint32_t f16x2_from_e2m1x2(uint32_t byte) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(r) : "r"(byte));
+  return r;
+}
+
+__device__ __forceinline__ float f16_lo(uint32_t h2) {
+  return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+}
+__device__ __forceinline__ float f16_hi(uint32_t h2) {
+  return __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
+}
+
 // ---- mbarrier ----------------------------------------------------------
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -145,6 +193,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *er
       return false;
     }
   }
+}
+
+// Shared-memory atomic add with acquire-release semantics at CTA scope;
+// returns the previous value.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_cta(uint32_t addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+  return old;
 }
 
 // ---- proxies, TMA, tcgen05 --------------------------------------------
@@ -212,6 +268,14 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
 
 __device__ __forceinline__ void tc_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// 32 lanes x 32 bit, 4 consecutive columns.
+__device__ __forceinline__ void tmem_ld_x4(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr)
+               : "memory");
 }
 
 // 32 lanes x 32 bit, 8 consecutive columns.
