@@ -240,9 +240,9 @@ def run_gpu(args):
     stream = torch.cuda.current_stream(dev)
     call = lambda: m.mla_combine_uv(inp["o"], inp["lse"], inp["q"], inp["spr"], inp["w_v"],
                                     inp["w_fmt"], inp["gate"], out, w_scale=inp["w_scale"],
-                                    stream=stream)
+                                    stream=stream, kernel=args.kernel, tile_tokens=args.tile)
     a = m.make_args(inp["o"], inp["lse"], inp["q"], inp["spr"], inp["w_v"], inp["w_fmt"],
-                    inp["gate"], out, inp["w_scale"])
+                    inp["gate"], out, inp["w_scale"], kernel=args.kernel, tile_tokens=args.tile)
     plan = m.mla_combine_uv_plan(a)
     kname = "tc" if plan["kernel"] == m.MLA_KERNEL_TC else "simt"
     nbytes = synth.algorithmic_bytes(inp)
@@ -292,7 +292,8 @@ def run_gpu(args):
         for k in pin:
             dev_bufs[k].copy_(pin[k], non_blocking=True)
         m.mla_combine_uv(dev_bufs["o"], dev_bufs.get("lse"), inp["q"], inp["spr"], inp["w_v"],
-                         inp["w_fmt"], dev_bufs["gate"], out, w_scale=inp["w_scale"], stream=stream)
+                         inp["w_fmt"], dev_bufs["gate"], out, w_scale=inp["w_scale"], stream=stream,
+                         kernel=args.kernel, tile_tokens=args.tile)
         out_host.copy_(out, non_blocking=True)
 
     e2e_step()
@@ -366,6 +367,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA cores, 2 tensor cores")
+    ap.add_argument("--tile", type=int, default=0, help="tensor-core token tile (16/32; 0 auto)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

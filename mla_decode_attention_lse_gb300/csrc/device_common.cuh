@@ -100,6 +100,13 @@ __device__ __forceinline__ float sane(float x) {
   return (x != x || x == __int_as_float(0x7F800000)) ? __int_as_float(0xFF800000) : x;
 }
 
+// Per-half unsigned maximum of two packed 16-bit pairs.
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 // ---- packed fp32 pairs and hardware E2M1 conversions (sm_100 family) -----
 
 // Round-to-nearest packed fp32 arithmetic on (lo, hi) pairs: one rounding

@@ -69,9 +69,9 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int
 // dequantised value, returned as bf16.
 __device__ __forceinline__ uint4 mx_chunk(uint4 x) {
   uint32_t u[4] = {x.x, x.y, x.z, x.w};
-  uint32_t am = 0;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) am = max(am, max(u[q] & 0x7FFFu, (u[q] >> 16) & 0x7FFFu));
+  uint32_t am2 = max_u16x2(max_u16x2(u[0] & 0x7FFF7FFFu, u[1] & 0x7FFF7FFFu),
+                           max_u16x2(u[2] & 0x7FFF7FFFu, u[3] & 0x7FFF7FFFu));
+  uint32_t am = max(am2 & 0xFFFFu, am2 >> 16);
   am = max(am, __shfl_xor_sync(0xffffffffu, am, 1));
   am = max(am, __shfl_xor_sync(0xffffffffu, am, 2));
   const uint32_t sc = mx_scale_code(am);
@@ -92,12 +92,12 @@ template <int BN, int WFMT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tmap_w) {
   constexpr int TPW = BN / kWorkers;       // tokens per warp per unit
-  constexpr int JB = 8 / TPW;              // partials per load batch (16 x 16 B in flight per lane)
-  constexpr int CPW = BN / 4;              // TMEM columns each worker warp drains
+  constexpr int JB = 4 / TPW;              // partials per batch: 4 rows (8 x 16 B per lane)
+  constexpr int CPW = BN / 4;              // TMEM columns each warp drains
   constexpr uint32_t kBBytes = BN * 1024u; // one latent buffer (BN x 512 bf16)
   constexpr uint32_t kCols = (2 * BN < 32) ? 32u : (uint32_t)(2 * BN);
   constexpr uint32_t kIdesc = idesc_bf16(128, BN);
-  static_assert(TPW >= 1 && BN % kWorkers == 0, "tile must split over the worker warps");
+  static_assert(TPW >= 1 && BN % kWorkers == 0 && JB >= 1, "tile must split over the warps");
   static_assert(CPW == 4 || CPW == 8, "epilogue drains 4 or 8 columns per warp");
 
   extern __shared__ uint8_t smem_raw[];
@@ -142,7 +142,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int wq = warp & 3;   // TMEM lane quadrant of this warp
   const int ws = warp >> 2;  // which quarter of the tile's columns it drains
   const int layout = p.layout, n = p.n_part;
+  const bool pass = (layout == kPassthrough);
   const float kNegInf = __int_as_float(0xFF800000);
+  const int nb = (n + JB - 1) / JB;  // load batches per unit
+
+  auto head_of = [&](int i) { return (ub + i) / tph; };
 
   // Epilogue of local unit j: TMEM accumulator -> bf16 -> * gate -> core.
   auto epilogue = [&](int j) -> bool {
@@ -181,126 +185,94 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     return true;
   };
 
-  // This lane's LSE of partial `lane` for the warp's tokens of a unit (-inf
+  // This lane's LSE of partial `lane` for the warp's tokens of unit i (-inf
   // past n or past S; sanitised when used).
-  auto load_lse = [&](int u, float (&lv)[TPW]) {
-    const int h = u / tph, t0 = (u - h * tph) * BN;
+  auto load_lse = [&](int i, float (&lv)[TPW]) {
+    const int u = ub + i, h = u / tph, t0 = (u - h * tph) * BN;
 #pragma unroll
     for (int tk = 0; tk < TPW; ++tk) {
       const int t = t0 + warp * TPW + tk;
       lv[tk] = kNegInf;
-      if (layout != kPassthrough && t < p.S && lane < n) {
+      if (!pass && t < p.S && lane < n) {
         const int r0 = (layout == kRequestMajor) ? (t / p.q) * p.spr : 0;
         lv[tk] = __ldg(p.lse + (long long)(r0 + lane) * p.l_sp + (long long)t * p.l_st + (long long)h * p.l_sh);
       }
     }
   };
 
-  // Combine the warp's TPW tokens of a unit into latent buffer b.
-  auto combine = [&](int h, int t0, int b, const float (&lv)[TPW]) {
-    uint8_t *gB = gB0 + (size_t)b * kBBytes;
-    int tt[TPW];
-    bool valid[TPW];
+  // Weight of partial `lane` per token (LSE rule; one partial passes through).
+  auto weights_of = [&](const float (&lv)[TPW], float (&wg)[TPW]) {
 #pragma unroll
     for (int tk = 0; tk < TPW; ++tk) {
-      tt[tk] = t0 + warp * TPW + tk;
-      valid[tk] = tt[tk] < p.S;
+      if (pass) {
+        wg[tk] = (lane == 0) ? 1.0f : 0.0f;
+        continue;
+      }
+      const float l = sane(lv[tk]);
+      float m = l;
+#pragma unroll
+      for (int s = 16; s > 0; s >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
+      if (m == kNegInf) m = 0.0f;
+      const float e = (lane < n) ? exp2f(__fmul_rn(__fsub_rn(l, m), kLog2e)) : 0.0f;
+      float Z = 0.0f;  // sequential fp32 sum in partial order
+      for (int j = 0; j < n; ++j) Z = __fadd_rn(Z, __shfl_sync(0xffffffffu, e, j));
+      const float inv = (Z == 0.0f) ? 0.0f : __frcp_rn(Z);
+      wg[tk] = (e == 0.0f) ? 0.0f : __fmul_rn(e, inv);
     }
-    uint4 res[TPW][2];
-    if (layout == kPassthrough) {
+  };
+
+  using Buf = uint4[JB][TPW][2];
+  using Wts = float[JB][TPW];
+
+  // Issue the loads of pipeline step k: unit k / nb, partials (k % nb) * JB ..
+  // (rows of zero weight and tokens past S are not read).
+  auto issue = [&](int k, Buf &buf, Wts &w, const float (&wg)[TPW]) {
+    const int i = k / nb, j0 = (k - i * nb) * JB;
+    const int u = ub + i, h = u / tph, t0 = (u - h * tph) * BN;
 #pragma unroll
-      for (int tk = 0; tk < TPW; ++tk) {
-        if (valid[tk]) {
-          const uint4 *row =
-              reinterpret_cast<const uint4 *>(p.o + (long long)tt[tk] * p.o_st + (long long)h * p.o_sh);
-          res[tk][0] = __ldcs(row + lane);
-          res[tk][1] = __ldcs(row + lane + 32);
+    for (int tk = 0; tk < TPW; ++tk) {
+      const int t = t0 + warp * TPW + tk;
+      const int r0 = (layout == kRequestMajor) ? (t / p.q) * p.spr : 0;
+      const uint16_t *base = p.o + (long long)t * p.o_st + (long long)h * p.o_sh + (long long)r0 * p.o_sp;
+#pragma unroll
+      for (int jj = 0; jj < JB; ++jj) {
+        w[jj][tk] = __shfl_sync(0xffffffffu, wg[tk], (j0 + jj) & 31);  // 0 past n
+        if (w[jj][tk] != 0.0f && t < p.S) {
+          const uint4 *row = reinterpret_cast<const uint4 *>(base + (long long)(j0 + jj) * p.o_sp);
+          buf[jj][tk][0] = __ldcs(row + lane);
+          buf[jj][tk][1] = __ldcs(row + lane + 32);
         } else {
-          res[tk][0] = res[tk][1] = make_uint4(0, 0, 0, 0);
+          buf[jj][tk][0] = buf[jj][tk][1] = make_uint4(0, 0, 0, 0);
         }
       }
-    } else {
-      long long rowoff[TPW];  // o element offset of token tk's first partial
-      float wgt[TPW];         // weight of partial `lane` for token tk
+    }
+  };
+
+  uint64_t acc[TPW][8];  // fp32 pairs: elements (2q, 2q+1) of chunk q/4
+  auto clear_acc = [&]() {
+#pragma unroll
+    for (int tk = 0; tk < TPW; ++tk)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[tk][e] = 0ull;
+  };
+
+  // Merge one batch in partial order: acc += w * o, one rounding per op.
+  auto consume = [&](const Buf &buf, const Wts &w) {
+#pragma unroll
+    for (int jj = 0; jj < JB; ++jj) {
 #pragma unroll
       for (int tk = 0; tk < TPW; ++tk) {
-        const int r0 = (layout == kRequestMajor) ? (tt[tk] / p.q) * p.spr : 0;
-        rowoff[tk] = (long long)r0 * p.o_sp + (long long)tt[tk] * p.o_st + (long long)h * p.o_sh;
-        const float l = sane(lv[tk]);
-        float m = l;
-#pragma unroll
-        for (int s = 16; s > 0; s >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
-        if (m == kNegInf) m = 0.0f;
-        const float e = (lane < n) ? exp2f(__fmul_rn(__fsub_rn(l, m), kLog2e)) : 0.0f;
-        float Z = 0.0f;  // sequential fp32 sum in partial order
-        for (int j = 0; j < n; ++j) Z = __fadd_rn(Z, __shfl_sync(0xffffffffu, e, j));
-        const float inv = (Z == 0.0f) ? 0.0f : __frcp_rn(Z);
-        wgt[tk] = (e == 0.0f) ? 0.0f : __fmul_rn(e, inv);
-      }
-      uint64_t acc[TPW][8];  // fp32 pairs: elements (2q, 2q+1) of chunk q/4
-#pragma unroll
-      for (int tk = 0; tk < TPW; ++tk)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[tk][e] = 0ull;
-      for (int j0 = 0; j0 < n; j0 += JB) {
-        uint4 buf[JB][TPW][2];
-        float w[JB][TPW];
-#pragma unroll
-        for (int jj = 0; jj < JB; ++jj) {
-#pragma unroll
-          for (int tk = 0; tk < TPW; ++tk) {
-            w[jj][tk] = __shfl_sync(0xffffffffu, wgt[tk], j0 + jj);  // 0 past n
-            if (w[jj][tk] != 0.0f) {
-              const uint4 *row =
-                  reinterpret_cast<const uint4 *>(p.o + rowoff[tk] + (long long)(j0 + jj) * p.o_sp);
-              buf[jj][tk][0] = __ldcs(row + lane);
-              buf[jj][tk][1] = __ldcs(row + lane + 32);
-            } else {
-              buf[jj][tk][0] = buf[jj][tk][1] = make_uint4(0, 0, 0, 0);
-            }
-          }
-        }
-#pragma unroll
-        for (int jj = 0; jj < JB; ++jj) {
-#pragma unroll
-          for (int tk = 0; tk < TPW; ++tk) {
-            if (w[jj][tk] == 0.0f) continue;
-            const uint64_t w2 = f2_pack(w[jj][tk], w[jj][tk]);
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              const uint32_t uu[4] = {buf[jj][tk][c].x, buf[jj][tk][c].y, buf[jj][tk][c].z, buf[jj][tk][c].w};
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const uint64_t o2 = f2_pack(bf16_lo(uu[q]), bf16_hi(uu[q]));
-                acc[tk][c * 4 + q] = f2_add(acc[tk][c * 4 + q], f2_mul(w2, o2));
-              }
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int tk = 0; tk < TPW; ++tk)
+        if (w[jj][tk] == 0.0f) continue;
+        const uint64_t w2 = f2_pack(w[jj][tk], w[jj][tk]);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          uint32_t pk[4];
+          const uint32_t uu[4] = {buf[jj][tk][c].x, buf[jj][tk][c].y, buf[jj][tk][c].z, buf[jj][tk][c].w};
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            float lo, hi;
-            f2_unpack(acc[tk][c * 4 + q], lo, hi);
-            pk[q] = pack_bf16(lo, hi);
+            const uint64_t o2 = f2_pack(bf16_lo(uu[q]), bf16_hi(uu[q]));
+            acc[tk][c * 4 + q] = f2_add(acc[tk][c * 4 + q], f2_mul(w2, o2));
           }
-          res[tk][c] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
-    }
-#pragma unroll
-    for (int tk = 0; tk < TPW; ++tk) {
-      const int row = warp * TPW + tk;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint4 x = res[tk][c];
-        if (WFMT == 1) x = mx_chunk(x);
-        if (!valid[tk]) x = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4 *>(gB + sw128_offset(row, lane + 32 * c, BN)) = x;
       }
     }
   };
@@ -326,6 +298,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   };
 
+  // bf16 W_V: thread 0 starts the TMA copy of W_V[h] (after the MMAs of the
+  // previous head, local unit i-1, are complete).
+  uint32_t nchg = 0;  // W_V loads so far
+  auto load_wv_tma = [&](int i, int h) -> bool {
+    bool go = true;
+    if (i > 0) go = wait_or_abort(bar_mma0 + 8 * ((i - 1) & 1), ((i - 1) >> 1) & 1, p.err, kErrWaitMma, s_abort);
+    if (go) {
+      mbar_arrive_expect_tx(bar_wv, kABytes);
+#pragma unroll
+      for (int kb = 0; kb < 8; ++kb) tma_load_3d(sA + kb * 16384u, &tmap_w, kb * 64, 0, h, bar_wv);
+      misc[5] = nchg;
+    }
+    return go;
+  };
+
   // The unit's MMAs (one thread): D[v, t] = sum_k W_V[h][v][k] * lat[t][k].
   auto issue_mma = [&](int i) {
     const int b = i & 1;
@@ -342,44 +329,37 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     misc[4] = (uint32_t)(i + 1);
   };
 
-  int prev_h = -1;
-  uint32_t nchg = 0;  // head changes so far (W_V loads)
-  bool ok = true;
-  float lcur[TPW], lnxt[TPW];
-  if (nu > 0) load_lse(ub, lcur);
-  for (int i = 0; i < nu; ++i) {
-    if (*s_abort) {
-      ok = false;
-      break;
-    }
+  bool ep_early = false;  // epilogue of the previous unit already done
+
+  // Unit i's latents are merged: round / quantise, store, arrive (the last
+  // warp issues the MMAs), then drain the previous unit's accumulator.
+  auto finish = [&](int i, const Buf &raw_rows) -> bool {
     const int u = ub + i, h = u / tph, t0 = (u - h * tph) * BN, b = i & 1;
-    bool ep_done = false;
-    if (h != prev_h) {
-      ++nchg;
-      if (WFMT == 1) {
-        // every MMA reading the previous head's W_V must be done first
-        if (i > 0) {
-          if (!epilogue(i - 1)) {
-            ok = false;
-            break;
-          }
-          ep_done = true;
-        }
-        dequant_wv(h);
-      } else if (threadIdx.x == 0) {
-        bool go = true;
-        if (i > 0) go = wait_or_abort(bar_mma0 + 8 * ((i - 1) & 1), ((i - 1) >> 1) & 1, p.err, kErrWaitMma, s_abort);
-        if (go) {
-          mbar_arrive_expect_tx(bar_wv, kABytes);
+    uint8_t *gB = gB0 + (size_t)b * kBBytes;
 #pragma unroll
-          for (int kb = 0; kb < 8; ++kb) tma_load_3d(sA + kb * 16384u, &tmap_w, kb * 64, 0, h, bar_wv);
-          misc[5] = nchg;
+    for (int tk = 0; tk < TPW; ++tk) {
+      const bool valid = t0 + warp * TPW + tk < p.S;
+      const int row = warp * TPW + tk;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint4 x;
+        if (pass) {
+          x = raw_rows[0][tk][c];
+        } else {
+          uint32_t pk[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float lo, hi;
+            f2_unpack(acc[tk][c * 4 + q], lo, hi);
+            pk[q] = pack_bf16(lo, hi);
+          }
+          x = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
+        if (WFMT == 1) x = mx_chunk(x);
+        if (!valid) x = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(gB + sw128_offset(row, lane + 32 * c, BN)) = x;
       }
-      prev_h = h;
     }
-    if (i + 1 < nu) load_lse(u + 1, lnxt);
-    combine(h, t0, b, lcur);
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
@@ -393,14 +373,85 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
     __syncwarp();
-    if (i > 0 && !ep_done) {
-      if (!epilogue(i - 1)) {
-        ok = false;
-        break;
+    bool ok = true;
+    if (i > 0 && !ep_early) ok = epilogue(i - 1);
+    ep_early = false;
+    clear_acc();
+    // next unit on another head: W_V must be replaced once this unit's MMAs
+    // are complete
+    if (ok && i + 1 < nu && head_of(i + 1) != h) {
+      ++nchg;
+      if (WFMT == 1) {
+        ok = epilogue(i);
+        ep_early = true;
+        if (ok) dequant_wv(head_of(i + 1));
+      } else if (threadIdx.x == 0) {
+        load_wv_tma(i + 1, head_of(i + 1));
       }
     }
+    return ok;
+  };
+
+  // ---- the pipeline: step k merges batch k while batch k+1 is in flight ----
+  const int total = nu * nb;
+  bool ok = true;
+  clear_acc();
+  float lse1[TPW], lse2[TPW];  // LSE of units i+1 and i+2
+  float wcur[TPW], wnxt[TPW];  // weights of units i and i+1
+  Buf bufA, bufB;
+  Wts wA, wB;
+  if (nu > 0) {
+    float lse0[TPW];
+    load_lse(0, lse0);
+    if (nu > 1) load_lse(1, lse1);
+    if (nu > 2) load_lse(2, lse2);
+    ++nchg;
+    if (WFMT == 1) {
+      dequant_wv(head_of(0));
+    } else if (threadIdx.x == 0) {
+      load_wv_tma(0, head_of(0));
+    }
+    weights_of(lse0, wcur);
+    issue(0, bufA, wA, wcur);
+  }
+
+  auto step = [&](int k, Buf &cur, Wts &wc, Buf &nxt, Wts &wn) -> bool {
+    const int i = k / nb;
+    const int bi = k - i * nb;
+    if (k + 1 < total) {
+      if (bi == nb - 1) {
+        // the next batch opens unit i+1
+        weights_of(lse1, wnxt);
 #pragma unroll
-    for (int tk = 0; tk < TPW; ++tk) lcur[tk] = lnxt[tk];
+        for (int tk = 0; tk < TPW; ++tk) lse1[tk] = lse2[tk];
+        if (i + 3 < nu) load_lse(i + 3, lse2);
+        issue(k + 1, nxt, wn, wnxt);
+      } else {
+        issue(k + 1, nxt, wn, wcur);
+      }
+    }
+    consume(cur, wc);
+    if (bi == nb - 1) {
+      if (!finish(i, cur)) return false;
+#pragma unroll
+      for (int tk = 0; tk < TPW; ++tk) wcur[tk] = wnxt[tk];
+    }
+    return true;
+  };
+
+  for (int k = 0; k < total; k += 2) {
+    if (*s_abort) {
+      ok = false;
+      break;
+    }
+    if (!step(k, bufA, wA, bufB, wB)) {
+      ok = false;
+      break;
+    }
+    if (k + 1 < total && !step(k + 1, bufB, wB, bufA, wA)) {
+      ok = false;
+      break;
+    }
   }
   if (ok && nu > 0 && !*s_abort) epilogue(nu - 1);
 
