@@ -5,7 +5,6 @@
 // (host_args / mla_post): strided o / lse rows and heads with a unit-stride
 // last dimension, dense gate / core, launch on the caller's stream, every
 // check done before anything is launched.
-#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -26,12 +25,6 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int *g_err_ptr[kMaxDevices] = {};
 int g_num_sms[kMaxDevices] = {};
-
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
-                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
-                                   CUtensorMapFloatOOBfill);
-EncodeTiledFn g_encode = nullptr;
 
 bool aligned(const void *ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
@@ -156,34 +149,10 @@ int32_t device_state(int *dev_out, int *sms_out, int **err_out) {
     g_num_sms[dev] = sms;
     g_err_ptr[dev] = static_cast<int *>(ptr);
   }
-  if (!g_encode) {
-    void *fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || !fn)
-      return MLA_ERR_CUDA;
-    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
-  }
   *dev_out = dev;
   *sms_out = g_num_sms[dev];
   *err_out = g_err_ptr[dev];
   return MLA_OK;
-}
-
-// TMA descriptor of bf16 W_V [H, 128, 512]: boxes of 64 K x 128 rows, 128-byte
-// swizzle (the layout the MMA's shared-memory descriptor expects).
-int32_t make_wv_tmap(const KParams &k, CUtensorMap *tm) {
-  cuuint64_t dims[3] = {512, 128, (cuuint64_t)k.H};
-  cuuint64_t strides[2] = {(cuuint64_t)k.w_sv * 2, (cuuint64_t)k.w_sh * 2};
-  cuuint32_t box[3] = {64, 128, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  if (k.H == 1) strides[1] = (cuuint64_t)128 * k.w_sv * 2;  // unused dimension; any legal stride
-  if (strides[1] == 0) strides[1] = 16;
-  CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(k.w_v), dims, strides, box,
-                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
 }
 
 }  // namespace
@@ -235,13 +204,7 @@ int32_t mla_combine_uv(const mla_combine_uv_args *args, void *stream) {
   if (pl.kernel == MLA_KERNEL_SIMT) {
     e = mla::launch_simt(kp, s);
   } else {
-    alignas(64) CUtensorMap tm;
-    std::memset(&tm, 0, sizeof tm);
-    if (kp.w_fmt == MLA_W_BF16) {
-      st = make_wv_tmap(kp, &tm);
-      if (st != MLA_OK) return st;
-    }
-    e = mla::launch_tc(kp, &tm, pl.grid, s);
+    e = mla::launch_tc(kp, pl.grid, s);
   }
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }

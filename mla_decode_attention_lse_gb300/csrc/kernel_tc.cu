@@ -4,7 +4,9 @@
 //
 // Work unit: (head h, BN-token tile), head-major, split into one contiguous
 // run per CTA (persistent grid of at most one CTA per SM), so a CTA keeps
-// W_V[h] resident in shared memory across the token tiles of a head.
+// W_V[h] resident in shared memory across the token tiles of a head.  The
+// epilogue stages each warp's bf16 accumulators through shared memory so the
+// gate loads and core stores are 16-byte, token-major accesses.
 //
 // GEMM orientation (per unit): D[v, t] = sum_k W_V[h][v][k] * lat[t][k] with
 // M = 128 (the V rows), N = BN tokens, K = 512, both operands K-major with
@@ -17,8 +19,9 @@
 // completes a unit's latents last (per-buffer monotonic arrival counters)
 // issues that unit's 32 MMAs from one thread and commits them to an
 // mbarrier; being last also proves every warp has drained the previous
-// accumulator in that TMEM buffer.  Thread 0 allocates TMEM and loads W_V[h]
-// with TMA (bf16) at each head change.  Latent buffers and TMEM accumulators
+// accumulator in that TMEM buffer.  At a head change every warp first waits
+// for the previous head's MMAs, then copies (bf16) or dequantises (MXFP4)
+// W_V[h] into the A tile.  Latent buffers and TMEM accumulators
 // are double-buffered, so the combine of unit i overlaps the MMA of unit i-1
 // and the epilogue of unit i-2.  A warp issues all of its tokens' partial-row
 // loads of a batch at once and prefetches the next unit's LSE values while
@@ -33,7 +36,6 @@
 // index order (packed f32x2 arithmetic rounds each lane like a scalar op).
 // Every mbarrier wait is bounded; on timeout the kernel records an error,
 // drains its own in-flight copies and MMAs, frees TMEM and returns.
-#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -46,6 +48,7 @@ namespace {
 
 constexpr uint32_t kABytes = 128u * 1024u;  // W_V[h], bf16, 8 K-blocks x 16 KiB
 constexpr int kWorkers = kTcWarps;           // all warps combine, drain and (one of them) issue
+constexpr uint32_t kEpiBytes = kTcWarps * 8u * 32u * 2u;  // epilogue staging, 8 KiB
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int *err, int code,
                                               volatile int *abort_flag) {
@@ -90,7 +93,7 @@ __device__ __forceinline__ uint4 mx_chunk(uint4 x) {
 
 template <int BN, int WFMT>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tmap_w) {
+    tc_kernel(const __grid_constant__ KParams p) {
   constexpr int TPW = BN / kWorkers;       // tokens per warp per unit
   constexpr int JB = 4 / TPW;              // partials per batch: 4 rows (8 x 16 B per lane)
   constexpr int CPW = BN / 4;              // TMEM columns each warp drains
@@ -108,18 +111,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t sB0 = sbase + kABytes;
   uint8_t *gA = gbase;
   uint8_t *gB0 = gbase + kABytes;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(gbase + kABytes + 2 * kBBytes);
+  // per-warp epilogue staging: CPW tokens x 32 V rows of bf16
+  uint16_t *gE = reinterpret_cast<uint16_t *>(gbase + kABytes + 2 * kBBytes);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(gbase + kABytes + 2 * kBBytes + kEpiBytes);
   uint32_t *misc = reinterpret_cast<uint32_t *>(bars + 4);
   // misc[0] TMEM base, misc[1] abort flag, misc[2..3] arrival counters,
-  // misc[4] last unit whose MMAs were issued (+1), misc[5] W_V copies issued
+  // misc[4] last unit whose MMAs were issued (+1)
   volatile int *s_abort = reinterpret_cast<volatile int *>(&misc[1]);
-  const uint32_t bar_wv = smem_u32(&bars[0]);
-  const uint32_t bar_mma0 = smem_u32(&bars[1]);  // +8*b
+  const uint32_t bar_mma0 = smem_u32(&bars[0]);  // +8*b
   const uint32_t cnt0 = smem_u32(&misc[2]);      // +4*b
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(bar_wv, 1u);
     mbar_init(bar_mma0, 1u);
     mbar_init(bar_mma0 + 8, 1u);
     for (int k = 1; k < 6; ++k) misc[k] = 0u;
@@ -146,19 +149,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const float kNegInf = __int_as_float(0xFF800000);
   const int nb = (n + JB - 1) / JB;  // load batches per unit
 
-  auto head_of = [&](int i) { return (ub + i) / tph; };
-
-  // Epilogue of local unit j: TMEM accumulator -> bf16 -> * gate -> core.
-  auto epilogue = [&](int j) -> bool {
-    const int u = ub + j, h = u / tph, t0 = (u - h * tph) * BN, bj = j & 1;
-    const int v = wq * 32 + lane;
-    const int tb = t0 + ws * CPW;
-    uint16_t g[CPW];
-#pragma unroll
-    for (int e = 0; e < CPW; ++e) {
-      const int t = tb + e;
-      g[e] = (t < p.S) ? __ldg(p.gate + (long long)t * Wrow + h * kV + v) : (uint16_t)0;
+  // A cursor over the CTA's units: head and token tile, advanced one unit at
+  // a time (no division in the loop).
+  struct Cur {
+    int h, tile;
+  };
+  const Cur c_first{ub / tph, ub - (ub / tph) * tph};
+  auto advance = [&](Cur &c) {
+    if (++c.tile == tph) {
+      c.tile = 0;
+      ++c.h;
     }
+  };
+
+  // Epilogue of a unit: TMEM accumulator -> bf16 -> (staged through shared
+  // memory, token-major) * gate -> core with 16-byte accesses.
+  uint16_t *stage = gE + warp * (CPW * 32);
+  auto epilogue = [&](int j, const Cur &c) -> bool {
+    const int bj = j & 1;
+    // lane -> (token e, 8 consecutive V rows)
+    constexpr int kLanes = CPW * 4;
+    const int e = lane >> 2, v8 = (lane & 3) * 8;
+    const int t = c.tile * BN + ws * CPW + e;
+    const bool act = lane < kLanes && t < p.S;
+    const long long off = (long long)t * Wrow + c.h * kV + wq * 32 + v8;
+    uint4 g = make_uint4(0, 0, 0, 0);
+    if (act) g = __ldg(reinterpret_cast<const uint4 *>(p.gate + off));
     bool ok = wait_or_abort(bar_mma0 + 8 * bj, (j >> 1) & 1, p.err, kErrWaitMma, s_abort);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) return false;
@@ -173,29 +189,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_wait_ld();
     tc_fence_before();
 #pragma unroll
-    for (int e = 0; e < CPW; ++e) {
-      const int t = tb + e;
-      if (t < p.S) {
-        const float a = round_bf16(__uint_as_float(r[e]));
-        const float gv = __uint_as_float((uint32_t)g[e] << 16);
-        const __nv_bfloat16 o = __float2bfloat16_rn(a * gv);
-        p.out[(long long)t * Wrow + h * kV + v] = *reinterpret_cast<const uint16_t *>(&o);
-      }
+    for (int x = 0; x < CPW; ++x) {
+      const __nv_bfloat16 a = __float2bfloat16_rn(__uint_as_float(r[x]));
+      stage[x * 32 + lane] = *reinterpret_cast<const uint16_t *>(&a);
     }
+    __syncwarp();
+    if (act) {
+      const uint4 a = *reinterpret_cast<const uint4 *>(stage + e * 32 + v8);
+      const uint32_t aa[4] = {a.x, a.y, a.z, a.w}, gg[4] = {g.x, g.y, g.z, g.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        o[q] = pack_bf16(bf16_lo(aa[q]) * bf16_lo(gg[q]), bf16_hi(aa[q]) * bf16_hi(gg[q]));
+      *reinterpret_cast<uint4 *>(p.out + off) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    __syncwarp();
     return true;
   };
 
-  // This lane's LSE of partial `lane` for the warp's tokens of unit i (-inf
+  // This lane's LSE of partial `lane` for the warp's tokens of a unit (-inf
   // past n or past S; sanitised when used).
-  auto load_lse = [&](int i, float (&lv)[TPW]) {
-    const int u = ub + i, h = u / tph, t0 = (u - h * tph) * BN;
+  auto load_lse = [&](const Cur &c, float (&lv)[TPW]) {
 #pragma unroll
     for (int tk = 0; tk < TPW; ++tk) {
-      const int t = t0 + warp * TPW + tk;
+      const int t = c.tile * BN + warp * TPW + tk;
       lv[tk] = kNegInf;
       if (!pass && t < p.S && lane < n) {
         const int r0 = (layout == kRequestMajor) ? (t / p.q) * p.spr : 0;
-        lv[tk] = __ldg(p.lse + (long long)(r0 + lane) * p.l_sp + (long long)t * p.l_st + (long long)h * p.l_sh);
+        lv[tk] = __ldg(p.lse + (long long)(r0 + lane) * p.l_sp + (long long)t * p.l_st + (long long)c.h * p.l_sh);
       }
     }
   };
@@ -224,21 +245,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   using Buf = uint4[JB][TPW][2];
   using Wts = float[JB][TPW];
 
-  // Issue the loads of pipeline step k: unit k / nb, partials (k % nb) * JB ..
+  // Issue the loads of one batch: unit at cursor c, partials j0 .. j0+JB-1
   // (rows of zero weight and tokens past S are not read).
-  auto issue = [&](int k, Buf &buf, Wts &w, const float (&wg)[TPW]) {
-    const int i = k / nb, j0 = (k - i * nb) * JB;
-    const int u = ub + i, h = u / tph, t0 = (u - h * tph) * BN;
+  auto issue = [&](const Cur &c, int j0, Buf &buf, Wts &w, const float (&wg)[TPW]) {
 #pragma unroll
     for (int tk = 0; tk < TPW; ++tk) {
-      const int t = t0 + warp * TPW + tk;
+      const int t = c.tile * BN + warp * TPW + tk;
       const int r0 = (layout == kRequestMajor) ? (t / p.q) * p.spr : 0;
-      const uint16_t *base = p.o + (long long)t * p.o_st + (long long)h * p.o_sh + (long long)r0 * p.o_sp;
+      const uint16_t *base = p.o + (long long)t * p.o_st + (long long)c.h * p.o_sh + (long long)(r0 + j0) * p.o_sp;
 #pragma unroll
       for (int jj = 0; jj < JB; ++jj) {
         w[jj][tk] = __shfl_sync(0xffffffffu, wg[tk], (j0 + jj) & 31);  // 0 past n
         if (w[jj][tk] != 0.0f && t < p.S) {
-          const uint4 *row = reinterpret_cast<const uint4 *>(base + (long long)(j0 + jj) * p.o_sp);
+          const uint4 *row = reinterpret_cast<const uint4 *>(base + (long long)jj * p.o_sp);
           buf[jj][tk][0] = __ldcs(row + lane);
           buf[jj][tk][1] = __ldcs(row + lane + 32);
         } else {
@@ -277,8 +296,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   };
 
-  // MXFP4: W_V[h] codes + scales -> exact bf16 values in the swizzled A tile.
-  auto dequant_wv = [&](int h) {
+  // W_V[h] -> the swizzled bf16 A tile: bf16 rows copied, MXFP4 codes +
+  // scales turned into their exact bf16 values.
+  auto load_wv = [&](int h) {
+    if (WFMT == 0) {
+      const uint16_t *wb = static_cast<const uint16_t *>(p.w_v) + (long long)h * p.w_sh;
+      constexpr int kPer = kV * 64 / kTcThreads;
+      uint4 x[kPer];
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int s = threadIdx.x + i * kTcThreads;
+        x[i] = __ldg(reinterpret_cast<const uint4 *>(wb + (long long)(s >> 6) * p.w_sv) + (s & 63));
+      }
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int s = threadIdx.x + i * kTcThreads;
+        *reinterpret_cast<uint4 *>(gA + sw128_offset(s >> 6, s & 63, kV)) = x[i];
+      }
+      return;
+    }
     const uint8_t *wbase = static_cast<const uint8_t *>(p.w_v) + (long long)h * p.w_sh;
     const uint8_t *sbase_h = p.w_scale + (long long)h * p.s_sh;
     constexpr int kPer = kV * 64 / kTcThreads;  // 16-byte chunks per thread
@@ -296,21 +332,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       *reinterpret_cast<uint4 *>(gA + sw128_offset(v, c, kV)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
-  };
-
-  // bf16 W_V: thread 0 starts the TMA copy of W_V[h] (after the MMAs of the
-  // previous head, local unit i-1, are complete).
-  uint32_t nchg = 0;  // W_V loads so far
-  auto load_wv_tma = [&](int i, int h) -> bool {
-    bool go = true;
-    if (i > 0) go = wait_or_abort(bar_mma0 + 8 * ((i - 1) & 1), ((i - 1) >> 1) & 1, p.err, kErrWaitMma, s_abort);
-    if (go) {
-      mbar_arrive_expect_tx(bar_wv, kABytes);
-#pragma unroll
-      for (int kb = 0; kb < 8; ++kb) tma_load_3d(sA + kb * 16384u, &tmap_w, kb * 64, 0, h, bar_wv);
-      misc[5] = nchg;
-    }
-    return go;
   };
 
   // The unit's MMAs (one thread): D[v, t] = sum_k W_V[h][v][k] * lat[t][k].
@@ -331,33 +352,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   bool ep_early = false;  // epilogue of the previous unit already done
 
-  // Unit i's latents are merged: round / quantise, store, arrive (the last
-  // warp issues the MMAs), then drain the previous unit's accumulator.
-  auto finish = [&](int i, const Buf &raw_rows) -> bool {
-    const int u = ub + i, h = u / tph, t0 = (u - h * tph) * BN, b = i & 1;
+  // Unit i (cursor c; previous unit at cp) has its latents merged: round /
+  // quantise, store, arrive (the last warp issues the MMAs), then drain the
+  // previous unit's accumulator.
+  auto finish = [&](int i, const Cur &c, const Cur &cp, const Buf &raw_rows) -> bool {
+    const int b = i & 1;
     uint8_t *gB = gB0 + (size_t)b * kBBytes;
 #pragma unroll
     for (int tk = 0; tk < TPW; ++tk) {
-      const bool valid = t0 + warp * TPW + tk < p.S;
+      const bool valid = c.tile * BN + warp * TPW + tk < p.S;
       const int row = warp * TPW + tk;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint4 x;
         if (pass) {
-          x = raw_rows[0][tk][c];
+          x = raw_rows[0][tk][cc];
         } else {
           uint32_t pk[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             float lo, hi;
-            f2_unpack(acc[tk][c * 4 + q], lo, hi);
+            f2_unpack(acc[tk][cc * 4 + q], lo, hi);
             pk[q] = pack_bf16(lo, hi);
           }
           x = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
         if (WFMT == 1) x = mx_chunk(x);
         if (!valid) x = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4 *>(gB + sw128_offset(row, lane + 32 * c, BN)) = x;
+        *reinterpret_cast<uint4 *>(gB + sw128_offset(row, lane + 32 * cc, BN)) = x;
       }
     }
     fence_proxy_async_smem();
@@ -366,75 +388,81 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // arrivals on buffer b are numbered across its uses: use (i >> 1) takes
       // numbers (i >> 1) * kWorkers .. + kWorkers - 1; the last one issues
       const uint32_t prev = atom_add_acq_rel_cta(cnt0 + 4 * b, 1u);
-      if (prev == (uint32_t)((i >> 1) + 1) * kWorkers - 1u) {
-        bool go = true;
-        if (WFMT == 0) go = wait_or_abort(bar_wv, (nchg - 1u) & 1u, p.err, kErrWaitWv, s_abort);
-        if (go) issue_mma(i);
-      }
+      if (prev == (uint32_t)((i >> 1) + 1) * kWorkers - 1u) issue_mma(i);
     }
     __syncwarp();
     bool ok = true;
-    if (i > 0 && !ep_early) ok = epilogue(i - 1);
+    if (i > 0 && !ep_early) ok = epilogue(i - 1, cp);
     ep_early = false;
     clear_acc();
     // next unit on another head: W_V must be replaced once this unit's MMAs
     // are complete
-    if (ok && i + 1 < nu && head_of(i + 1) != h) {
-      ++nchg;
-      if (WFMT == 1) {
-        ok = epilogue(i);
-        ep_early = true;
-        if (ok) dequant_wv(head_of(i + 1));
-      } else if (threadIdx.x == 0) {
-        load_wv_tma(i + 1, head_of(i + 1));
-      }
+    if (ok && i + 1 < nu && c.tile + 1 == tph) {
+      ok = epilogue(i, c);
+      ep_early = true;
+      if (ok) load_wv(c.h + 1);
     }
     return ok;
   };
 
   // ---- the pipeline: step k merges batch k while batch k+1 is in flight ----
-  const int total = nu * nb;
   bool ok = true;
   clear_acc();
   float lse1[TPW], lse2[TPW];  // LSE of units i+1 and i+2
   float wcur[TPW], wnxt[TPW];  // weights of units i and i+1
   Buf bufA, bufB;
   Wts wA, wB;
+  Cur cu = c_first;    // unit i (being merged)
+  Cur cprev = c_first; // unit i-1
+  Cur cn = c_first;    // unit of the next batch to issue
+  Cur cl = c_first;    // next unit whose LSE is loaded (i+3)
+  int i = 0, bi = 0;   // unit and batch being merged
+  int nbi = 1;         // batch index of the next batch within its unit
   if (nu > 0) {
     float lse0[TPW];
-    load_lse(0, lse0);
-    if (nu > 1) load_lse(1, lse1);
-    if (nu > 2) load_lse(2, lse2);
-    ++nchg;
-    if (WFMT == 1) {
-      dequant_wv(head_of(0));
-    } else if (threadIdx.x == 0) {
-      load_wv_tma(0, head_of(0));
-    }
+    load_lse(cl, lse0);
+    advance(cl);
+    if (nu > 1) load_lse(cl, lse1);
+    advance(cl);
+    if (nu > 2) load_lse(cl, lse2);
+    advance(cl);
+    load_wv(c_first.h);
     weights_of(lse0, wcur);
-    issue(0, bufA, wA, wcur);
+    issue(cu, 0, bufA, wA, wcur);
+    if (nbi == nb) {
+      nbi = 0;
+      advance(cn);
+    }
   }
+  const int total = nu * nb;
 
   auto step = [&](int k, Buf &cur, Wts &wc, Buf &nxt, Wts &wn) -> bool {
-    const int i = k / nb;
-    const int bi = k - i * nb;
     if (k + 1 < total) {
-      if (bi == nb - 1) {
+      if (nbi == 0) {
         // the next batch opens unit i+1
         weights_of(lse1, wnxt);
 #pragma unroll
         for (int tk = 0; tk < TPW; ++tk) lse1[tk] = lse2[tk];
-        if (i + 3 < nu) load_lse(i + 3, lse2);
-        issue(k + 1, nxt, wn, wnxt);
+        if (i + 3 < nu) load_lse(cl, lse2);
+        advance(cl);
+        issue(cn, 0, nxt, wn, wnxt);
       } else {
-        issue(k + 1, nxt, wn, wcur);
+        issue(cn, nbi * JB, nxt, wn, wcur);
+      }
+      if (++nbi == nb) {
+        nbi = 0;
+        advance(cn);
       }
     }
     consume(cur, wc);
-    if (bi == nb - 1) {
-      if (!finish(i, cur)) return false;
+    if (++bi == nb) {
+      if (!finish(i, cu, cprev, cur)) return false;
 #pragma unroll
       for (int tk = 0; tk < TPW; ++tk) wcur[tk] = wnxt[tk];
+      cprev = cu;
+      advance(cu);
+      ++i;
+      bi = 0;
     }
     return true;
   };
@@ -453,7 +481,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       break;
     }
   }
-  if (ok && nu > 0 && !*s_abort) epilogue(nu - 1);
+  if (ok && nu > 0 && !*s_abort) epilogue(nu - 1, cprev);
 
   // rows S .. S_out-1 of core are zero (this CTA's slice of them)
   const long long n16 = (long long)(p.S_out - p.S) * p.H * (kV * 2 / 16);
@@ -467,8 +495,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   if (threadIdx.x == 0) {
     // drain what this CTA started (only pending after an abort): the last
-    // W_V copy and the last committed MMAs
-    if (misc[5] > 0u) mbar_wait(bar_wv, (misc[5] - 1u) & 1u, p.err, kErrWaitTeardown);
+    // committed MMAs
     if (misc[4] > 0u) {
       const int last = (int)misc[4] - 1;
       mbar_wait(bar_mma0 + 8 * (last & 1), (last >> 1) & 1, p.err, kErrWaitTeardown);
@@ -481,22 +508,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
-size_t tc_smem_bytes(int tile) { return 1024 + kABytes + 2u * (size_t)tile * 1024u + 128; }
+size_t tc_smem_bytes(int tile) { return 1024 + kABytes + 2u * (size_t)tile * 1024u + kEpiBytes + 128; }
 
 template <int BN, int WFMT>
-static cudaError_t launch_one(const KParams &p, const CUtensorMap *tmap, int grid, cudaStream_t s) {
+static cudaError_t launch_one(const KParams &p, int grid, cudaStream_t s) {
   const size_t smem = tc_smem_bytes(BN);
   cudaError_t e = cudaFuncSetAttribute(tc_kernel<BN, WFMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  tc_kernel<BN, WFMT><<<grid, kTcThreads, smem, s>>>(p, *tmap);
+  tc_kernel<BN, WFMT><<<grid, kTcThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_tc(const KParams &p, const CUtensorMap *tmap_w, int grid, cudaStream_t stream) {
-  if (p.tile == 16) return p.w_fmt == 0 ? launch_one<16, 0>(p, tmap_w, grid, stream)
-                                        : launch_one<16, 1>(p, tmap_w, grid, stream);
-  if (p.tile == 32) return p.w_fmt == 0 ? launch_one<32, 0>(p, tmap_w, grid, stream)
-                                        : launch_one<32, 1>(p, tmap_w, grid, stream);
+cudaError_t launch_tc(const KParams &p, int grid, cudaStream_t stream) {
+  if (p.tile == 16) return p.w_fmt == 0 ? launch_one<16, 0>(p, grid, stream) : launch_one<16, 1>(p, grid, stream);
+  if (p.tile == 32) return p.w_fmt == 0 ? launch_one<32, 0>(p, grid, stream) : launch_one<32, 1>(p, grid, stream);
   return cudaErrorInvalidValue;
 }
 

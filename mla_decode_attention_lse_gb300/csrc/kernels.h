@@ -1,7 +1,6 @@
 // kernels.h -- host-side launch entry points of the kernels (internal).
 #pragma once
 
-#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "kparams.h"
@@ -12,12 +11,11 @@ namespace mla {
 size_t simt_smem_bytes(int n_part);
 cudaError_t launch_simt(const KParams &p, cudaStream_t stream);
 
-// Fused tcgen05 kernel: tile = 16 or 32 tokens, n_part <= 32.  `tmap_w` is
-// the TMA descriptor of bf16 W_V (unused for MXFP4).
+// Fused tcgen05 kernel: tile = 16 or 32 tokens, n_part <= 32.
 constexpr int kTcWarps = 16;
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kTcMaxPart = 32;
 size_t tc_smem_bytes(int tile);
-cudaError_t launch_tc(const KParams &p, const CUtensorMap *tmap_w, int grid, cudaStream_t stream);
+cudaError_t launch_tc(const KParams &p, int grid, cudaStream_t stream);
 
 }  // namespace mla
