@@ -99,7 +99,7 @@ int32_t plan_impl(const mla_combine_uv_args *a, int32_t num_sms, mla_plan *pl, K
     pl->units = a->H * ((S + tile - 1) / tile);
     pl->grid = pl->units < num_sms ? pl->units : num_sms;
     pl->threads = mla::kTcThreads;
-    pl->smem_bytes = (int32_t)mla::tc_smem_bytes(tile);
+    pl->smem_bytes = (int32_t)mla::tc_smem_bytes(tile, a->w_fmt);
   }
 
   if (kp) {

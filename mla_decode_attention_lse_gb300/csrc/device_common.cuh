@@ -265,6 +265,23 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint
       : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::mxf4 with E8M0 block-32 scales
+// (two scales per row per K=64 step, taken from TMEM at sfa / sfb).
+__device__ __forceinline__ void tc_mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Copy a 32-row x 16-byte shared-memory matrix into TMEM lanes 0..31 of four
+// columns, replicated into all four lane quadrants.
+__device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // Arrive on `bar` once every tcgen05 operation this thread issued so far is
 // complete.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
@@ -306,6 +323,29 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   d |= (uint64_t)2 << 61;                           // swizzle mode: 128 B
   return d;
 }
+
+// Shared-memory descriptor without swizzle: 16-byte rows, 8-row groups 128
+// bytes apart (the source layout of a 32x128b tcgen05.cp).
+__device__ __forceinline__ uint64_t smem_desc_rows16(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(16u >> 4) << 16;
+  d |= (uint64_t)(128u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
+// Instruction descriptor, kind::mxf4 block-scaled: E2M1 A and B, E8M0 scales,
+// fp32 D, both K-major.  The scale-factor ids (byte offset of the two scales
+// in each 32-bit TMEM word: 0 or 2) are or-ed in per K step.
+__host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N) {
+  return (1u << 7)                      // A format: E2M1
+         | (1u << 10)                   // B format: E2M1
+         | ((uint32_t)(N >> 3) << 17)   // N / 8
+         | (1u << 23)                   // scale format: UE8M0
+         | ((uint32_t)(M >> 4) << 24);  // M / 16
+}
+__host__ __device__ constexpr uint32_t idesc_sf_ids(uint32_t id) { return (id << 4) | (id << 29); }
 
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 D, both K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {

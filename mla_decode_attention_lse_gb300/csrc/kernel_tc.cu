@@ -1,6 +1,6 @@
 // kernel_tc.cu -- fused tensor-core kernel of the MLA decode post-attention
-// stage for sm_103a: LSE combine -> (MXFP4) latents in shared memory ->
-// tcgen05 W_UV GEMM with the accumulator in TMEM -> gate epilogue.
+// stage for sm_103a: LSE combine -> bf16 (or MXFP4) latents in shared memory
+// -> tcgen05 W_UV GEMM with the accumulator in TMEM -> gate epilogue.
 //
 // Work unit: (head h, BN-token tile), head-major, split into one contiguous
 // run per CTA (persistent grid of at most one CTA per SM), so a CTA keeps
@@ -11,17 +11,23 @@
 // GEMM orientation (per unit): D[v, t] = sum_k W_V[h][v][k] * lat[t][k] with
 // M = 128 (the V rows), N = BN tokens, K = 512, both operands K-major with
 // the 128-byte swizzle.  This keeps M at the tensor core's 128 while the
-// token tile stays small enough for decode batches.
+// token tile stays small enough for decode batches.  bf16 W_V: 32 MMAs of
+// kind::f16 (K = 16).  MXFP4 W_V: W_V stays as packed E2M1 codes (32 KiB),
+// the latents are quantised straight to E2M1 codes + E8M0 block scales, and
+// 8 MMAs of kind::mxf4.block_scale (K = 64) read both operands' scales from
+// TMEM, where tcgen05.cp puts them: for V row m, lane m, column
+// (group base + m / 32); for token n, lane 32q + n in every lane quadrant q;
+// each 32-bit word holds the scales of four consecutive 32-wide K blocks.
 //
 // Warp roles (512 threads, 16 warps, all alike): each warp combines BN/16 of
 // a unit's tokens into the latent buffer, then runs the epilogue of the
 // previous unit (TMEM -> registers, bf16(acc) * gate -> core).  The warp that
 // completes a unit's latents last (per-buffer monotonic arrival counters)
-// issues that unit's 32 MMAs from one thread and commits them to an
+// issues that unit's MMAs from one thread and commits them to an
 // mbarrier; being last also proves every warp has drained the previous
 // accumulator in that TMEM buffer.  At a head change every warp first waits
-// for the previous head's MMAs, then copies (bf16) or dequantises (MXFP4)
-// W_V[h] into the A tile.  Latent buffers and TMEM accumulators
+// for the previous head's MMAs, then copies W_V[h] (and, for MXFP4, its
+// scales) into shared memory.  Latent buffers and TMEM accumulators
 // are double-buffered, so the combine of unit i overlaps the MMA of unit i-1
 // and the epilogue of unit i-2.  A warp issues all of its tokens' partial-row
 // loads of a batch at once and prefetches the next unit's LSE values while
@@ -46,9 +52,31 @@ namespace mla {
 
 namespace {
 
-constexpr uint32_t kABytes = 128u * 1024u;  // W_V[h], bf16, 8 K-blocks x 16 KiB
-constexpr int kWorkers = kTcWarps;           // all warps combine, drain and (one of them) issue
-constexpr uint32_t kEpiBytes = kTcWarps * 8u * 32u * 2u;  // epilogue staging, 8 KiB
+constexpr int kWorkers = kTcWarps;  // all warps combine, drain and (one of them) issue
+
+// Shared memory and TMEM plan of one CTA.
+struct TcLayout {
+  uint32_t a_bytes, b_off, b_bytes, sfa_off, sfb_off, epi_off, bar_off, total;
+  uint32_t tmem_cols, sfa_col, sfb_col;
+};
+__host__ __device__ constexpr TcLayout tc_layout(int BN, int WFMT) {
+  TcLayout L{};
+  L.a_bytes = WFMT ? 128u * 256u : 128u * 1024u;           // W_V[h]: E2M1 codes or bf16
+  L.b_off = L.a_bytes;
+  L.b_bytes = WFMT ? (uint32_t)BN * 256u : (uint32_t)BN * 1024u;  // one latent buffer
+  L.sfa_off = L.b_off + 2 * L.b_bytes;
+  L.sfb_off = L.sfa_off + (WFMT ? 2048u : 0u);
+  L.epi_off = L.sfb_off + (WFMT ? 2u * 2048u : 0u);
+  L.bar_off = L.epi_off + kTcWarps * 8u * 32u * 2u;         // epilogue staging, 8 KiB
+  L.total = L.bar_off + 128u;
+  // TMEM: two fp32 accumulators of BN columns; MXFP4 adds two 16-column
+  // scale regions for W_V and two for the latents (columns 64..127)
+  const uint32_t acc = 2u * (uint32_t)BN;
+  L.sfa_col = 64u;
+  L.sfb_col = 96u;
+  L.tmem_cols = WFMT ? 128u : (acc < 32u ? 32u : acc);
+  return L;
+}
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int *err, int code,
                                               volatile int *abort_flag) {
@@ -65,28 +93,25 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int
   }
 }
 
-// MXFP4 round trip of a lane's 8 bf16 latents (one 16-byte chunk): the block
-// of 32 spans lanes 4g..4g+3.  Scale code from the largest sign-cleared bf16
-// pattern; elements scaled by an exact power of two, converted to E2M1 by the
-// hardware (nearest even, saturating at 6) and back; the result is the exact
-// dequantised value, returned as bf16.
-__device__ __forceinline__ uint4 mx_chunk(uint4 x) {
-  uint32_t u[4] = {x.x, x.y, x.z, x.w};
-  uint32_t am2 = max_u16x2(max_u16x2(u[0] & 0x7FFF7FFFu, u[1] & 0x7FFF7FFFu),
-                           max_u16x2(u[2] & 0x7FFF7FFFu, u[3] & 0x7FFF7FFFu));
+// MXFP4 quantisation of a lane's 8 bf16 latents (one 16-byte chunk; the
+// block of 32 spans lanes 4g..4g+3).  Scale code from the largest
+// sign-cleared bf16 pattern; elements scaled by an exact power of two and
+// converted to E2M1 by the hardware (nearest even, saturating at 6).  Returns
+// the 8 codes packed (element 2i in the low nibble of byte i) and the scale.
+__device__ __forceinline__ uint32_t mx_codes(uint4 x, uint32_t &sc) {
+  const uint32_t u[4] = {x.x, x.y, x.z, x.w};
+  const uint32_t am2 = max_u16x2(max_u16x2(u[0] & 0x7FFF7FFFu, u[1] & 0x7FFF7FFFu),
+                                 max_u16x2(u[2] & 0x7FFF7FFFu, u[3] & 0x7FFF7FFFu));
   uint32_t am = max(am2 & 0xFFFFu, am2 >> 16);
   am = max(am, __shfl_xor_sync(0xffffffffu, am, 1));
   am = max(am, __shfl_xor_sync(0xffffffffu, am, 2));
-  const uint32_t sc = mx_scale_code(am);
-  if (sc == 255u) return make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);
-  const float scale = e8m0_to_f32(sc), inv = e8m0_inverse(sc);
+  sc = mx_scale_code(am);
+  if (sc == 255u) return 0u;  // Inf / NaN in the block: the NaN scale carries it
+  const float inv = e8m0_inverse(sc);
+  uint32_t w = 0;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint32_t e = e2m1x2_from_f32(bf16_lo(u[q]) * inv, bf16_hi(u[q]) * inv);
-    const uint32_t h2 = f16x2_from_e2m1x2(e);
-    u[q] = pack_bf16(f16_lo(h2) * scale, f16_hi(h2) * scale);
-  }
-  return make_uint4(u[0], u[1], u[2], u[3]);
+  for (int q = 0; q < 4; ++q) w |= e2m1x2_from_f32(bf16_lo(u[q]) * inv, bf16_hi(u[q]) * inv) << (8 * q);
+  return w;
 }
 
 }  // namespace
@@ -97,9 +122,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr int TPW = BN / kWorkers;       // tokens per warp per unit
   constexpr int JB = 4 / TPW;              // partials per batch: 4 rows (8 x 16 B per lane)
   constexpr int CPW = BN / 4;              // TMEM columns each warp drains
-  constexpr uint32_t kBBytes = BN * 1024u; // one latent buffer (BN x 512 bf16)
-  constexpr uint32_t kCols = (2 * BN < 32) ? 32u : (uint32_t)(2 * BN);
-  constexpr uint32_t kIdesc = idesc_bf16(128, BN);
+  constexpr TcLayout L = tc_layout(BN, WFMT);
+  constexpr uint32_t kCols = L.tmem_cols;
   static_assert(TPW >= 1 && BN % kWorkers == 0 && JB >= 1, "tile must split over the warps");
   static_assert(CPW == 4 || CPW == 8, "epilogue drains 4 or 8 columns per warp");
 
@@ -108,12 +132,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t sbase = (raw + 1023u) & ~1023u;    // 1024-byte aligned (swizzle atoms)
   uint8_t *gbase = smem_raw + (sbase - raw);
   const uint32_t sA = sbase;
-  const uint32_t sB0 = sbase + kABytes;
+  const uint32_t sB0 = sbase + L.b_off;
   uint8_t *gA = gbase;
-  uint8_t *gB0 = gbase + kABytes;
+  uint8_t *gB0 = gbase + L.b_off;
+  uint8_t *gSFA = gbase + L.sfa_off;   // MXFP4: W_V scale atoms (4 x 512 B)
+  uint8_t *gSFB0 = gbase + L.sfb_off;  // MXFP4: latent scale atoms, per buffer
   // per-warp epilogue staging: CPW tokens x 32 V rows of bf16
-  uint16_t *gE = reinterpret_cast<uint16_t *>(gbase + kABytes + 2 * kBBytes);
-  uint64_t *bars = reinterpret_cast<uint64_t *>(gbase + kABytes + 2 * kBBytes + kEpiBytes);
+  uint16_t *gE = reinterpret_cast<uint16_t *>(gbase + L.epi_off);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(gbase + L.bar_off);
   uint32_t *misc = reinterpret_cast<uint32_t *>(bars + 4);
   // misc[0] TMEM base, misc[1] abort flag, misc[2..3] arrival counters,
   // misc[4] last unit whose MMAs were issued (+1)
@@ -148,6 +174,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const bool pass = (layout == kPassthrough);
   const float kNegInf = __int_as_float(0xFF800000);
   const int nb = (n + JB - 1) / JB;  // load batches per unit
+  int np2 = 1;                       // n rounded up to a power of two
+  while (np2 < n) np2 <<= 1;
 
   // A cursor over the CTA's units: head and token tile, advanced one unit at
   // a time (no division in the loop).
@@ -230,9 +258,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         continue;
       }
       const float l = sane(lv[tk]);
-      float m = l;
-#pragma unroll
-      for (int s = 16; s > 0; s >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
+      float m = l;  // max over lanes 0 .. np2-1 (lanes >= n hold -inf)
+      for (int s = 1; s < np2; s <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
       if (m == kNegInf) m = 0.0f;
       const float e = (lane < n) ? exp2f(__fmul_rn(__fsub_rn(l, m), kLog2e)) : 0.0f;
       float Z = 0.0f;  // sequential fp32 sum in partial order
@@ -296,8 +323,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   };
 
-  // W_V[h] -> the swizzled bf16 A tile: bf16 rows copied, MXFP4 codes +
-  // scales turned into their exact bf16 values.
+  // W_V[h] -> shared memory: bf16 rows into the swizzled bf16 A tile, or
+  // MXFP4 code rows into the swizzled E2M1 A tile plus the scale atoms (atom
+  // g, line r: the scales of K blocks 4g..4g+3 of rows r, r+32, r+64, r+96).
   auto load_wv = [&](int h) {
     if (WFMT == 0) {
       const uint16_t *wb = static_cast<const uint16_t *>(p.w_v) + (long long)h * p.w_sh;
@@ -313,24 +341,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int s = threadIdx.x + i * kTcThreads;
         *reinterpret_cast<uint4 *>(gA + sw128_offset(s >> 6, s & 63, kV)) = x[i];
       }
-      return;
-    }
-    const uint8_t *wbase = static_cast<const uint8_t *>(p.w_v) + (long long)h * p.w_sh;
-    const uint8_t *sbase_h = p.w_scale + (long long)h * p.s_sh;
-    constexpr int kPer = kV * 64 / kTcThreads;  // 16-byte chunks per thread
-#pragma unroll 4
-    for (int i = 0; i < kPer; ++i) {
-      const int s = threadIdx.x + i * kTcThreads;
-      const int v = s >> 6, c = s & 63;
-      const uint32_t codes = __ldg(reinterpret_cast<const uint32_t *>(wbase + (long long)v * p.w_sv) + c);
-      const float scale = e8m0_to_f32(__ldg(sbase_h + (long long)v * p.s_sv + (c >> 2)));
-      uint32_t pk[4];
+    } else {
+      const uint8_t *wb = static_cast<const uint8_t *>(p.w_v) + (long long)h * p.w_sh;
+      constexpr int kPer = kV * 16 / kTcThreads;  // 16-byte code chunks per thread
+      uint4 x[kPer];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t h2 = f16x2_from_e2m1x2((codes >> (8 * q)) & 0xFFu);
-        pk[q] = pack_bf16(f16_lo(h2) * scale, f16_hi(h2) * scale);
+      for (int i = 0; i < kPer; ++i) {
+        const int s = threadIdx.x + i * kTcThreads;
+        x[i] = __ldg(reinterpret_cast<const uint4 *>(wb + (long long)(s >> 4) * p.w_sv) + (s & 15));
       }
-      *reinterpret_cast<uint4 *>(gA + sw128_offset(v, c, kV)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int s = threadIdx.x + i * kTcThreads;
+        const int v = s >> 4, c = s & 15;  // row, 16-byte chunk (32 codes)
+        *reinterpret_cast<uint4 *>(gA + (c >> 3) * (kV * 128) + v * 128 + (((c & 7) ^ (v & 7)) << 4)) = x[i];
+      }
+      // scales: thread -> (row v, group g)
+      const int v = threadIdx.x >> 2, g = threadIdx.x & 3;
+      const uint8_t *sr = p.w_scale + (long long)h * p.s_sh + (long long)v * p.s_sv + 4 * g;
+      const uint32_t word = (uint32_t)__ldg(sr) | ((uint32_t)__ldg(sr + 1) << 8) | ((uint32_t)__ldg(sr + 2) << 16) |
+                            ((uint32_t)__ldg(sr + 3) << 24);
+      *reinterpret_cast<uint32_t *>(gSFA + g * 512 + (v & 31) * 16 + (v >> 5) * 4) = word;
     }
   };
 
@@ -339,12 +370,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int b = i & 1;
     tc_fence_after();
     const uint32_t d = tmem + (uint32_t)(b * BN);
-    const uint32_t sB = sB0 + (uint32_t)b * kBBytes;
+    const uint32_t sB = sB0 + (uint32_t)b * L.b_bytes;
+    if (WFMT == 0) {
+      constexpr uint32_t kIdesc = idesc_bf16(128, BN);
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      const uint32_t kb = k >> 2, kk = k & 3;
-      tc_mma_f16(d, smem_desc_sw128(sA + kb * 16384u + kk * 32u),
-                 smem_desc_sw128(sB + kb * (uint32_t)(BN * 128) + kk * 32u), kIdesc, k > 0 ? 1u : 0u);
+      for (int k = 0; k < 32; ++k) {
+        const uint32_t kb = k >> 2, kk = k & 3;
+        tc_mma_f16(d, smem_desc_sw128(sA + kb * 16384u + kk * 32u),
+                   smem_desc_sw128(sB + kb * (uint32_t)(BN * 128) + kk * 32u), kIdesc, k > 0 ? 1u : 0u);
+      }
+    } else {
+      constexpr uint32_t kIdesc = idesc_mxf4(128, BN);
+      const uint32_t sfa = tmem + L.sfa_col + 16u * (uint32_t)b, sfb = tmem + L.sfb_col + 16u * (uint32_t)b;
+      const uint32_t sSFA = smem_u32(gSFA), sSFB = smem_u32(gSFB0) + (uint32_t)b * 2048u;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        tc_cp_32x128b_warpx4(sfa + 4u * g, smem_desc_rows16(sSFA + 512u * g));
+        tc_cp_32x128b_warpx4(sfb + 4u * g, smem_desc_rows16(sSFB + 512u * g));
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {  // K = 64 per step: two 32-blocks, scale word k/2, bytes 2(k%2)..
+        const uint32_t kb = k >> 2, kk = k & 3;
+        tc_mma_mxf4(d, smem_desc_sw128(sA + kb * (uint32_t)(kV * 128) + kk * 32u),
+                    smem_desc_sw128(sB + kb * (uint32_t)(BN * 128) + kk * 32u),
+                    kIdesc | idesc_sf_ids(2u * (k & 1)), sfa + 4u * (k >> 1), sfb + 4u * (k >> 1), k > 0 ? 1u : 0u);
+      }
     }
     tc_commit(bar_mma0 + 8 * b);
     misc[4] = (uint32_t)(i + 1);
@@ -357,7 +407,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // previous unit's accumulator.
   auto finish = [&](int i, const Cur &c, const Cur &cp, const Buf &raw_rows) -> bool {
     const int b = i & 1;
-    uint8_t *gB = gB0 + (size_t)b * kBBytes;
+    uint8_t *gB = gB0 + (size_t)b * L.b_bytes;
 #pragma unroll
     for (int tk = 0; tk < TPW; ++tk) {
       const bool valid = c.tile * BN + warp * TPW + tk < p.S;
@@ -377,9 +427,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           x = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
-        if (WFMT == 1) x = mx_chunk(x);
-        if (!valid) x = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4 *>(gB + sw128_offset(row, lane + 32 * cc, BN)) = x;
+        if (WFMT == 0) {
+          if (!valid) x = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4 *>(gB + sw128_offset(row, lane + 32 * cc, BN)) = x;
+        } else {
+          // codes of elements 256cc + 8 lane .. +7: K block cc of the row,
+          // bytes 4 lane .. 4 lane + 3; the scale of block 8cc + lane/4
+          uint32_t sc;
+          uint32_t w = mx_codes(x, sc);
+          if (!valid) {
+            w = 0u;
+            sc = 127u;
+          }
+          *reinterpret_cast<uint32_t *>(gB + cc * (BN * 128) + row * 128 + ((((lane >> 2) ^ (row & 7))) << 4) +
+                                        4 * (lane & 3)) = w;
+          if ((lane & 3) == 0) {
+            const int blk = 8 * cc + (lane >> 2);
+            gSFB0[(size_t)b * 2048 + (blk >> 2) * 512 + row * 16 + (blk & 3)] = (uint8_t)sc;
+          }
+        }
       }
     }
     fence_proxy_async_smem();
@@ -508,11 +574,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
-size_t tc_smem_bytes(int tile) { return 1024 + kABytes + 2u * (size_t)tile * 1024u + kEpiBytes + 128; }
+size_t tc_smem_bytes(int tile, int w_fmt) { return 1024 + tc_layout(tile, w_fmt).total; }
 
 template <int BN, int WFMT>
 static cudaError_t launch_one(const KParams &p, int grid, cudaStream_t s) {
-  const size_t smem = tc_smem_bytes(BN);
+  const size_t smem = tc_smem_bytes(BN, WFMT);
   cudaError_t e = cudaFuncSetAttribute(tc_kernel<BN, WFMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   tc_kernel<BN, WFMT><<<grid, kTcThreads, smem, s>>>(p);

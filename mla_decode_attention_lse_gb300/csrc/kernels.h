@@ -15,7 +15,7 @@ cudaError_t launch_simt(const KParams &p, cudaStream_t stream);
 constexpr int kTcWarps = 16;
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kTcMaxPart = 32;
-size_t tc_smem_bytes(int tile);
+size_t tc_smem_bytes(int tile, int w_fmt);
 cudaError_t launch_tc(const KParams &p, int grid, cudaStream_t stream);
 
 }  // namespace mla
