@@ -78,11 +78,12 @@ _lib = None
 
 
 def load_library(path: str | None = None):
-    """Load the CUDA library (built in-tree by ``build.build()``)."""
+    """Load the CUDA library (built in-tree by ``build.build()``; the
+    environment variable ``MLA_COMBINE_UV_LIB`` names another build)."""
     global _lib
     if _lib is not None:
         return _lib
-    path = path or LIB_PATH
+    path = path or os.environ.get("MLA_COMBINE_UV_LIB") or LIB_PATH
     if not os.path.exists(path):
         raise ImportError(
             f"{path} is missing: build it with `python -m mla_decode_attention_lse_gb300.build` "

@@ -11,7 +11,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/mla_combine_uv.h"
+#include "mla_combine_uv.h"
 #include "kernels.h"
 
 namespace {

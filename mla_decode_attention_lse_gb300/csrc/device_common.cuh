@@ -210,6 +210,11 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_cta(uint32_t addr, uint32_t
   return old;
 }
 
+// Bulk prefetch of a global range into L2 (size a multiple of 16 bytes).
+__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // ---- proxies, TMA, tcgen05 --------------------------------------------
 
 // Make this thread's generic-proxy shared-memory writes visible to the async

@@ -249,6 +249,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   };
 
+  // L2 prefetch of a unit's live partial rows: lane j prefetches partial j's
+  // 1-KiB row of each of the warp's tokens when its LSE is finite (the rows
+  // the merge will read), so the merge's own loads hit L2.  Used with bf16
+  // W_V, where the merge is latency-bound; with MXFP4 W_V (more arithmetic
+  // per row between loads) it measured slower and is left out.
+  auto prefetch_rows = [&](const Cur &c, const float (&lv)[TPW]) {
+    if (WFMT != 0) return;
+#pragma unroll
+    for (int tk = 0; tk < TPW; ++tk) {
+      const int t = c.tile * BN + warp * TPW + tk;
+      const bool live = pass ? (lane == 0 && t < p.S) : isfinite(lv[tk]);
+      if (live) {
+        const int r0 = (layout == kRequestMajor) ? (t / p.q) * p.spr : 0;
+        prefetch_l2_bulk(p.o + (long long)t * p.o_st + (long long)c.h * p.o_sh + (long long)(r0 + lane) * p.o_sp,
+                         kD * 2);
+      }
+    }
+  };
+
   // Weight of partial `lane` per token (LSE rule; one partial passes through).
   auto weights_of = [&](const float (&lv)[TPW], float (&wg)[TPW]) {
 #pragma unroll
@@ -492,6 +511,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     advance(cl);
     if (nu > 2) load_lse(cl, lse2);
     advance(cl);
+    {
+      Cur c1 = c_first;
+      advance(c1);
+      if (nu > 1) prefetch_rows(c1, lse1);
+    }
     load_wv(c_first.h);
     weights_of(lse0, wcur);
     issue(cu, 0, bufA, wA, wcur);
@@ -509,6 +533,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         weights_of(lse1, wnxt);
 #pragma unroll
         for (int tk = 0; tk < TPW; ++tk) lse1[tk] = lse2[tk];
+        if (i + 2 < nu) {
+          Cur c2 = cn;  // unit i+1; lse1 now holds unit i+2's LSE
+          advance(c2);
+          prefetch_rows(c2, lse1);
+        }
         if (i + 3 < nu) load_lse(cl, lse2);
         advance(cl);
         issue(cn, 0, nxt, wn, wnxt);
