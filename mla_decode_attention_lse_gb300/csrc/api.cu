@@ -94,11 +94,14 @@ int32_t plan_impl(const mla_combine_uv_args *a, int32_t num_sms, mla_plan *pl, K
   } else {
     if (num_sms <= 0) return MLA_ERR_SHAPE;
     int tile = a->tile_tokens;
+    // 32-token tiles once they give every SM a unit, else 16-token tiles
+    // (with MXFP4 W_V on two CTAs per SM)
     if (tile == 0) tile = ((int64_t)a->H * ((S + 31) / 32) >= num_sms) ? 32 : 16;
     pl->tile_tokens = tile;
     pl->units = a->H * ((S + tile - 1) / tile);
-    pl->grid = pl->units < num_sms ? pl->units : num_sms;
-    pl->threads = mla::kTcThreads;
+    const int slots = num_sms * mla::tc_ctas_per_sm(tile, a->w_fmt);
+    pl->grid = pl->units < slots ? pl->units : slots;
+    pl->threads = mla::tc_warps(tile, a->w_fmt) * 32;
     pl->smem_bytes = (int32_t)mla::tc_smem_bytes(tile, a->w_fmt);
   }
 

@@ -52,32 +52,39 @@ namespace mla {
 
 namespace {
 
-constexpr int kWorkers = kTcWarps;  // all warps combine, drain and (one of them) issue
 
 // Shared memory and TMEM plan of one CTA.
 struct TcLayout {
   uint32_t a_bytes, b_off, b_bytes, sfa_off, sfb_off, epi_off, bar_off, total;
   uint32_t tmem_cols, sfa_col, sfb_col;
 };
-__host__ __device__ constexpr TcLayout tc_layout(int BN, int WFMT) {
+// Pipeline stages (latent buffers, TMEM accumulators, latent scale buffers):
+// the epilogue of unit i - (stages - 1) runs after unit i is merged, giving
+// the MMAs of a unit a full unit of slack.  bf16 W_V with 32-token tiles only
+// has shared memory for two.
+__host__ __device__ constexpr int tc_stages(int BN, int WFMT) { return (WFMT == 0 && BN == 32) ? 2 : 3; }
+__host__ __device__ constexpr TcLayout tc_layout(int BN, int WFMT, int NW) {
   TcLayout L{};
+  const uint32_t st = (uint32_t)tc_stages(BN, WFMT);
   L.a_bytes = WFMT ? 128u * 256u : 128u * 1024u;           // W_V[h]: E2M1 codes or bf16
   L.b_off = L.a_bytes;
   L.b_bytes = WFMT ? (uint32_t)BN * 256u : (uint32_t)BN * 1024u;  // one latent buffer
-  L.sfa_off = L.b_off + 2 * L.b_bytes;
+  L.sfa_off = L.b_off + st * L.b_bytes;
   L.sfb_off = L.sfa_off + (WFMT ? 2048u : 0u);
-  L.epi_off = L.sfb_off + (WFMT ? 2u * 2048u : 0u);
-  L.bar_off = L.epi_off + kTcWarps * 8u * 32u * 2u;         // epilogue staging, 8 KiB
+  L.epi_off = L.sfb_off + (WFMT ? st * 2048u : 0u);
+  L.bar_off = L.epi_off + (uint32_t)NW * (4u * (uint32_t)BN / (uint32_t)NW) * 64u;  // epilogue staging
   L.total = L.bar_off + 128u;
-  // TMEM: two fp32 accumulators of BN columns; MXFP4 adds two 16-column
-  // scale regions for W_V and two for the latents (columns 64..127)
-  const uint32_t acc = 2u * (uint32_t)BN;
-  L.sfa_col = 64u;
-  L.sfb_col = 96u;
-  L.tmem_cols = WFMT ? 128u : (acc < 32u ? 32u : acc);
+  // TMEM: `st` fp32 accumulators of BN columns; MXFP4 adds a 16-column region
+  // for W_V's scales and one per stage for the latents' scales
+  const uint32_t acc = st * (uint32_t)BN;
+  L.sfa_col = (acc + 15u) & ~15u;
+  L.sfb_col = L.sfa_col + 16u;
+  const uint32_t need = WFMT ? L.sfb_col + 16u * st : acc;
+  uint32_t cols = 32u;
+  while (cols < need) cols *= 2u;
+  L.tmem_cols = cols;
   return L;
 }
-
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int *err, int code,
                                               volatile int *abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -116,16 +123,19 @@ __device__ __forceinline__ uint32_t mx_codes(uint4 x, uint32_t &sc) {
 
 }  // namespace
 
-template <int BN, int WFMT>
-__global__ void __launch_bounds__(kTcThreads, 1)
+template <int BN, int WFMT, int NW>
+__global__ void __launch_bounds__(NW * 32, 16 / NW)
     tc_kernel(const __grid_constant__ KParams p) {
-  constexpr int TPW = BN / kWorkers;       // tokens per warp per unit
+  constexpr int kWorkers = NW;             // all warps combine, drain and (one of them) issue
+  constexpr int NT = NW * 32;              // threads
+  constexpr int TPW = BN / NW;             // tokens per warp per unit
   constexpr int JB = 4 / TPW;              // partials per batch: 4 rows (8 x 16 B per lane)
-  constexpr int CPW = BN / 4;              // TMEM columns each warp drains
-  constexpr TcLayout L = tc_layout(BN, WFMT);
+  constexpr int CPW = 4 * BN / NW;         // TMEM columns each warp drains
+  constexpr TcLayout L = tc_layout(BN, WFMT, NW);
   constexpr uint32_t kCols = L.tmem_cols;
-  static_assert(TPW >= 1 && BN % kWorkers == 0 && JB >= 1, "tile must split over the warps");
-  static_assert(CPW == 4 || CPW == 8, "epilogue drains 4 or 8 columns per warp");
+  constexpr int ST = tc_stages(BN, WFMT);
+  static_assert(TPW >= 1 && BN % NW == 0 && JB >= 1 && NW % 4 == 0, "tile must split over the warps");
+  static_assert(CPW == 4 || CPW == 8 || CPW == 16, "epilogue drains 4, 8 or 16 columns per warp");
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -141,17 +151,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint16_t *gE = reinterpret_cast<uint16_t *>(gbase + L.epi_off);
   uint64_t *bars = reinterpret_cast<uint64_t *>(gbase + L.bar_off);
   uint32_t *misc = reinterpret_cast<uint32_t *>(bars + 4);
-  // misc[0] TMEM base, misc[1] abort flag, misc[2..3] arrival counters,
-  // misc[4] last unit whose MMAs were issued (+1)
+  // misc[0] TMEM base, misc[1] abort flag, misc[2] last unit whose MMAs were
+  // issued (+1), misc[4..4+ST) arrival counters (one per stage)
   volatile int *s_abort = reinterpret_cast<volatile int *>(&misc[1]);
-  const uint32_t bar_mma0 = smem_u32(&bars[0]);  // +8*b
-  const uint32_t cnt0 = smem_u32(&misc[2]);      // +4*b
+  const uint32_t bar_mma0 = smem_u32(&bars[0]);  // +8*b, one per stage
+  const uint32_t cnt0 = smem_u32(&misc[4]);      // +4*b
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(bar_mma0, 1u);
-    mbar_init(bar_mma0 + 8, 1u);
-    for (int k = 1; k < 6; ++k) misc[k] = 0u;
+    for (int b = 0; b < ST; ++b) mbar_init(bar_mma0 + 8 * b, 1u);
+    for (int k = 1; k < 4 + ST; ++k) misc[k] = 0u;
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -194,22 +203,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // memory, token-major) * gate -> core with 16-byte accesses.
   uint16_t *stage = gE + warp * (CPW * 32);
   auto epilogue = [&](int j, const Cur &c) -> bool {
-    const int bj = j & 1;
-    // lane -> (token e, 8 consecutive V rows)
-    constexpr int kLanes = CPW * 4;
-    const int e = lane >> 2, v8 = (lane & 3) * 8;
-    const int t = c.tile * BN + ws * CPW + e;
-    const bool act = lane < kLanes && t < p.S;
-    const long long off = (long long)t * Wrow + c.h * kV + wq * 32 + v8;
-    uint4 g = make_uint4(0, 0, 0, 0);
-    if (act) g = __ldg(reinterpret_cast<const uint4 *>(p.gate + off));
-    bool ok = wait_or_abort(bar_mma0 + 8 * bj, (j >> 1) & 1, p.err, kErrWaitMma, s_abort);
+    const int bj = j % ST;
+    // lane -> (token e0 + lane/4, 8 consecutive V rows)
+    constexpr int kRounds = (CPW + 7) / 8;
+    const int v8 = (lane & 3) * 8;
+    uint4 g[kRounds];
+    long long off[kRounds];
+    bool act[kRounds];
+#pragma unroll
+    for (int rd = 0; rd < kRounds; ++rd) {
+      const int e = rd * 8 + (lane >> 2);
+      const int t = c.tile * BN + ws * CPW + e;
+      act[rd] = e < CPW && t < p.S;
+      off[rd] = (long long)t * Wrow + c.h * kV + wq * 32 + v8;
+      g[rd] = act[rd] ? __ldg(reinterpret_cast<const uint4 *>(p.gate + off[rd])) : make_uint4(0, 0, 0, 0);
+    }
+    bool ok = wait_or_abort(bar_mma0 + 8 * bj, (uint32_t)(j / ST) & 1u, p.err, kErrWaitMma, s_abort);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) return false;
     tc_fence_after();
     uint32_t r[CPW];
     const uint32_t taddr = tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(bj * BN + ws * CPW);
-    if constexpr (CPW == 8) {
+    if constexpr (CPW == 16) {
+      tmem_ld_x16(taddr, r);
+    } else if constexpr (CPW == 8) {
       tmem_ld_x8(taddr, r);
     } else {
       tmem_ld_x4(taddr, r);
@@ -222,14 +239,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       stage[x * 32 + lane] = *reinterpret_cast<const uint16_t *>(&a);
     }
     __syncwarp();
-    if (act) {
-      const uint4 a = *reinterpret_cast<const uint4 *>(stage + e * 32 + v8);
-      const uint32_t aa[4] = {a.x, a.y, a.z, a.w}, gg[4] = {g.x, g.y, g.z, g.w};
-      uint32_t o[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        o[q] = pack_bf16(bf16_lo(aa[q]) * bf16_lo(gg[q]), bf16_hi(aa[q]) * bf16_hi(gg[q]));
-      *reinterpret_cast<uint4 *>(p.out + off) = make_uint4(o[0], o[1], o[2], o[3]);
+    for (int rd = 0; rd < kRounds; ++rd) {
+      if (act[rd]) {
+        const int e = rd * 8 + (lane >> 2);
+        const uint4 a = *reinterpret_cast<const uint4 *>(stage + e * 32 + v8);
+        const uint32_t aa[4] = {a.x, a.y, a.z, a.w}, gg[4] = {g[rd].x, g[rd].y, g[rd].z, g[rd].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          o[q] = pack_bf16(bf16_lo(aa[q]) * bf16_lo(gg[q]), bf16_hi(aa[q]) * bf16_hi(gg[q]));
+        *reinterpret_cast<uint4 *>(p.out + off[rd]) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
     }
     __syncwarp();
     return true;
@@ -348,45 +369,54 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   auto load_wv = [&](int h) {
     if (WFMT == 0) {
       const uint16_t *wb = static_cast<const uint16_t *>(p.w_v) + (long long)h * p.w_sh;
-      constexpr int kPer = kV * 64 / kTcThreads;
-      uint4 x[kPer];
+      constexpr int kChunks = kV * 64;  // 16-byte chunks of the bf16 tile
+      constexpr int kPer = 16;          // per pass and thread
+#pragma unroll 1
+      for (int s0 = 0; s0 < kChunks; s0 += kPer * NT) {
+        uint4 x[kPer];
 #pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        const int s = threadIdx.x + i * kTcThreads;
-        x[i] = __ldg(reinterpret_cast<const uint4 *>(wb + (long long)(s >> 6) * p.w_sv) + (s & 63));
-      }
+        for (int i = 0; i < kPer; ++i) {
+          const int s = s0 + threadIdx.x + i * NT;
+          x[i] = __ldg(reinterpret_cast<const uint4 *>(wb + (long long)(s >> 6) * p.w_sv) + (s & 63));
+        }
 #pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        const int s = threadIdx.x + i * kTcThreads;
-        *reinterpret_cast<uint4 *>(gA + sw128_offset(s >> 6, s & 63, kV)) = x[i];
+        for (int i = 0; i < kPer; ++i) {
+          const int s = s0 + threadIdx.x + i * NT;
+          *reinterpret_cast<uint4 *>(gA + sw128_offset(s >> 6, s & 63, kV)) = x[i];
+        }
       }
     } else {
       const uint8_t *wb = static_cast<const uint8_t *>(p.w_v) + (long long)h * p.w_sh;
-      constexpr int kPer = kV * 16 / kTcThreads;  // 16-byte code chunks per thread
+      constexpr int kPer = kV * 16 / NT;  // 16-byte code chunks per thread
       uint4 x[kPer];
 #pragma unroll
       for (int i = 0; i < kPer; ++i) {
-        const int s = threadIdx.x + i * kTcThreads;
+        const int s = threadIdx.x + i * NT;
         x[i] = __ldg(reinterpret_cast<const uint4 *>(wb + (long long)(s >> 4) * p.w_sv) + (s & 15));
       }
 #pragma unroll
       for (int i = 0; i < kPer; ++i) {
-        const int s = threadIdx.x + i * kTcThreads;
+        const int s = threadIdx.x + i * NT;
         const int v = s >> 4, c = s & 15;  // row, 16-byte chunk (32 codes)
         *reinterpret_cast<uint4 *>(gA + (c >> 3) * (kV * 128) + v * 128 + (((c & 7) ^ (v & 7)) << 4)) = x[i];
       }
-      // scales: thread -> (row v, group g)
-      const int v = threadIdx.x >> 2, g = threadIdx.x & 3;
-      const uint8_t *sr = p.w_scale + (long long)h * p.s_sh + (long long)v * p.s_sv + 4 * g;
-      const uint32_t word = (uint32_t)__ldg(sr) | ((uint32_t)__ldg(sr + 1) << 8) | ((uint32_t)__ldg(sr + 2) << 16) |
-                            ((uint32_t)__ldg(sr + 3) << 24);
-      *reinterpret_cast<uint32_t *>(gSFA + g * 512 + (v & 31) * 16 + (v >> 5) * 4) = word;
+      // scales: (row v, group g) tasks
+#pragma unroll
+      for (int s = threadIdx.x; s < kV * 4; s += NT) {
+        const int v = s >> 2, g = s & 3;
+        const uint8_t *sr = p.w_scale + (long long)h * p.s_sh + (long long)v * p.s_sv + 4 * g;
+        const uint32_t word = (uint32_t)__ldg(sr) | ((uint32_t)__ldg(sr + 1) << 8) |
+                              ((uint32_t)__ldg(sr + 2) << 16) | ((uint32_t)__ldg(sr + 3) << 24);
+        *reinterpret_cast<uint32_t *>(gSFA + g * 512 + (v & 31) * 16 + (v >> 5) * 4) = word;
+      }
     }
   };
 
   // The unit's MMAs (one thread): D[v, t] = sum_k W_V[h][v][k] * lat[t][k].
-  auto issue_mma = [&](int i) {
-    const int b = i & 1;
+  // `first` marks the first unit of a head in this CTA: W_V's scales go to
+  // TMEM then (every earlier MMA is complete by that time).
+  auto issue_mma = [&](int i, bool first) {
+    const int b = i % ST;
     tc_fence_after();
     const uint32_t d = tmem + (uint32_t)(b * BN);
     const uint32_t sB = sB0 + (uint32_t)b * L.b_bytes;
@@ -400,13 +430,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     } else {
       constexpr uint32_t kIdesc = idesc_mxf4(128, BN);
-      const uint32_t sfa = tmem + L.sfa_col + 16u * (uint32_t)b, sfb = tmem + L.sfb_col + 16u * (uint32_t)b;
+      const uint32_t sfa = tmem + L.sfa_col, sfb = tmem + L.sfb_col + 16u * (uint32_t)b;
       const uint32_t sSFA = smem_u32(gSFA), sSFB = smem_u32(gSFB0) + (uint32_t)b * 2048u;
+      if (first) {
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        tc_cp_32x128b_warpx4(sfa + 4u * g, smem_desc_rows16(sSFA + 512u * g));
-        tc_cp_32x128b_warpx4(sfb + 4u * g, smem_desc_rows16(sSFB + 512u * g));
+        for (int g = 0; g < 4; ++g) tc_cp_32x128b_warpx4(sfa + 4u * g, smem_desc_rows16(sSFA + 512u * g));
       }
+#pragma unroll
+      for (int g = 0; g < 4; ++g) tc_cp_32x128b_warpx4(sfb + 4u * g, smem_desc_rows16(sSFB + 512u * g));
 #pragma unroll
       for (int k = 0; k < 8; ++k) {  // K = 64 per step: two 32-blocks, scale word k/2, bytes 2(k%2)..
         const uint32_t kb = k >> 2, kk = k & 3;
@@ -416,16 +447,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
     tc_commit(bar_mma0 + 8 * b);
-    misc[4] = (uint32_t)(i + 1);
+    misc[2] = (uint32_t)(i + 1);
   };
 
-  bool ep_early = false;  // epilogue of the previous unit already done
+  int drained = 0;        // next unit whose accumulator is drained
+  Cur cdr = c_first;      // its cursor
+  auto drain_to = [&](int last) -> bool {  // epilogues of units drained .. last
+    while (drained <= last) {
+      if (!epilogue(drained, cdr)) return false;
+      ++drained;
+      advance(cdr);
+    }
+    return true;
+  };
 
   // Unit i (cursor c; previous unit at cp) has its latents merged: round /
   // quantise, store, arrive (the last warp issues the MMAs), then drain the
   // previous unit's accumulator.
-  auto finish = [&](int i, const Cur &c, const Cur &cp, const Buf &raw_rows) -> bool {
-    const int b = i & 1;
+  auto finish = [&](int i, const Cur &c, const Buf &raw_rows) -> bool {
+    const int b = i % ST;
     uint8_t *gB = gB0 + (size_t)b * L.b_bytes;
 #pragma unroll
     for (int tk = 0; tk < TPW; ++tk) {
@@ -470,23 +510,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      // arrivals on buffer b are numbered across its uses: use (i >> 1) takes
-      // numbers (i >> 1) * kWorkers .. + kWorkers - 1; the last one issues
+      // arrivals on stage b are numbered across its uses: use i / ST takes
+      // numbers (i / ST) * kWorkers .. + kWorkers - 1; the last one issues
       const uint32_t prev = atom_add_acq_rel_cta(cnt0 + 4 * b, 1u);
-      if (prev == (uint32_t)((i >> 1) + 1) * kWorkers - 1u) issue_mma(i);
+      if (prev == (uint32_t)(i / ST + 1) * kWorkers - 1u) issue_mma(i, i == 0 || c.tile == 0);
     }
     __syncwarp();
-    bool ok = true;
-    if (i > 0 && !ep_early) ok = epilogue(i - 1, cp);
-    ep_early = false;
+    // drain the accumulator of unit i - (ST - 1); before the next unit of
+    // another head, drain everything (W_V is replaced once those MMAs are done)
+    const bool head_change = i + 1 < nu && c.tile + 1 == tph;
+    bool ok = drain_to(head_change ? i : i - (ST - 1));
     clear_acc();
-    // next unit on another head: W_V must be replaced once this unit's MMAs
-    // are complete
-    if (ok && i + 1 < nu && c.tile + 1 == tph) {
-      ok = epilogue(i, c);
-      ep_early = true;
-      if (ok) load_wv(c.h + 1);
-    }
+    if (ok && head_change) load_wv(c.h + 1);
     return ok;
   };
 
@@ -498,7 +533,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   Buf bufA, bufB;
   Wts wA, wB;
   Cur cu = c_first;    // unit i (being merged)
-  Cur cprev = c_first; // unit i-1
   Cur cn = c_first;    // unit of the next batch to issue
   Cur cl = c_first;    // next unit whose LSE is loaded (i+3)
   int i = 0, bi = 0;   // unit and batch being merged
@@ -551,10 +585,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     consume(cur, wc);
     if (++bi == nb) {
-      if (!finish(i, cu, cprev, cur)) return false;
+      if (!finish(i, cu, cur)) return false;
 #pragma unroll
       for (int tk = 0; tk < TPW; ++tk) wcur[tk] = wnxt[tk];
-      cprev = cu;
       advance(cu);
       ++i;
       bi = 0;
@@ -576,7 +609,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       break;
     }
   }
-  if (ok && nu > 0 && !*s_abort) epilogue(nu - 1, cprev);
+  if (ok && nu > 0 && !*s_abort) drain_to(nu - 1);
 
   // rows S .. S_out-1 of core are zero (this CTA's slice of them)
   const long long n16 = (long long)(p.S_out - p.S) * p.H * (kV * 2 / 16);
@@ -584,16 +617,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const long long zb = (long long)blockIdx.x * n16 / gridDim.x;
     const long long ze = (long long)(blockIdx.x + 1) * n16 / gridDim.x;
     uint4 *dst = reinterpret_cast<uint4 *>(p.out + (long long)p.S * Wrow);
-    for (long long k = zb + threadIdx.x; k < ze; k += kTcThreads) dst[k] = make_uint4(0, 0, 0, 0);
+    for (long long k = zb + threadIdx.x; k < ze; k += NT) dst[k] = make_uint4(0, 0, 0, 0);
   }
 
   __syncthreads();
   if (threadIdx.x == 0) {
     // drain what this CTA started (only pending after an abort): the last
     // committed MMAs
-    if (misc[4] > 0u) {
-      const int last = (int)misc[4] - 1;
-      mbar_wait(bar_mma0 + 8 * (last & 1), (last >> 1) & 1, p.err, kErrWaitTeardown);
+    if (misc[2] > 0u) {
+      const int last = (int)misc[2] - 1;
+      mbar_wait(bar_mma0 + 8 * (last % ST), (uint32_t)(last / ST) & 1u, p.err, kErrWaitTeardown);
     }
   }
   __syncthreads();
@@ -603,20 +636,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
-size_t tc_smem_bytes(int tile, int w_fmt) { return 1024 + tc_layout(tile, w_fmt).total; }
+// MXFP4 W_V with 16-token tiles: two 8-warp CTAs per SM (64 KiB of shared
+// memory each, independent pipelines); otherwise one 16-warp CTA per SM.
+int tc_warps(int tile, int w_fmt) { return (w_fmt && tile == 16) ? 8 : 16; }
+int tc_ctas_per_sm(int tile, int w_fmt) { return (w_fmt && tile == 16) ? 2 : 1; }
 
-template <int BN, int WFMT>
+size_t tc_smem_bytes(int tile, int w_fmt) { return 1024 + tc_layout(tile, w_fmt, tc_warps(tile, w_fmt)).total; }
+
+template <int BN, int WFMT, int NW>
 static cudaError_t launch_one(const KParams &p, int grid, cudaStream_t s) {
   const size_t smem = tc_smem_bytes(BN, WFMT);
-  cudaError_t e = cudaFuncSetAttribute(tc_kernel<BN, WFMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(tc_kernel<BN, WFMT, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  tc_kernel<BN, WFMT><<<grid, kTcThreads, smem, s>>>(p);
+  tc_kernel<BN, WFMT, NW><<<grid, NW * 32, smem, s>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_tc(const KParams &p, int grid, cudaStream_t stream) {
-  if (p.tile == 16) return p.w_fmt == 0 ? launch_one<16, 0>(p, grid, stream) : launch_one<16, 1>(p, grid, stream);
-  if (p.tile == 32) return p.w_fmt == 0 ? launch_one<32, 0>(p, grid, stream) : launch_one<32, 1>(p, grid, stream);
+  if (p.tile == 16) return p.w_fmt == 0 ? launch_one<16, 0, 16>(p, grid, stream) : launch_one<16, 1, 8>(p, grid, stream);
+  if (p.tile == 32) return p.w_fmt == 0 ? launch_one<32, 0, 16>(p, grid, stream) : launch_one<32, 1, 16>(p, grid, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -12,9 +12,9 @@ size_t simt_smem_bytes(int n_part);
 cudaError_t launch_simt(const KParams &p, cudaStream_t stream);
 
 // Fused tcgen05 kernel: tile = 16 or 32 tokens, n_part <= 32.
-constexpr int kTcWarps = 16;
-constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kTcMaxPart = 32;
+int tc_warps(int tile, int w_fmt);        // warps per CTA
+int tc_ctas_per_sm(int tile, int w_fmt);  // resident CTAs per SM the grid is sized for
 size_t tc_smem_bytes(int tile, int w_fmt);
 cudaError_t launch_tc(const KParams &p, int grid, cudaStream_t stream);
 
