@@ -95,14 +95,16 @@ int32_t plan_impl(const mla_combine_uv_args *a, int32_t num_sms, mla_plan *pl, K
     if (num_sms <= 0) return MLA_ERR_SHAPE;
     int tile = a->tile_tokens;
     // 32-token tiles once they give every SM a unit, else 16-token tiles
-    // (with MXFP4 W_V on two CTAs per SM)
-    if (tile == 0) tile = ((int64_t)a->H * ((S + 31) / 32) >= num_sms) ? 32 : 16;
+    // (with MXFP4 W_V on two CTAs per SM); more than 16 partials per token
+    // need 16-token tiles
+    if (tile == 0) tile = ((int64_t)a->H * ((S + 31) / 32) >= num_sms && n_part <= 16) ? 32 : 16;
+    if (n_part > mla::tc_max_part(tile, a->w_fmt)) return MLA_ERR_KERNEL;
     pl->tile_tokens = tile;
     pl->units = a->H * ((S + tile - 1) / tile);
-    const int slots = num_sms * mla::tc_ctas_per_sm(tile, a->w_fmt);
+    const int slots = num_sms * mla::tc_ctas_per_sm(tile, a->w_fmt, n_part);
     pl->grid = pl->units < slots ? pl->units : slots;
-    pl->threads = mla::tc_warps(tile, a->w_fmt) * 32;
-    pl->smem_bytes = (int32_t)mla::tc_smem_bytes(tile, a->w_fmt);
+    pl->threads = mla::tc_warps(tile, a->w_fmt, n_part) * 32;
+    pl->smem_bytes = (int32_t)mla::tc_smem_bytes(tile, a->w_fmt, n_part);
   }
 
   if (kp) {

@@ -140,6 +140,33 @@ __device__ __forceinline__ uint32_t e2m1x2_from_f32(float lo, float hi) {
   return r;
 }
 
+// Eight bf16 values (four packed pairs) times an exact power of two -> eight
+// E2M1 codes (nearest even, saturating at 6), element 2i in the low nibble of
+// byte i.
+__device__ __forceinline__ uint32_t e2m1x8_from_bf16x8(const uint32_t (&u)[4], float scale) {
+  uint32_t r;
+  asm("{\n\t"
+      ".reg .b8 c0, c1, c2, c3;\n\t"
+      ".reg .f32 l0, h0, l1, h1, l2, h2, l3, h3;\n\t"
+      "shl.b32 l0, %1, 16;\n\tand.b32 h0, %1, 0xffff0000;\n\t"
+      "shl.b32 l1, %2, 16;\n\tand.b32 h1, %2, 0xffff0000;\n\t"
+      "shl.b32 l2, %3, 16;\n\tand.b32 h2, %3, 0xffff0000;\n\t"
+      "shl.b32 l3, %4, 16;\n\tand.b32 h3, %4, 0xffff0000;\n\t"
+      "mul.rn.f32 l0, l0, %5;\n\tmul.rn.f32 h0, h0, %5;\n\t"
+      "mul.rn.f32 l1, l1, %5;\n\tmul.rn.f32 h1, h1, %5;\n\t"
+      "mul.rn.f32 l2, l2, %5;\n\tmul.rn.f32 h2, h2, %5;\n\t"
+      "mul.rn.f32 l3, l3, %5;\n\tmul.rn.f32 h3, h3, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c0, h0, l0;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c1, h1, l1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c2, h2, l2;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c3, h3, l3;\n\t"
+      "mov.b32 %0, {c0, c1, c2, c3};\n\t"
+      "}"
+      : "=r"(r)
+      : "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "f"(scale));
+  return r;
+}
+
 // An E2M1 pair (low nibble -> lo) -> two fp16 values packed as (lo, hi).
 __device__ __forceinline__ uint32_t f16x2_from_e2m1x2(uint32_t byte) {
   uint32_t r;

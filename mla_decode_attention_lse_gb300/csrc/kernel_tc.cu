@@ -115,10 +115,7 @@ __device__ __forceinline__ uint32_t mx_codes(uint4 x, uint32_t &sc) {
   sc = mx_scale_code(am);
   if (sc == 255u) return 0u;  // Inf / NaN in the block: the NaN scale carries it
   const float inv = e8m0_inverse(sc);
-  uint32_t w = 0;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) w |= e2m1x2_from_f32(bf16_lo(u[q]) * inv, bf16_hi(u[q]) * inv) << (8 * q);
-  return w;
+  return e2m1x8_from_bf16x8(u, inv);
 }
 
 }  // namespace
@@ -183,7 +180,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
   const bool pass = (layout == kPassthrough);
   const float kNegInf = __int_as_float(0xFF800000);
   const int nb = (n + JB - 1) / JB;  // load batches per unit
-  int np2 = 1;                       // n rounded up to a power of two
+  int np2 = 1;                       // n rounded up to a power of two (<= SEG)
   while (np2 < n) np2 <<= 1;
 
   // A cursor over the CTA's units: head and token tile, advanced one unit at
@@ -256,57 +253,54 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
     return true;
   };
 
-  // This lane's LSE of partial `lane` for the warp's tokens of a unit (-inf
-  // past n or past S; sanitised when used).
-  auto load_lse = [&](const Cur &c, float (&lv)[TPW]) {
-#pragma unroll
-    for (int tk = 0; tk < TPW; ++tk) {
-      const int t = c.tile * BN + warp * TPW + tk;
-      lv[tk] = kNegInf;
-      if (!pass && t < p.S && lane < n) {
-        const int r0 = (layout == kRequestMajor) ? (t / p.q) * p.spr : 0;
-        lv[tk] = __ldg(p.lse + (long long)(r0 + lane) * p.l_sp + (long long)t * p.l_st + (long long)c.h * p.l_sh);
-      }
+  // LSE values and weights are packed one (token, partial) per lane: the
+  // warp's TPW tokens take SEG = 32 / TPW lanes each, lane tk * SEG + j holding
+  // partial j of token tk (n <= SEG), so one warp-wide pass serves all of them.
+  constexpr int SEG = 32 / TPW;
+  const int my_tk = lane / SEG, my_j = lane % SEG;
+
+  // This lane's LSE (-inf past n or past S; sanitised when used).
+  auto load_lse = [&](const Cur &c, float &lv) {
+    const int t = c.tile * BN + warp * TPW + my_tk;
+    lv = kNegInf;
+    if (!pass && t < p.S && my_j < n) {
+      const int r0 = (layout == kRequestMajor) ? (t / p.q) * p.spr : 0;
+      lv = __ldg(p.lse + (long long)(r0 + my_j) * p.l_sp + (long long)t * p.l_st + (long long)c.h * p.l_sh);
     }
   };
 
-  // L2 prefetch of a unit's live partial rows: lane j prefetches partial j's
-  // 1-KiB row of each of the warp's tokens when its LSE is finite (the rows
-  // the merge will read), so the merge's own loads hit L2.  Used with bf16
-  // W_V, where the merge is latency-bound; with MXFP4 W_V (more arithmetic
-  // per row between loads) it measured slower and is left out.
-  auto prefetch_rows = [&](const Cur &c, const float (&lv)[TPW]) {
+  // L2 prefetch of a unit's live partial rows: each lane prefetches its
+  // partial's 1-KiB row when its LSE is finite (the rows the merge will
+  // read), so the merge's own loads hit L2.  Used with bf16 W_V, where the
+  // merge is latency-bound; with MXFP4 W_V (more arithmetic per row between
+  // loads) it measured slower and is left out.
+  auto prefetch_rows = [&](const Cur &c, float lv) {
     if (WFMT != 0) return;
-#pragma unroll
-    for (int tk = 0; tk < TPW; ++tk) {
-      const int t = c.tile * BN + warp * TPW + tk;
-      const bool live = pass ? (lane == 0 && t < p.S) : isfinite(lv[tk]);
-      if (live) {
-        const int r0 = (layout == kRequestMajor) ? (t / p.q) * p.spr : 0;
-        prefetch_l2_bulk(p.o + (long long)t * p.o_st + (long long)c.h * p.o_sh + (long long)(r0 + lane) * p.o_sp,
-                         kD * 2);
-      }
+    const int t = c.tile * BN + warp * TPW + my_tk;
+    const bool live = pass ? (my_j == 0 && t < p.S) : isfinite(lv);
+    if (live) {
+      const int r0 = (layout == kRequestMajor) ? (t / p.q) * p.spr : 0;
+      prefetch_l2_bulk(p.o + (long long)t * p.o_st + (long long)c.h * p.o_sh + (long long)(r0 + my_j) * p.o_sp,
+                       kD * 2);
     }
   };
 
-  // Weight of partial `lane` per token (LSE rule; one partial passes through).
-  auto weights_of = [&](const float (&lv)[TPW], float (&wg)[TPW]) {
-#pragma unroll
-    for (int tk = 0; tk < TPW; ++tk) {
-      if (pass) {
-        wg[tk] = (lane == 0) ? 1.0f : 0.0f;
-        continue;
-      }
-      const float l = sane(lv[tk]);
-      float m = l;  // max over lanes 0 .. np2-1 (lanes >= n hold -inf)
-      for (int s = 1; s < np2; s <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
-      if (m == kNegInf) m = 0.0f;
-      const float e = (lane < n) ? exp2f(__fmul_rn(__fsub_rn(l, m), kLog2e)) : 0.0f;
-      float Z = 0.0f;  // sequential fp32 sum in partial order
-      for (int j = 0; j < n; ++j) Z = __fadd_rn(Z, __shfl_sync(0xffffffffu, e, j));
-      const float inv = (Z == 0.0f) ? 0.0f : __frcp_rn(Z);
-      wg[tk] = (e == 0.0f) ? 0.0f : __fmul_rn(e, inv);
+  // This lane's weight (LSE rule; one partial passes through).
+  auto weights_of = [&](float lv, float &wg) {
+    if (pass) {
+      wg = (my_j == 0) ? 1.0f : 0.0f;
+      return;
     }
+    const float l = sane(lv);
+    float m = l;  // max over the token's lanes (np2 <= SEG; lanes past n hold -inf)
+    for (int s = 1; s < np2; s <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
+    if (m == kNegInf) m = 0.0f;
+    const float e = (my_j < n) ? exp2f(__fmul_rn(__fsub_rn(l, m), kLog2e)) : 0.0f;
+    float Z = 0.0f;  // sequential fp32 sum in partial order
+    const int seg0 = my_tk * SEG;
+    for (int j = 0; j < n; ++j) Z = __fadd_rn(Z, __shfl_sync(0xffffffffu, e, seg0 + j));
+    const float inv = (Z == 0.0f) ? 0.0f : __frcp_rn(Z);
+    wg = (e == 0.0f) ? 0.0f : __fmul_rn(e, inv);
   };
 
   using Buf = uint4[JB][TPW][2];
@@ -314,7 +308,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
 
   // Issue the loads of one batch: unit at cursor c, partials j0 .. j0+JB-1
   // (rows of zero weight and tokens past S are not read).
-  auto issue = [&](const Cur &c, int j0, Buf &buf, Wts &w, const float (&wg)[TPW]) {
+  auto issue = [&](const Cur &c, int j0, Buf &buf, Wts &w, float wg) {
 #pragma unroll
     for (int tk = 0; tk < TPW; ++tk) {
       const int t = c.tile * BN + warp * TPW + tk;
@@ -322,7 +316,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
       const uint16_t *base = p.o + (long long)t * p.o_st + (long long)c.h * p.o_sh + (long long)(r0 + j0) * p.o_sp;
 #pragma unroll
       for (int jj = 0; jj < JB; ++jj) {
-        w[jj][tk] = __shfl_sync(0xffffffffu, wg[tk], (j0 + jj) & 31);  // 0 past n
+        w[jj][tk] = __shfl_sync(0xffffffffu, wg, tk * SEG + j0 + jj);  // 0 past n
         if (w[jj][tk] != 0.0f && t < p.S) {
           const uint4 *row = reinterpret_cast<const uint4 *>(base + (long long)jj * p.o_sp);
           buf[jj][tk][0] = __ldcs(row + lane);
@@ -528,8 +522,8 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
   // ---- the pipeline: step k merges batch k while batch k+1 is in flight ----
   bool ok = true;
   clear_acc();
-  float lse1[TPW], lse2[TPW];  // LSE of units i+1 and i+2
-  float wcur[TPW], wnxt[TPW];  // weights of units i and i+1
+  float lse1 = kNegInf, lse2 = kNegInf;  // LSE of units i+1 and i+2
+  float wcur = 0.0f, wnxt = 0.0f;       // weights of units i and i+1
   Buf bufA, bufB;
   Wts wA, wB;
   Cur cu = c_first;    // unit i (being merged)
@@ -538,7 +532,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
   int i = 0, bi = 0;   // unit and batch being merged
   int nbi = 1;         // batch index of the next batch within its unit
   if (nu > 0) {
-    float lse0[TPW];
+    float lse0;
     load_lse(cl, lse0);
     advance(cl);
     if (nu > 1) load_lse(cl, lse1);
@@ -565,8 +559,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
       if (nbi == 0) {
         // the next batch opens unit i+1
         weights_of(lse1, wnxt);
-#pragma unroll
-        for (int tk = 0; tk < TPW; ++tk) lse1[tk] = lse2[tk];
+        lse1 = lse2;
         if (i + 2 < nu) {
           Cur c2 = cn;  // unit i+1; lse1 now holds unit i+2's LSE
           advance(c2);
@@ -586,8 +579,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
     consume(cur, wc);
     if (++bi == nb) {
       if (!finish(i, cu, cur)) return false;
-#pragma unroll
-      for (int tk = 0; tk < TPW; ++tk) wcur[tk] = wnxt[tk];
+      wcur = wnxt;
       advance(cu);
       ++i;
       bi = 0;
@@ -636,16 +628,21 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
   }
 }
 
-// MXFP4 W_V with 16-token tiles: two 8-warp CTAs per SM (64 KiB of shared
-// memory each, independent pipelines); otherwise one 16-warp CTA per SM.
-int tc_warps(int tile, int w_fmt) { return (w_fmt && tile == 16) ? 8 : 16; }
-int tc_ctas_per_sm(int tile, int w_fmt) { return (w_fmt && tile == 16) ? 2 : 1; }
+// Warps per CTA: 16, except MXFP4 W_V with 16-token tiles and at most 16
+// partials per token, which runs two 8-warp CTAs per SM (about 60 KiB of
+// shared memory each, independent pipelines).  A warp owns BN / warps tokens;
+// with two tokens a warp holds at most 16 partials per token.
+int tc_warps(int tile, int w_fmt, int n_part) { return (w_fmt && tile == 16 && n_part <= 16) ? 8 : 16; }
+int tc_ctas_per_sm(int tile, int w_fmt, int n_part) { return tc_warps(tile, w_fmt, n_part) == 8 ? 2 : 1; }
+int tc_max_part(int tile, int /*w_fmt*/) { return tile == 16 ? 32 : 16; }
 
-size_t tc_smem_bytes(int tile, int w_fmt) { return 1024 + tc_layout(tile, w_fmt, tc_warps(tile, w_fmt)).total; }
+size_t tc_smem_bytes(int tile, int w_fmt, int n_part) {
+  return 1024 + tc_layout(tile, w_fmt, tc_warps(tile, w_fmt, n_part)).total;
+}
 
 template <int BN, int WFMT, int NW>
 static cudaError_t launch_one(const KParams &p, int grid, cudaStream_t s) {
-  const size_t smem = tc_smem_bytes(BN, WFMT);
+  const size_t smem = 1024 + tc_layout(BN, WFMT, NW).total;
   cudaError_t e = cudaFuncSetAttribute(tc_kernel<BN, WFMT, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   tc_kernel<BN, WFMT, NW><<<grid, NW * 32, smem, s>>>(p);
@@ -653,8 +650,10 @@ static cudaError_t launch_one(const KParams &p, int grid, cudaStream_t s) {
 }
 
 cudaError_t launch_tc(const KParams &p, int grid, cudaStream_t stream) {
-  if (p.tile == 16) return p.w_fmt == 0 ? launch_one<16, 0, 16>(p, grid, stream) : launch_one<16, 1, 8>(p, grid, stream);
-  if (p.tile == 32) return p.w_fmt == 0 ? launch_one<32, 0, 16>(p, grid, stream) : launch_one<32, 1, 16>(p, grid, stream);
+  const int nw = tc_warps(p.tile, p.w_fmt, p.n_part);
+  if (p.tile == 16 && p.w_fmt == 0) return launch_one<16, 0, 16>(p, grid, stream);
+  if (p.tile == 16 && p.w_fmt == 1) return nw == 8 ? launch_one<16, 1, 8>(p, grid, stream) : launch_one<16, 1, 16>(p, grid, stream);
+  if (p.tile == 32 && p.n_part <= 16) return p.w_fmt == 0 ? launch_one<32, 0, 16>(p, grid, stream) : launch_one<32, 1, 16>(p, grid, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -13,9 +13,10 @@ cudaError_t launch_simt(const KParams &p, cudaStream_t stream);
 
 // Fused tcgen05 kernel: tile = 16 or 32 tokens, n_part <= 32.
 constexpr int kTcMaxPart = 32;
-int tc_warps(int tile, int w_fmt);        // warps per CTA
-int tc_ctas_per_sm(int tile, int w_fmt);  // resident CTAs per SM the grid is sized for
-size_t tc_smem_bytes(int tile, int w_fmt);
+int tc_warps(int tile, int w_fmt, int n_part);        // warps per CTA
+int tc_ctas_per_sm(int tile, int w_fmt, int n_part);  // resident CTAs per SM the grid is sized for
+int tc_max_part(int tile, int w_fmt);                 // partials per token the tile supports
+size_t tc_smem_bytes(int tile, int w_fmt, int n_part);
 cudaError_t launch_tc(const KParams &p, int grid, cudaStream_t stream);
 
 }  // namespace mla

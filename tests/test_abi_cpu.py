@@ -120,6 +120,13 @@ def test_kernel_and_tile_choice(lib):
     p = mla_combine_uv_plan(args(S=4096, H=96, P=4, q=4, spr=4), SMS)
     assert (p["tile_tokens"], p["units"], p["grid"]) == (32, 96 * 128, SMS)
     assert p["smem_bytes"] <= 227 * 1024
+    # 17..32 partials per token: 16-token tiles, one token per warp
+    p = mla_combine_uv_plan(args(S=4096, H=96, P=20, spr=20), SMS)
+    assert (p["kernel"], p["tile_tokens"], p["threads"]) == (m.MLA_KERNEL_TC, 16, 512)
+    assert status_of(args(P=20, spr=20, tile=32)) == m.MLA_ERR_KERNEL
+    # MXFP4 16-token tiles run two 8-warp CTAs per SM
+    p = mla_combine_uv_plan(args(S=256, H=12, P=8, spr=8, w_fmt=1), SMS)
+    assert (p["tile_tokens"], p["units"], p["grid"], p["threads"]) == (16, 192, 192, 256)
     # more than 32 partials per token: CUDA cores only
     assert mla_combine_uv_plan(args(P=64, spr=64), SMS)["kernel"] == m.MLA_KERNEL_SIMT
     assert status_of(args(P=64, spr=64, kernel=m.MLA_KERNEL_TC)) == m.MLA_ERR_KERNEL

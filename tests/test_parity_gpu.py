@@ -125,6 +125,13 @@ def test_request_major_with_q3(lib, orc, kernel):
     check_full(orc, inp, kernel, 16, "rm q3")
 
 
+@pytest.mark.parametrize("w_fmt", [0, 1])
+def test_17_to_32_partials_on_tensor_cores(lib, orc, w_fmt):
+    # one token per warp (16-token tiles); 20 partials, 25% dead
+    inp = custom(S=40, H=3, P=20, q=1, spr=20, w_fmt=w_fmt, neg_inf_frac=0.25, seed=12 + w_fmt)
+    check_full(orc, inp, TC, 0, f"P=20 w_fmt={w_fmt}")
+
+
 def test_more_than_32_partials_on_cuda_cores(lib, orc):
     inp = custom(S=8, H=2, P=40, q=1, spr=40, w_fmt=0, neg_inf_frac=0.3, seed=6)
     check_full(orc, inp, SIMT, 0, "P=40")
