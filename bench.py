@@ -34,6 +34,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "combine+W_UV tokens/s and achieved HBM GB/s (% of GB300 roofline)"
 DEFAULT_WORKLOAD = "mtp_mxfp4"
+L2_DEFEAT_BYTES = 256 << 20  # working set per rotation, about twice the 129 MB L2
 
 
 def load_peaks():
@@ -234,41 +235,75 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     m.load_library()
 
-    inp = synth.make(args.workload, device=dev, seed=synth.WORKLOADS[args.workload].seed + rank)
+    seed0 = synth.WORKLOADS[args.workload].seed + rank
+    inp = synth.make(args.workload, device=dev, seed=seed0)
     S, H, S_out = inp["S"], inp["H"], inp["S_out"]
-    out = torch.empty(S_out, H * 128, dtype=torch.bfloat16, device=dev)
+    nbytes = synth.algorithmic_bytes(inp)
+    # Workloads smaller than L2 cycle through independent copies of every
+    # input (W_V too: another layer's weights) so each step reads HBM.
+    rotate = args.rotate
+    if rotate == 0:
+        rotate = 1 if nbytes >= L2_DEFEAT_BYTES else -(-L2_DEFEAT_BYTES // nbytes)
+    copies = [inp] + [synth.make(args.workload, device=dev, seed=seed0 + 1000 * k) for k in range(1, rotate)]
+    outs = [torch.empty(S_out, H * 128, dtype=torch.bfloat16, device=dev) for _ in range(rotate)]
+    out = outs[0]
     stream = torch.cuda.current_stream(dev)
-    call = lambda: m.mla_combine_uv(inp["o"], inp["lse"], inp["q"], inp["spr"], inp["w_v"],
-                                    inp["w_fmt"], inp["gate"], out, w_scale=inp["w_scale"],
-                                    stream=stream, kernel=args.kernel, tile_tokens=args.tile)
+
+    def call(k=0):  # on the current stream (the capture stream inside a graph capture)
+        c = copies[k % rotate]
+        m.mla_combine_uv(c["o"], c["lse"], c["q"], c["spr"], c["w_v"], c["w_fmt"], c["gate"],
+                         outs[k % rotate], w_scale=c["w_scale"], kernel=args.kernel,
+                         tile_tokens=args.tile)
+
     a = m.make_args(inp["o"], inp["lse"], inp["q"], inp["spr"], inp["w_v"], inp["w_fmt"],
                     inp["gate"], out, inp["w_scale"], kernel=args.kernel, tile_tokens=args.tile)
     plan = m.mla_combine_uv_plan(a)
     kname = "tc" if plan["kernel"] == m.MLA_KERNEL_TC else "simt"
-    nbytes = synth.algorithmic_bytes(inp)
+    use_graph = args.graph or (args.graph is None and nbytes < L2_DEFEAT_BYTES)
 
-    for _ in range(max(3, args.warmup)):
-        call()
+    for k in range(max(3, args.warmup)):
+        call(k)
     torch.cuda.synchronize()
     assert m.mla_combine_uv_status(stream) == m.MLA_OK
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        t_wall0 = time.perf_counter()
-        for i in range(args.steps):
-            starts[i].record(stream)
-            call()
-            ends[i].record(stream)
+    if use_graph:
+        # the K launches back to back in one CUDA graph (no host launch gaps);
+        # per-launch time = the replay's time / K
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        with torch.cuda.graph(graph, stream=cap):
+            for k in range(args.steps):
+                call(k)
+        graph.replay()
         torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall0
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(local) as clk:
+            t_wall0 = time.perf_counter()
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            t_wall = time.perf_counter() - t_wall0
+        total_ms = e0.elapsed_time(e1)
+        kern_ms = [total_ms / args.steps]
+    else:
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        with ClockSampler(local) as clk:
+            t_wall0 = time.perf_counter()
+            for i in range(args.steps):
+                starts[i].record(stream)
+                call(i)
+                ends[i].record(stream)
+            torch.cuda.synchronize()
+            t_wall = time.perf_counter() - t_wall0
+        kern_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        total_ms = starts[0].elapsed_time(ends[-1])
     if dist:
         dist.barrier()
-    kern_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = starts[0].elapsed_time(ends[-1])
     clocks = clk.summary()
     assert m.mla_combine_uv_status(stream) == m.MLA_OK
 
@@ -330,12 +365,19 @@ def run_gpu(args):
             "data": "synthetic",
             "config": {"workload": f"{args.workload}: {wl.S // wl.q} requests x q={wl.q} "
                                    f"(S={S}), H={H}, {inp['spr']} splits per request, "
-                                   f"P={inp['P']} compact, "
-                                   f"{'MXFP4' if inp['w_fmt'] else 'bf16'} W_V",
+                                   f"P={inp['P']} "
+                                   + ("passthrough" if inp["P"] == 1 else
+                                      "compact" if inp["P"] == inp["spr"] else "request-major")
+                                   + f", {'MXFP4' if inp['w_fmt'] else 'bf16'} W_V",
                        "S": S, "H": H, "P": inp["P"], "w_fmt": ["bf16", "mxfp4"][inp["w_fmt"]],
                        "parallelism": f"replicas x{ws}", "kernel": kname,
                        "tile_tokens": plan["tile_tokens"], "grid": plan["grid"],
-                       "l2": "inputs 1.8 GB per step, larger than L2: no flush"},
+                       "l2": (f"inputs {nbytes / 1e9:.2f} GB per step, larger than L2: no flush"
+                              if rotate == 1 else
+                              f"{rotate} independent input copies ({rotate * nbytes / 1e6:.0f} MB) "
+                              "cycled, one per step: every step reads HBM"),
+                       "timing": ("CUDA graph of the timed steps, per-step time = replay / steps"
+                                  if use_graph else "CUDA events around each launch")},
             "achieved_gbs": achieved,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,
@@ -369,6 +411,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA cores, 2 tensor cores")
     ap.add_argument("--tile", type=int, default=0, help="tensor-core token tile (16/32; 0 auto)")
+    ap.add_argument("--rotate", type=int, default=0,
+                    help="independent input copies cycled per step (0: enough to exceed L2)")
+    ap.add_argument("--graph", action=argparse.BooleanOptionalAction, default=None,
+                    help="capture the timed steps in a CUDA graph (default: for workloads under L2 size)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

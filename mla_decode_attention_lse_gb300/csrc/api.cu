@@ -77,7 +77,9 @@ int32_t plan_impl(const mla_combine_uv_args *a, int32_t num_sms, mla_plan *pl, K
   if (kernel != MLA_KERNEL_AUTO && kernel != MLA_KERNEL_SIMT && kernel != MLA_KERNEL_TC) return MLA_ERR_KERNEL;
   if (a->tile_tokens != 0 && a->tile_tokens != 16 && a->tile_tokens != 32) return MLA_ERR_KERNEL;
   if (kernel == MLA_KERNEL_TC && n_part > mla::kTcMaxPart) return MLA_ERR_KERNEL;
-  if (kernel == MLA_KERNEL_AUTO) kernel = (n_part <= mla::kTcMaxPart && S >= 16) ? MLA_KERNEL_TC : MLA_KERNEL_SIMT;
+  // tensor cores whenever they can run it (even a single token: a 16-token
+  // tile with empty rows is still faster than the CUDA-core kernel)
+  if (kernel == MLA_KERNEL_AUTO) kernel = (n_part <= mla::kTcMaxPart) ? MLA_KERNEL_TC : MLA_KERNEL_SIMT;
   if (S == 0) kernel = MLA_KERNEL_SIMT;  // nothing to merge: zero rows only
   if (kernel == MLA_KERNEL_SIMT && mla::simt_smem_bytes(n_part) > 200 * 1024) return MLA_ERR_KERNEL;
 

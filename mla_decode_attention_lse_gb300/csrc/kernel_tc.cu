@@ -328,6 +328,26 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
     }
   };
 
+  // The first JB partials of a unit, for every valid token, without weights.
+  auto issue_blind = [&](const Cur &c, Buf &buf) {
+#pragma unroll
+    for (int tk = 0; tk < TPW; ++tk) {
+      const int t = c.tile * BN + warp * TPW + tk;
+      const int r0 = (layout == kRequestMajor) ? (t / p.q) * p.spr : 0;
+      const uint16_t *base = p.o + (long long)t * p.o_st + (long long)c.h * p.o_sh + (long long)r0 * p.o_sp;
+#pragma unroll
+      for (int jj = 0; jj < JB; ++jj) {
+        if (jj < n && t < p.S) {
+          const uint4 *row = reinterpret_cast<const uint4 *>(base + (long long)jj * p.o_sp);
+          buf[jj][tk][0] = __ldcs(row + lane);
+          buf[jj][tk][1] = __ldcs(row + lane + 32);
+        } else {
+          buf[jj][tk][0] = buf[jj][tk][1] = make_uint4(0, 0, 0, 0);
+        }
+      }
+    }
+  };
+
   uint64_t acc[TPW][8];  // fp32 pairs: elements (2q, 2q+1) of chunk q/4
   auto clear_acc = [&]() {
 #pragma unroll
@@ -362,11 +382,12 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
   // g, line r: the scales of K blocks 4g..4g+3 of rows r, r+32, r+64, r+96).
   auto load_wv = [&](int h) {
     if (WFMT == 0) {
+      // bf16 (128 KiB): through registers, 16 chunks per thread and pass
+      // (measured faster here than asynchronous copies)
       const uint16_t *wb = static_cast<const uint16_t *>(p.w_v) + (long long)h * p.w_sh;
-      constexpr int kChunks = kV * 64;  // 16-byte chunks of the bf16 tile
-      constexpr int kPer = 16;          // per pass and thread
+      constexpr int kPer = 16;
 #pragma unroll 1
-      for (int s0 = 0; s0 < kChunks; s0 += kPer * NT) {
+      for (int s0 = 0; s0 < kV * 64; s0 += kPer * NT) {
         uint4 x[kPer];
 #pragma unroll
         for (int i = 0; i < kPer; ++i) {
@@ -380,30 +401,31 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
         }
       }
     } else {
+      // MXFP4 (34 KiB): asynchronous copies (cp.async), no registers held,
+      // overlapped with the loads that follow; each thread waits for its own
+      // copies before it next arrives on a latent buffer
       const uint8_t *wb = static_cast<const uint8_t *>(p.w_v) + (long long)h * p.w_sh;
-      constexpr int kPer = kV * 16 / NT;  // 16-byte code chunks per thread
-      uint4 x[kPer];
-#pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        const int s = threadIdx.x + i * NT;
-        x[i] = __ldg(reinterpret_cast<const uint4 *>(wb + (long long)(s >> 4) * p.w_sv) + (s & 15));
-      }
-#pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        const int s = threadIdx.x + i * NT;
+      for (int s = threadIdx.x; s < kV * 16; s += NT) {
         const int v = s >> 4, c = s & 15;  // row, 16-byte chunk (32 codes)
-        *reinterpret_cast<uint4 *>(gA + (c >> 3) * (kV * 128) + v * 128 + (((c & 7) ^ (v & 7)) << 4)) = x[i];
+        cp_async_16(smem_u32(gA + (c >> 3) * (kV * 128) + v * 128 + (((c & 7) ^ (v & 7)) << 4)),
+                    reinterpret_cast<const uint4 *>(wb + (long long)v * p.w_sv) + c);
       }
-      // scales: (row v, group g) tasks
-#pragma unroll
+      // scales: (row v, group g) -> the 4 scales of K blocks 4g..4g+3
+      const uint8_t *sb = p.w_scale + (long long)h * p.s_sh;
+      const bool al4 = ((reinterpret_cast<uintptr_t>(sb) | (uintptr_t)p.s_sv) & 3u) == 0;
       for (int s = threadIdx.x; s < kV * 4; s += NT) {
         const int v = s >> 2, g = s & 3;
-        const uint8_t *sr = p.w_scale + (long long)h * p.s_sh + (long long)v * p.s_sv + 4 * g;
-        const uint32_t word = (uint32_t)__ldg(sr) | ((uint32_t)__ldg(sr + 1) << 8) |
-                              ((uint32_t)__ldg(sr + 2) << 16) | ((uint32_t)__ldg(sr + 3) << 24);
-        *reinterpret_cast<uint32_t *>(gSFA + g * 512 + (v & 31) * 16 + (v >> 5) * 4) = word;
+        const uint8_t *sr = sb + (long long)v * p.s_sv + 4 * g;
+        uint8_t *dst = gSFA + g * 512 + (v & 31) * 16 + (v >> 5) * 4;
+        if (al4) {
+          cp_async_4(smem_u32(dst), sr);
+        } else {
+          *reinterpret_cast<uint32_t *>(dst) = (uint32_t)__ldg(sr) | ((uint32_t)__ldg(sr + 1) << 8) |
+                                               ((uint32_t)__ldg(sr + 2) << 16) | ((uint32_t)__ldg(sr + 3) << 24);
+        }
       }
     }
+    cp_async_commit();
   };
 
   // The unit's MMAs (one thread): D[v, t] = sum_k W_V[h][v][k] * lat[t][k].
@@ -501,6 +523,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
         }
       }
     }
+    cp_async_wait<0>();  // this thread's W_V copies, if any, have landed
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
@@ -545,8 +568,15 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
       if (nu > 1) prefetch_rows(c1, lse1);
     }
     load_wv(c_first.h);
+    // the first batch is issued before its weights are known (all partials
+    // of the range; rows that turn out dead are loaded but never merged), so
+    // its loads overlap the LSE and W_V round trips
+    issue_blind(cu, bufA);
     weights_of(lse0, wcur);
-    issue(cu, 0, bufA, wA, wcur);
+#pragma unroll
+    for (int jj = 0; jj < JB; ++jj)
+#pragma unroll
+      for (int tk = 0; tk < TPW; ++tk) wA[jj][tk] = __shfl_sync(0xffffffffu, wcur, tk * SEG + jj);
     if (nbi == nb) {
       nbi = 0;
       advance(cn);
@@ -612,6 +642,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
     for (long long k = zb + threadIdx.x; k < ze; k += NT) dst[k] = make_uint4(0, 0, 0, 0);
   }
 
+  cp_async_wait<0>();
   __syncthreads();
   if (threadIdx.x == 0) {
     // drain what this CTA started (only pending after an abort): the last

@@ -111,8 +111,9 @@ def test_layouts(lib):
 
 
 def test_kernel_and_tile_choice(lib):
-    # tiny token counts -> CUDA-core kernel
-    assert mla_combine_uv_plan(args(S=4, H=2, P=4, q=2, spr=2), SMS)["kernel"] == m.MLA_KERNEL_SIMT
+    # even tiny token counts run on tensor cores (a 16-token tile, mostly empty)
+    p = mla_combine_uv_plan(args(S=4, H=2, P=4, q=2, spr=2), SMS)
+    assert (p["kernel"], p["tile_tokens"], p["units"]) == (m.MLA_KERNEL_TC, 16, 2)
     # decode sizes -> tensor cores, 16-token tiles when 32 would not fill the GPU
     p = mla_combine_uv_plan(args(S=64, P=16, spr=16), SMS)
     assert (p["kernel"], p["tile_tokens"], p["units"], p["grid"]) == (m.MLA_KERNEL_TC, 16, 48, 48)
