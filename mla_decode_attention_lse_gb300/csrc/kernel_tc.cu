@@ -60,9 +60,13 @@ struct TcLayout {
 };
 // Pipeline stages (latent buffers, TMEM accumulators, latent scale buffers):
 // the epilogue of unit i - (stages - 1) runs after unit i is merged, giving
-// the MMAs of a unit a full unit of slack.  bf16 W_V with 32-token tiles only
-// has shared memory for two.
-__host__ __device__ constexpr int tc_stages(int BN, int WFMT) { return (WFMT == 0 && BN == 32) ? 2 : 3; }
+// the MMAs of a unit a full unit of slack.
+__host__ __device__ constexpr int tc_stages(int, int) { return 3; }
+// bf16 W_V with 32-token tiles has no room for the 8 KiB epilogue staging
+// area: its epilogue stages in the warp's own rows of the latent buffer of
+// the unit being drained (that unit's MMAs are complete, and only this warp
+// rewrites those rows, at its next finish of that stage).
+__host__ __device__ constexpr bool tc_epi_in_latents(int BN, int WFMT) { return WFMT == 0 && BN == 32; }
 __host__ __device__ constexpr TcLayout tc_layout(int BN, int WFMT, int NW) {
   TcLayout L{};
   const uint32_t st = (uint32_t)tc_stages(BN, WFMT);
@@ -72,7 +76,7 @@ __host__ __device__ constexpr TcLayout tc_layout(int BN, int WFMT, int NW) {
   L.sfa_off = L.b_off + st * L.b_bytes;
   L.sfb_off = L.sfa_off + (WFMT ? 2048u : 0u);
   L.epi_off = L.sfb_off + (WFMT ? st * 2048u : 0u);
-  L.bar_off = L.epi_off + (uint32_t)NW * (4u * (uint32_t)BN / (uint32_t)NW) * 64u;  // epilogue staging
+  L.bar_off = L.epi_off + (tc_epi_in_latents(BN, WFMT) ? 0u : (uint32_t)NW * (4u * (uint32_t)BN / (uint32_t)NW) * 64u);
   L.total = L.bar_off + 128u;
   // TMEM: `st` fp32 accumulators of BN columns; MXFP4 adds a 16-column region
   // for W_V's scales and one per stage for the latents' scales
@@ -198,9 +202,16 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
 
   // Epilogue of a unit: TMEM accumulator -> bf16 -> (staged through shared
   // memory, token-major) * gate -> core with 16-byte accesses.
-  uint16_t *stage = gE + warp * (CPW * 32);
   auto epilogue = [&](int j, const Cur &c) -> bool {
     const int bj = j % ST;
+    // staging: CPW tokens x 32 V rows of bf16 (512 bytes), addressed in
+    // 128-byte pieces: the warp's own area, or (see tc_epi_in_latents) the
+    // K blocks 0..3 of the warp's first latent row in stage bj
+    uint8_t *const st_base = tc_epi_in_latents(BN, WFMT)
+                                 ? gB0 + (size_t)bj * L.b_bytes + (size_t)(warp * TPW) * 128u
+                                 : reinterpret_cast<uint8_t *>(gE + warp * (CPW * 32));
+    constexpr uint32_t kPiece = tc_epi_in_latents(BN, WFMT) ? (uint32_t)BN * 128u : 128u;
+    auto stg = [&](uint32_t o) { return st_base + (o >> 7) * kPiece + (o & 127u); };
     // lane -> (token e0 + lane/4, 8 consecutive V rows)
     constexpr int kRounds = (CPW + 7) / 8;
     const int v8 = (lane & 3) * 8;
@@ -233,14 +244,14 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
 #pragma unroll
     for (int x = 0; x < CPW; ++x) {
       const __nv_bfloat16 a = __float2bfloat16_rn(__uint_as_float(r[x]));
-      stage[x * 32 + lane] = *reinterpret_cast<const uint16_t *>(&a);
+      *reinterpret_cast<uint16_t *>(stg((uint32_t)(x * 64 + 2 * lane))) = *reinterpret_cast<const uint16_t *>(&a);
     }
     __syncwarp();
 #pragma unroll
     for (int rd = 0; rd < kRounds; ++rd) {
       if (act[rd]) {
         const int e = rd * 8 + (lane >> 2);
-        const uint4 a = *reinterpret_cast<const uint4 *>(stage + e * 32 + v8);
+        const uint4 a = *reinterpret_cast<const uint4 *>(stg((uint32_t)(e * 64 + 2 * v8)));
         const uint32_t aa[4] = {a.x, a.y, a.z, a.w}, gg[4] = {g[rd].x, g[rd].y, g[rd].z, g[rd].w};
         uint32_t o[4];
 #pragma unroll
