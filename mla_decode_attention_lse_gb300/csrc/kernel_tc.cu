@@ -578,11 +578,13 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
       advance(c1);
       if (nu > 1) prefetch_rows(c1, lse1);
     }
-    load_wv(c_first.h);
     // the first batch is issued before its weights are known (all partials
     // of the range; rows that turn out dead are loaded but never merged), so
-    // its loads overlap the LSE and W_V round trips
+    // its loads overlap the LSE and W_V round trips (bf16 W_V, copied through
+    // registers, goes first: measured faster that way)
+    if (WFMT == 0) load_wv(c_first.h);
     issue_blind(cu, bufA);
+    if (WFMT != 0) load_wv(c_first.h);
     weights_of(lse0, wcur);
 #pragma unroll
     for (int jj = 0; jj < JB; ++jj)
