@@ -100,6 +100,23 @@ __device__ __forceinline__ float sane(float x) {
   return (x != x || x == __int_as_float(0x7F800000)) ? __int_as_float(0xFF800000) : x;
 }
 
+// Packed bf16 product, rounded once to nearest even: the same bits as the
+// fp32 product of the two bf16 values (exact) rounded to bf16.
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// One elected lane of a converged warp: returns true in that lane and sets
+// `leader` to its lane id in every lane.
+__device__ __forceinline__ bool elect_one(uint32_t &leader) {
+  uint32_t e;
+  asm volatile("{\n\t.reg .pred p;\n\telect.sync %0|p, 0xffffffff;\n\tselp.u32 %1, 1, 0, p;\n\t}"
+               : "=r"(leader), "=r"(e));
+  return e != 0;
+}
+
 // Per-half unsigned maximum of two packed 16-bit pairs.
 __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
   uint32_t d;

@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
         uint32_t o[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          o[q] = pack_bf16(bf16_lo(aa[q]) * bf16_lo(gg[q]), bf16_hi(aa[q]) * bf16_hi(gg[q]));
+          o[q] = mul_bf16x2(aa[q], gg[q]);  // bf16(acc) * gate, one rounding
         *reinterpret_cast<uint4 *>(p.out + off[rd]) = make_uint4(o[0], o[1], o[2], o[3]);
       }
     }
@@ -537,11 +537,21 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
     cp_async_wait<0>();  // this thread's W_V copies, if any, have landed
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) {
-      // arrivals on stage b are numbered across its uses: use i / ST takes
-      // numbers (i / ST) * kWorkers .. + kWorkers - 1; the last one issues
-      const uint32_t prev = atom_add_acq_rel_cta(cnt0 + 4 * b, 1u);
-      if (prev == (uint32_t)(i / ST + 1) * kWorkers - 1u) issue_mma(i, i == 0 || c.tile == 0);
+    // arrivals on stage b are numbered across its uses: use i / ST takes
+    // numbers (i / ST) * kWorkers .. + kWorkers - 1; the last one issues
+    const uint32_t last_no = (uint32_t)(i / ST + 1) * kWorkers - 1u;
+    if (WFMT != 0 && TPW == 2) {
+      // MXFP4, two tokens per warp: one elected lane arrives (acquiring the other warps'
+      // latents) and, if last, issues; the warp stays converged around it
+      // (measured faster than a divergent lane 0; with one token per warp it
+      // costs registers)
+      uint32_t leader, prev = 0;
+      const bool me = elect_one(leader);
+      if (me) prev = atom_add_acq_rel_cta(cnt0 + 4 * b, 1u);
+      prev = __shfl_sync(0xffffffffu, prev, (int)leader);
+      if (prev == last_no && me) issue_mma(i, i == 0 || c.tile == 0);
+    } else if (lane == 0) {
+      if (atom_add_acq_rel_cta(cnt0 + 4 * b, 1u) == last_no) issue_mma(i, i == 0 || c.tile == 0);
     }
     __syncwarp();
     // drain the accumulator of unit i - (ST - 1); before the next unit of
