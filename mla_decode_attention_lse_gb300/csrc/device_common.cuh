@@ -165,14 +165,16 @@ __device__ __forceinline__ uint32_t e2m1x8_from_bf16x8(const uint32_t (&u)[4], f
   asm("{\n\t"
       ".reg .b8 c0, c1, c2, c3;\n\t"
       ".reg .f32 l0, h0, l1, h1, l2, h2, l3, h3;\n\t"
+      ".reg .b64 p, s;\n\t"
       "shl.b32 l0, %1, 16;\n\tand.b32 h0, %1, 0xffff0000;\n\t"
       "shl.b32 l1, %2, 16;\n\tand.b32 h1, %2, 0xffff0000;\n\t"
       "shl.b32 l2, %3, 16;\n\tand.b32 h2, %3, 0xffff0000;\n\t"
       "shl.b32 l3, %4, 16;\n\tand.b32 h3, %4, 0xffff0000;\n\t"
-      "mul.rn.f32 l0, l0, %5;\n\tmul.rn.f32 h0, h0, %5;\n\t"
-      "mul.rn.f32 l1, l1, %5;\n\tmul.rn.f32 h1, h1, %5;\n\t"
-      "mul.rn.f32 l2, l2, %5;\n\tmul.rn.f32 h2, h2, %5;\n\t"
-      "mul.rn.f32 l3, l3, %5;\n\tmul.rn.f32 h3, h3, %5;\n\t"
+      "mov.b64 s, {%5, %5};\n\t"
+      "mov.b64 p, {l0, h0};\n\tmul.rn.f32x2 p, p, s;\n\tmov.b64 {l0, h0}, p;\n\t"
+      "mov.b64 p, {l1, h1};\n\tmul.rn.f32x2 p, p, s;\n\tmov.b64 {l1, h1}, p;\n\t"
+      "mov.b64 p, {l2, h2};\n\tmul.rn.f32x2 p, p, s;\n\tmov.b64 {l2, h2}, p;\n\t"
+      "mov.b64 p, {l3, h3};\n\tmul.rn.f32x2 p, p, s;\n\tmov.b64 {l3, h3}, p;\n\t"
       "cvt.rn.satfinite.e2m1x2.f32 c0, h0, l0;\n\t"
       "cvt.rn.satfinite.e2m1x2.f32 c1, h1, l1;\n\t"
       "cvt.rn.satfinite.e2m1x2.f32 c2, h2, l2;\n\t"
@@ -395,6 +397,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   d |= (uint64_t)1 << 46;                           // descriptor version (tcgen05)
   d |= (uint64_t)2 << 61;                           // swizzle mode: 128 B
   return d;
+}
+
+// The same descriptor at `off` bytes past the one whose lower word is `lo`:
+// the start address is the low 14 bits of the lower word (shared memory is
+// below 256 KiB), so a 16-byte-unit offset adds to the lower word alone.
+constexpr uint32_t kDescSw128Hi = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint64_t desc_sw128_at(uint32_t lo, uint32_t off) {
+  return ((uint64_t)kDescSw128Hi << 32) | (uint64_t)(lo + (off >> 4));
 }
 
 // Shared-memory descriptor without swizzle: 16-byte rows, 8-row groups 128

@@ -447,13 +447,14 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
     tc_fence_after();
     const uint32_t d = tmem + (uint32_t)(b * BN);
     const uint32_t sB = sB0 + (uint32_t)b * L.b_bytes;
+    const uint32_t dA = (uint32_t)smem_desc_sw128(sA), dB = (uint32_t)smem_desc_sw128(sB);
     if (WFMT == 0) {
       constexpr uint32_t kIdesc = idesc_bf16(128, BN);
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
         const uint32_t kb = k >> 2, kk = k & 3;
-        tc_mma_f16(d, smem_desc_sw128(sA + kb * 16384u + kk * 32u),
-                   smem_desc_sw128(sB + kb * (uint32_t)(BN * 128) + kk * 32u), kIdesc, k > 0 ? 1u : 0u);
+        tc_mma_f16(d, desc_sw128_at(dA, kb * 16384u + kk * 32u), desc_sw128_at(dB, kb * (uint32_t)(BN * 128) + kk * 32u),
+                   kIdesc, k > 0 ? 1u : 0u);
       }
     } else {
       constexpr uint32_t kIdesc = idesc_mxf4(128, BN);
@@ -468,8 +469,8 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
 #pragma unroll
       for (int k = 0; k < 8; ++k) {  // K = 64 per step: two 32-blocks, scale word k/2, bytes 2(k%2)..
         const uint32_t kb = k >> 2, kk = k & 3;
-        tc_mma_mxf4(d, smem_desc_sw128(sA + kb * (uint32_t)(kV * 128) + kk * 32u),
-                    smem_desc_sw128(sB + kb * (uint32_t)(BN * 128) + kk * 32u),
+        tc_mma_mxf4(d, desc_sw128_at(dA, kb * (uint32_t)(kV * 128) + kk * 32u),
+                    desc_sw128_at(dB, kb * (uint32_t)(BN * 128) + kk * 32u),
                     kIdesc | idesc_sf_ids(2u * (k & 1)), sfa + 4u * (k >> 1), sfb + 4u * (k >> 1), k > 0 ? 1u : 0u);
       }
     }
