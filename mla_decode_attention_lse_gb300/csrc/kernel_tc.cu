@@ -116,10 +116,15 @@ __device__ __forceinline__ uint32_t mx_codes(uint4 x, uint32_t &sc) {
   uint32_t am = max(am2 & 0xFFFFu, am2 >> 16);
   am = max(am, __shfl_xor_sync(0xffffffffu, am, 1));
   am = max(am, __shfl_xor_sync(0xffffffffu, am, 2));
-  sc = mx_scale_code(am);
-  if (sc == 255u) return 0u;  // Inf / NaN in the block: the NaN scale carries it
-  const float inv = e8m0_inverse(sc);
-  return e2m1x8_from_bf16x8(u, inv);
+  // exponent field ef of the block maximum: scale code max(ef, 3) - 2 (zero
+  // and tiny blocks clamp to 1; a finite block never exceeds 252), its
+  // inverse 2^(127 - code) has exponent field 256 - max(ef, 3); ef = 255
+  // (Inf / NaN in the block) gives the NaN code, which carries it, and zero
+  // codes
+  const uint32_t ef = am >> 7, e3 = max(ef, 3u);
+  sc = (ef == 255u) ? 255u : e3 - 2u;
+  const uint32_t w = e2m1x8_from_bf16x8(u, __uint_as_float((256u - e3) << 23));
+  return (ef == 255u) ? 0u : w;
 }
 
 }  // namespace
