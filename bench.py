@@ -286,7 +286,7 @@ def run_gpu(args):
     a = m.make_args(inp["o"], inp["lse"], inp["q"], inp["spr"], inp["w_v"], inp["w_fmt"],
                     inp["gate"], out, inp["w_scale"], kernel=args.kernel, tile_tokens=args.tile)
     plan = m.mla_combine_uv_plan(a)
-    kname = "tc" if plan["kernel"] == m.MLA_KERNEL_TC else "simt"
+    kname = {m.MLA_KERNEL_TC: "tc", m.MLA_KERNEL_KSPLIT: "tc_ksplit_cluster4"}.get(plan["kernel"], "simt")
     use_graph = args.graph or (args.graph is None and nbytes < L2_DEFEAT_BYTES)
 
     for k in range(max(3, args.warmup)):
@@ -433,7 +433,8 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=120.0,
                     help="seconds of oracle work for the whole --impl reference run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA cores, 2 tensor cores")
+    ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA cores, 2 tensor cores (persistent), "
+                    "3 tensor cores with the latents split over a 4-CTA cluster")
     ap.add_argument("--tile", type=int, default=0, help="tensor-core token tile (16/32; 0 auto)")
     ap.add_argument("--rotate", type=int, default=0,
                     help="independent input copies cycled per step (0: enough to exceed L2)")

@@ -80,7 +80,11 @@ enum {
 enum {
   MLA_KERNEL_AUTO = 0, /* pick by size (the plan says which)                  */
   MLA_KERNEL_SIMT = 1, /* CUDA-core kernel: any P; the small-batch path       */
-  MLA_KERNEL_TC = 2    /* fused tcgen05 kernel: partials per token <= 32       */
+  MLA_KERNEL_TC = 2,   /* fused tcgen05 kernel: partials per token <= 32       */
+  MLA_KERNEL_KSPLIT = 3 /* decode sizes: a (head, 16-token) unit per 4-CTA
+                          cluster, the 512 latents split over the cluster and
+                          the partial GEMMs summed through distributed shared
+                          memory; partials per token <= 16, S >= 1           */
 };
 
 typedef struct {
@@ -118,12 +122,12 @@ typedef struct {
 
 /* What a call would launch (host-side planning only). */
 typedef struct {
-  int32_t kernel;        /* MLA_KERNEL_SIMT or MLA_KERNEL_TC                  */
+  int32_t kernel;        /* MLA_KERNEL_SIMT, _TC or _KSPLIT                   */
   int32_t layout;        /* 0 passthrough, 1 compact, 2 request-major         */
   int32_t n_part;        /* partials each token merges                        */
   int32_t tile_tokens;   /* tokens per work unit                              */
   int32_t units;         /* (head, token tile) work units                     */
-  int32_t grid;          /* CTAs launched                                     */
+  int32_t grid;          /* CTAs launched (KSPLIT: 4 per unit, as clusters)   */
   int32_t threads;       /* threads per CTA                                   */
   int32_t smem_bytes;    /* dynamic shared memory per CTA                     */
 } mla_plan;

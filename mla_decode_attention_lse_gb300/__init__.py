@@ -23,6 +23,7 @@ MLA_W_MXFP4 = 1
 MLA_KERNEL_AUTO = 0
 MLA_KERNEL_SIMT = 1
 MLA_KERNEL_TC = 2
+MLA_KERNEL_KSPLIT = 3
 
 MLA_OK = 0
 MLA_ERR_NULL = 1

@@ -74,12 +74,24 @@ int32_t plan_impl(const mla_combine_uv_args *a, int32_t num_sms, mla_plan *pl, K
 
   // kernel choice
   int kernel = a->kernel;
-  if (kernel != MLA_KERNEL_AUTO && kernel != MLA_KERNEL_SIMT && kernel != MLA_KERNEL_TC) return MLA_ERR_KERNEL;
+  if (kernel != MLA_KERNEL_AUTO && kernel != MLA_KERNEL_SIMT && kernel != MLA_KERNEL_TC &&
+      kernel != MLA_KERNEL_KSPLIT)
+    return MLA_ERR_KERNEL;
   if (a->tile_tokens != 0 && a->tile_tokens != 16 && a->tile_tokens != 32) return MLA_ERR_KERNEL;
   if (kernel == MLA_KERNEL_TC && n_part > mla::kTcMaxPart) return MLA_ERR_KERNEL;
+  if (kernel == MLA_KERNEL_KSPLIT && (n_part > mla::kKsMaxPart || S == 0 ||
+                                      (a->tile_tokens != 0 && a->tile_tokens != 16)))
+    return MLA_ERR_KERNEL;
+  const int64_t units16 = (int64_t)a->H * ((S + 15) / 16);
   // tensor cores whenever they can run it (even a single token: a 16-token
-  // tile with empty rows is still faster than the CUDA-core kernel)
-  if (kernel == MLA_KERNEL_AUTO) kernel = (n_part <= mla::kTcMaxPart) ? MLA_KERNEL_TC : MLA_KERNEL_SIMT;
+  // tile with empty rows is still faster than the CUDA-core kernel); the
+  // cluster kernel when 16-token units leave SMs idle
+  if (kernel == MLA_KERNEL_AUTO) {
+    if (n_part <= mla::kKsMaxPart && S > 0 && num_sms > 0 && units16 < num_sms)
+      kernel = MLA_KERNEL_KSPLIT;
+    else
+      kernel = (n_part <= mla::kTcMaxPart) ? MLA_KERNEL_TC : MLA_KERNEL_SIMT;
+  }
   if (S == 0) kernel = MLA_KERNEL_SIMT;  // nothing to merge: zero rows only
   if (kernel == MLA_KERNEL_SIMT && mla::simt_smem_bytes(n_part) > 200 * 1024) return MLA_ERR_KERNEL;
 
@@ -93,6 +105,13 @@ int32_t plan_impl(const mla_combine_uv_args *a, int32_t num_sms, mla_plan *pl, K
     pl->grid = pl->units;
     pl->threads = 256;
     pl->smem_bytes = (int32_t)mla::simt_smem_bytes(n_part);
+  } else if (kernel == MLA_KERNEL_KSPLIT) {
+    if ((int64_t)units16 * mla::ks_ctas_per_unit() >= ((int64_t)1 << 31)) return MLA_ERR_SHAPE;
+    pl->tile_tokens = 16;
+    pl->units = (int32_t)units16;
+    pl->grid = pl->units * mla::ks_ctas_per_unit();
+    pl->threads = mla::ks_threads();
+    pl->smem_bytes = (int32_t)mla::ks_smem_bytes(a->w_fmt);
   } else {
     if (num_sms <= 0) return MLA_ERR_SHAPE;
     int tile = a->tile_tokens;
@@ -210,6 +229,8 @@ int32_t mla_combine_uv(const mla_combine_uv_args *args, void *stream) {
   cudaError_t e;
   if (pl.kernel == MLA_KERNEL_SIMT) {
     e = mla::launch_simt(kp, s);
+  } else if (pl.kernel == MLA_KERNEL_KSPLIT) {
+    e = mla::launch_ks(kp, s);
   } else {
     e = mla::launch_tc(kp, pl.grid, s);
   }

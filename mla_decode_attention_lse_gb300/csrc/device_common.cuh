@@ -186,6 +186,29 @@ __device__ __forceinline__ uint32_t e2m1x8_from_bf16x8(const uint32_t (&u)[4], f
   return r;
 }
 
+// MXFP4 quantisation of a lane's 8 bf16 latents (one 16-byte chunk; the
+// block of 32 spans lanes 4g..4g+3).  Scale code from the largest
+// sign-cleared bf16 pattern; elements scaled by an exact power of two and
+// converted to E2M1 by the hardware (nearest even, saturating at 6).  Returns
+// the 8 codes packed (element 2i in the low nibble of byte i) and the scale.
+__device__ __forceinline__ uint32_t mx_codes(uint4 x, uint32_t &sc) {
+  const uint32_t u[4] = {x.x, x.y, x.z, x.w};
+  const uint32_t am2 = max_u16x2(max_u16x2(u[0] & 0x7FFF7FFFu, u[1] & 0x7FFF7FFFu),
+                                 max_u16x2(u[2] & 0x7FFF7FFFu, u[3] & 0x7FFF7FFFu));
+  uint32_t am = max(am2 & 0xFFFFu, am2 >> 16);
+  am = max(am, __shfl_xor_sync(0xffffffffu, am, 1));
+  am = max(am, __shfl_xor_sync(0xffffffffu, am, 2));
+  // exponent field ef of the block maximum: scale code max(ef, 3) - 2 (zero
+  // and tiny blocks clamp to 1; a finite block never exceeds 252), its
+  // inverse 2^(127 - code) has exponent field 256 - max(ef, 3); ef = 255
+  // (Inf / NaN in the block) gives the NaN code, which carries it, and zero
+  // codes
+  const uint32_t ef = am >> 7, e3 = max(ef, 3u);
+  sc = (ef == 255u) ? 255u : e3 - 2u;
+  const uint32_t w = e2m1x8_from_bf16x8(u, __uint_as_float((256u - e3) << 23));
+  return (ef == 255u) ? 0u : w;
+}
+
 // An E2M1 pair (low nibble -> lo) -> two fp16 values packed as (lo, hi).
 __device__ __forceinline__ uint32_t f16x2_from_e2m1x2(uint32_t byte) {
   uint32_t r;
@@ -295,6 +318,47 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int 
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
+}
+
+// ---- programmatic dependent launch ---------------------------------------
+
+// Block until every grid this one depends on (the previous kernel on the
+// stream, when launched with programmatic stream serialization) has completed
+// and its memory is visible; returns at once otherwise.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allow the next dependent launch to begin (its own wait still orders it
+// after this grid's completion).
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+// ---- thread-block clusters and distributed shared memory ----------------
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+// All threads of every CTA of the cluster; release / acquire ordering of
+// shared-memory (and mbarrier) state across the cluster.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The shared::cluster address of `addr` (a shared::cta address) in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// 16-byte asynchronous store into another CTA's shared memory, counted as
+// transaction bytes on that CTA's mbarrier `rbar` (both shared::cluster).
+__device__ __forceinline__ void st_async_v4(uint32_t raddr, float a, float b, float c, float d, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(raddr),
+               "f"(a), "f"(b), "f"(c), "f"(d), "r"(rbar)
+               : "memory");
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {

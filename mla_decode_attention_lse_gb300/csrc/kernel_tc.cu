@@ -104,29 +104,6 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int
   }
 }
 
-// MXFP4 quantisation of a lane's 8 bf16 latents (one 16-byte chunk; the
-// block of 32 spans lanes 4g..4g+3).  Scale code from the largest
-// sign-cleared bf16 pattern; elements scaled by an exact power of two and
-// converted to E2M1 by the hardware (nearest even, saturating at 6).  Returns
-// the 8 codes packed (element 2i in the low nibble of byte i) and the scale.
-__device__ __forceinline__ uint32_t mx_codes(uint4 x, uint32_t &sc) {
-  const uint32_t u[4] = {x.x, x.y, x.z, x.w};
-  const uint32_t am2 = max_u16x2(max_u16x2(u[0] & 0x7FFF7FFFu, u[1] & 0x7FFF7FFFu),
-                                 max_u16x2(u[2] & 0x7FFF7FFFu, u[3] & 0x7FFF7FFFu));
-  uint32_t am = max(am2 & 0xFFFFu, am2 >> 16);
-  am = max(am, __shfl_xor_sync(0xffffffffu, am, 1));
-  am = max(am, __shfl_xor_sync(0xffffffffu, am, 2));
-  // exponent field ef of the block maximum: scale code max(ef, 3) - 2 (zero
-  // and tiny blocks clamp to 1; a finite block never exceeds 252), its
-  // inverse 2^(127 - code) has exponent field 256 - max(ef, 3); ef = 255
-  // (Inf / NaN in the block) gives the NaN code, which carries it, and zero
-  // codes
-  const uint32_t ef = am >> 7, e3 = max(ef, 3u);
-  sc = (ef == 255u) ? 255u : e3 - 2u;
-  const uint32_t w = e2m1x8_from_bf16x8(u, __uint_as_float((256u - e3) << 23));
-  return (ef == 255u) ? 0u : w;
-}
-
 }  // namespace
 
 template <int BN, int WFMT, int NW>

@@ -19,4 +19,12 @@ int tc_max_part(int tile, int w_fmt);                 // partials per token the 
 size_t tc_smem_bytes(int tile, int w_fmt, int n_part);
 cudaError_t launch_tc(const KParams &p, int grid, cudaStream_t stream);
 
+// Decode-size kernel: a (head, 16-token) unit per 4-CTA cluster, the latent
+// dimension split over the cluster; n_part <= 16.
+constexpr int kKsMaxPart = 16;
+int ks_ctas_per_unit();
+int ks_threads();
+size_t ks_smem_bytes(int w_fmt);
+cudaError_t launch_ks(const KParams &p, cudaStream_t stream);
+
 }  // namespace mla

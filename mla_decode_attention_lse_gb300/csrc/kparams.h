@@ -9,7 +9,8 @@ enum Layout : int { kPassthrough = 0, kCompact = 1, kRequestMajor = 2 };
 
 // Error codes a kernel writes into the device error word (first one wins).
 enum KernelError : int { kErrNone = 0, kErrWaitLatent = 1, kErrWaitMma = 2, kErrWaitAccEmpty = 3,
-                         kErrWaitWv = 4, kErrWaitTeardown = 5 };
+                         kErrWaitWv = 4, kErrWaitTeardown = 5,
+                         kErrWaitPeer = 6 };
 
 struct KParams {
   int S, S_out, H;

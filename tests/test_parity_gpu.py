@@ -14,7 +14,7 @@ from parity_util import (CANARY, bits_to_f32, compare, dead_rows, host_inputs, o
 
 pytestmark = pytest.mark.gpu
 
-SIMT, TC = 1, 2
+SIMT, TC, KS = 1, 2, 3
 
 
 @pytest.fixture(scope="module")
@@ -49,6 +49,8 @@ CASES = [
     ("splitkv_rm", 0, 0), ("splitkv_rm", SIMT, 0),
     ("stacked_mxfp4", 0, 0), ("stacked_mxfp4", SIMT, 0), ("stacked_mxfp4", TC, 16),
     ("stacked_mxfp4", TC, 32),
+    ("tiny_split", KS, 0), ("nosplit", KS, 0), ("splitkv", KS, 0), ("splitkv_rm", KS, 0),
+    ("stacked_mxfp4", KS, 0),
 ]
 
 
@@ -104,7 +106,7 @@ def custom(**kw):
     return synth().custom(device="cuda", **kw)
 
 
-@pytest.mark.parametrize("kernel", [SIMT, TC])
+@pytest.mark.parametrize("kernel", [SIMT, TC, KS])
 @pytest.mark.parametrize("S,S_out", [(1, 1), (17, 20), (33, 33), (47, 64)])
 def test_ragged_token_counts(lib, orc, kernel, S, S_out):
     inp = custom(S=S, S_out=S_out, H=3, P=3, q=1, spr=3, w_fmt=0, neg_inf_frac=0.2, seed=S)
@@ -118,7 +120,7 @@ def test_empty_batch_zeroes_padding(lib, orc, kernel):
     assert np.all(gpu == 0) and np.all(canary == CANARY)
 
 
-@pytest.mark.parametrize("kernel", [SIMT, TC])
+@pytest.mark.parametrize("kernel", [SIMT, TC, KS])
 def test_request_major_with_q3(lib, orc, kernel):
     # 6 requests x q=3, 5 splits each -> P = 30, request-major
     inp = custom(S=18, H=2, P=30, q=3, spr=5, w_fmt=1, neg_inf_frac=0.15, nan_frac=0.05, seed=5)
@@ -142,7 +144,7 @@ def test_more_than_32_partials_on_cuda_cores(lib, orc):
     assert e.value.status == m.MLA_ERR_KERNEL
 
 
-@pytest.mark.parametrize("kernel", [SIMT, TC])
+@pytest.mark.parametrize("kernel", [SIMT, TC, KS])
 @pytest.mark.parametrize("w_fmt", [0, 1])
 def test_all_dead_rows_and_planted_nan(lib, orc, kernel, w_fmt):
     inp = custom(S=32, H=4, P=4, q=1, spr=4, w_fmt=w_fmt, dead_rows=10, neg_inf_frac=0.3, seed=7)
@@ -153,7 +155,7 @@ def test_all_dead_rows_and_planted_nan(lib, orc, kernel, w_fmt):
     check_full(orc, inp, kernel, 16, "planted NaN")
 
 
-@pytest.mark.parametrize("kernel", [SIMT, TC])
+@pytest.mark.parametrize("kernel", [SIMT, TC, KS])
 def test_strided_views(lib, orc, kernel):
     s = synth()
     base = s.custom(S=40, H=6, P=3, q=1, spr=3, w_fmt=0, seed=8, device="cuda")
@@ -169,7 +171,7 @@ def test_strided_views(lib, orc, kernel):
     check_full(orc, inp, kernel, 16, "strided")
 
 
-@pytest.mark.parametrize("kernel", [SIMT, TC])
+@pytest.mark.parametrize("kernel", [SIMT, TC, KS])
 def test_passthrough_mxfp4_with_inf_latent(lib, orc, kernel):
     # P == 1: the o row is the latent; an Inf in it makes its block's scale NaN
     inp = custom(S=16, H=2, P=1, q=1, spr=0, w_fmt=1, lse_unused=True, seed=9)
@@ -190,3 +192,17 @@ def test_two_calls_two_streams(lib, orc):
     a, _ = run_gpu(inp, stream=s1)
     b, _ = run_gpu(inp, stream=s2)
     assert np.array_equal(a, b)  # deterministic
+
+
+def test_cluster_kernel_two_streams_and_auto_choice(lib, orc):
+    import mla_decode_attention_lse_gb300 as m
+
+    inp = synth().make("splitkv", device="cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    a, _ = run_gpu(inp, stream=s1, kernel=KS)
+    b, _ = run_gpu(inp, stream=s2)  # automatic choice at this size
+    assert np.array_equal(a, b)  # same kernel, deterministic (rank-ordered sums)
+    args = m.make_args(inp["o"], inp["lse"], inp["q"], inp["spr"], inp["w_v"], inp["w_fmt"], inp["gate"],
+                       torch.empty(inp["S_out"], inp["H"] * 128, dtype=torch.bfloat16, device="cuda"),
+                       inp.get("w_scale"))
+    assert m.mla_combine_uv_plan(args)["kernel"] == m.MLA_KERNEL_KSPLIT
