@@ -81,10 +81,11 @@ enum {
   MLA_KERNEL_AUTO = 0, /* pick by size (the plan says which)                  */
   MLA_KERNEL_SIMT = 1, /* CUDA-core kernel: any P; the small-batch path       */
   MLA_KERNEL_TC = 2,   /* fused tcgen05 kernel: partials per token <= 32       */
-  MLA_KERNEL_KSPLIT = 3 /* decode sizes: a (head, 16-token) unit per 4-CTA
-                          cluster, the 512 latents split over the cluster and
-                          the partial GEMMs summed through distributed shared
-                          memory; partials per token <= 16, S >= 1           */
+  MLA_KERNEL_KSPLIT = 3 /* a (head, 16-token) unit per 4-CTA cluster, the
+                          512 latents split over the cluster and the partial
+                          GEMMs summed through distributed shared memory;
+                          partials per token <= 16, S >= 1; on request only
+                          (automatic choice never picks it)                   */
 };
 
 typedef struct {

@@ -83,15 +83,12 @@ int32_t plan_impl(const mla_combine_uv_args *a, int32_t num_sms, mla_plan *pl, K
                                       (a->tile_tokens != 0 && a->tile_tokens != 16)))
     return MLA_ERR_KERNEL;
   const int64_t units16 = (int64_t)a->H * ((S + 15) / 16);
-  // tensor cores whenever they can run it (even a single token: a 16-token
-  // tile with empty rows is still faster than the CUDA-core kernel); the
-  // cluster kernel when 16-token units leave SMs idle
-  if (kernel == MLA_KERNEL_AUTO) {
-    if (n_part <= mla::kKsMaxPart && S > 0 && num_sms > 0 && units16 < num_sms)
-      kernel = MLA_KERNEL_KSPLIT;
-    else
-      kernel = (n_part <= mla::kTcMaxPart) ? MLA_KERNEL_TC : MLA_KERNEL_SIMT;
-  }
+  // the persistent tensor-core kernel whenever it can run it: even a single
+  // token (a 16-token tile with empty rows) is faster than the CUDA-core
+  // kernel, and with its prologue overlapping the previous launch it also
+  // beats the cluster kernel at every decode size measured; the cluster
+  // kernel runs on request only
+  if (kernel == MLA_KERNEL_AUTO) kernel = (n_part <= mla::kTcMaxPart) ? MLA_KERNEL_TC : MLA_KERNEL_SIMT;
   if (S == 0) kernel = MLA_KERNEL_SIMT;  // nothing to merge: zero rows only
   if (kernel == MLA_KERNEL_SIMT && mla::simt_smem_bytes(n_part) > 200 * 1024) return MLA_ERR_KERNEL;
 

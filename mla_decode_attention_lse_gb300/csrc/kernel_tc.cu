@@ -154,6 +154,10 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
+  // the next launch on the stream may begin its prologue as this grid's CTAs
+  // finish (its dependent work waits for this grid's completion)
+  grid_launch_dependents();
+  constexpr bool kPdlWvFirst = true;
 
   const int tph = p.tiles_per_head;
   const int ub = (int)((long long)blockIdx.x * p.units / gridDim.x);
@@ -558,6 +562,12 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
   Cur cl = c_first;    // next unit whose LSE is loaded (i+3)
   int i = 0, bi = 0;   // unit and batch being merged
   int nbi = 1;         // batch index of the next batch within its unit
+  // W_V of the first head is a weight (no earlier kernel writes it): copied
+  // before waiting for the previous grid on the stream, so that with a
+  // programmatic dependent launch it overlaps that grid's tail; every read
+  // of o, lse and gate and every write comes after the wait
+  if (kPdlWvFirst && nu > 0) load_wv(c_first.h);
+  grid_dependency_wait();
   if (nu > 0) {
     float lse0;
     load_lse(cl, lse0);
@@ -575,9 +585,9 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
     // of the range; rows that turn out dead are loaded but never merged), so
     // its loads overlap the LSE and W_V round trips (bf16 W_V, copied through
     // registers, goes first: measured faster that way)
-    if (WFMT == 0) load_wv(c_first.h);
+    if (!kPdlWvFirst && WFMT == 0) load_wv(c_first.h);
     issue_blind(cu, bufA);
-    if (WFMT != 0) load_wv(c_first.h);
+    if (!kPdlWvFirst && WFMT != 0) load_wv(c_first.h);
     weights_of(lse0, wcur);
 #pragma unroll
     for (int jj = 0; jj < JB; ++jj)
@@ -682,7 +692,19 @@ static cudaError_t launch_one(const KParams &p, int grid, cudaStream_t s) {
   const size_t smem = 1024 + tc_layout(BN, WFMT, NW).total;
   cudaError_t e = cudaFuncSetAttribute(tc_kernel<BN, WFMT, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  tc_kernel<BN, WFMT, NW><<<grid, NW * 32, smem, s>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(NW * 32, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  // programmatic dependent launch (see the prologue)
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, tc_kernel<BN, WFMT, NW>, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -111,24 +111,22 @@ def test_layouts(lib):
 
 
 def test_kernel_and_tile_choice(lib):
-    # fewer 16-token units than SMs (decode sizes, even a few tokens): the
-    # cluster kernel, 4 CTAs of 256 threads per unit
+    # even tiny token counts run on the persistent tensor-core kernel (a
+    # 16-token tile, mostly empty); decode sizes: 16-token tiles when 32 would
+    # not fill the GPU
     p = mla_combine_uv_plan(args(S=4, H=2, P=4, q=2, spr=2), SMS)
-    assert (p["kernel"], p["tile_tokens"], p["units"], p["grid"], p["threads"]) == (m.MLA_KERNEL_KSPLIT, 16, 2, 8, 256)
+    assert (p["kernel"], p["tile_tokens"], p["units"]) == (m.MLA_KERNEL_TC, 16, 2)
     p = mla_combine_uv_plan(args(S=64, P=16, spr=16), SMS)
-    assert (p["kernel"], p["tile_tokens"], p["units"], p["grid"]) == (m.MLA_KERNEL_KSPLIT, 16, 48, 192)
-    p = mla_combine_uv_plan(args(S=64, P=1, spr=0), SMS)
-    assert (p["kernel"], p["layout"], p["grid"]) == (m.MLA_KERNEL_KSPLIT, 0, 192)
-    # ... unless asked for the persistent kernel, or with more than 16 partials
-    p = mla_combine_uv_plan(args(S=64, P=16, spr=16, kernel=m.MLA_KERNEL_TC), SMS)
     assert (p["kernel"], p["tile_tokens"], p["units"], p["grid"]) == (m.MLA_KERNEL_TC, 16, 48, 48)
-    assert mla_combine_uv_plan(args(S=64, P=20, spr=20), SMS)["kernel"] == m.MLA_KERNEL_TC
+    # the cluster kernel on request: 4 CTAs of 256 threads per 16-token unit
+    p = mla_combine_uv_plan(args(S=64, P=16, spr=16, kernel=m.MLA_KERNEL_KSPLIT), SMS)
+    assert (p["kernel"], p["tile_tokens"], p["units"], p["grid"], p["threads"]) == (m.MLA_KERNEL_KSPLIT, 16, 48, 192, 256)
+    p = mla_combine_uv_plan(args(S=4, H=2, P=1, spr=0, kernel=m.MLA_KERNEL_KSPLIT), SMS)
+    assert (p["kernel"], p["layout"], p["units"], p["grid"]) == (m.MLA_KERNEL_KSPLIT, 0, 2, 8)
+    assert p["smem_bytes"] <= 227 * 1024
     assert status_of(args(S=64, P=20, spr=20, kernel=m.MLA_KERNEL_KSPLIT)) == m.MLA_ERR_KERNEL
     assert status_of(args(S=64, kernel=m.MLA_KERNEL_KSPLIT, tile=32)) == m.MLA_ERR_KERNEL
     assert status_of(args(S=0, S_out=4, kernel=m.MLA_KERNEL_KSPLIT)) == m.MLA_ERR_KERNEL
-    # as many units as SMs: the persistent kernel
-    p = mla_combine_uv_plan(args(S=16 * SMS // 12 + 16, P=16, spr=16), SMS)
-    assert p["kernel"] == m.MLA_KERNEL_TC
     # the large batch: 32-token tiles over a persistent grid of SMS CTAs
     p = mla_combine_uv_plan(args(S=4096, H=96, P=4, q=4, spr=4), SMS)
     assert (p["tile_tokens"], p["units"], p["grid"]) == (32, 96 * 128, SMS)
