@@ -95,6 +95,19 @@ __device__ __forceinline__ float e8m0_inverse(uint32_t sc) {
   return __uint_as_float(0x00400000u);
 }
 
+// The hardware's base-2 exponential and reciprocal (the approximations the
+// page's combine uses; exact at 0 -> 1 and for powers of two, ex2(-inf) = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Sanitise an LSE: NaN and +inf become -inf.
 __device__ __forceinline__ float sane(float x) {
   return (x != x || x == __int_as_float(0x7F800000)) ? __int_as_float(0xFF800000) : x;

@@ -189,10 +189,10 @@ __global__ void __launch_bounds__(kKsThreads, 2) ks_kernel(const __grid_constant
     float m = l;
     for (int s = 1; s < np2; s <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
     if (m == kNegInf) m = 0.0f;
-    const float e = (l16 < n) ? exp2f(__fmul_rn(__fsub_rn(l, m), kLog2e)) : 0.0f;
+    const float e = (l16 < n) ? ex2_approx(__fmul_rn(__fsub_rn(l, m), kLog2e)) : 0.0f;
     float Z = 0.0f;  // sequential fp32 sum in partial order
     for (int j = 0; j < n; ++j) Z = __fadd_rn(Z, __shfl_sync(0xffffffffu, e, (lane & 16) + j));
-    const float inv = (Z == 0.0f) ? 0.0f : __frcp_rn(Z);
+    const float inv = (Z == 0.0f) ? 0.0f : rcp_approx(Z);
     wg = (e == 0.0f) ? 0.0f : __fmul_rn(e, inv);
   }
 

@@ -292,11 +292,11 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
     float m = l;  // max over the token's lanes (np2 <= SEG; lanes past n hold -inf)
     for (int s = 1; s < np2; s <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
     if (m == kNegInf) m = 0.0f;
-    const float e = (my_j < n) ? exp2f(__fmul_rn(__fsub_rn(l, m), kLog2e)) : 0.0f;
+    const float e = (my_j < n) ? ex2_approx(__fmul_rn(__fsub_rn(l, m), kLog2e)) : 0.0f;
     float Z = 0.0f;  // sequential fp32 sum in partial order
     const int seg0 = my_tk * SEG;
     for (int j = 0; j < n; ++j) Z = __fadd_rn(Z, __shfl_sync(0xffffffffu, e, seg0 + j));
-    const float inv = (Z == 0.0f) ? 0.0f : __frcp_rn(Z);
+    const float inv = (Z == 0.0f) ? 0.0f : rcp_approx(Z);
     wg = (e == 0.0f) ? 0.0f : __fmul_rn(e, inv);
   };
 
