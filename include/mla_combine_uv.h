@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define MLA_ABI_VERSION 1
+#define MLA_ABI_VERSION 2
 
 /* W_V storage format. */
 enum {
@@ -131,6 +131,10 @@ typedef struct {
   int32_t grid;          /* CTAs launched (KSPLIT: 4 per unit, as clusters)   */
   int32_t threads;       /* threads per CTA                                   */
   int32_t smem_bytes;    /* dynamic shared memory per CTA                     */
+  int32_t offsets32;     /* 1: every element offset the call dereferences in
+                            o, lse, gate and out is below 2^32, and the kernel
+                            computes addresses in 32-bit arithmetic; 0: 64-bit
+                            (added in ABI version 2)                         */
 } mla_plan;
 
 /*

@@ -69,7 +69,7 @@ class Plan(ctypes.Structure):
     """Mirror of ``mla_plan``."""
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("kernel", "layout", "n_part", "tile_tokens", "units", "grid", "threads",
-                 "smem_bytes")]
+                 "smem_bytes", "offsets32")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

@@ -125,6 +125,25 @@ int32_t plan_impl(const mla_combine_uv_args *a, int32_t num_sms, mla_plan *pl, K
     pl->smem_bytes = (int32_t)mla::tc_smem_bytes(tile, a->w_fmt, n_part);
   }
 
+  // 32-bit offsets when the largest offset the kernels dereference fits
+  // (terms are checked one by one, so nothing here can overflow)
+  const int64_t lim = (int64_t)1 << 32;
+  auto fits = [lim](int64_t n0, int64_t s0, int64_t n1, int64_t s1, int64_t n2, int64_t s2, int64_t extra) {
+    const int64_t n[3] = {n0, n1, n2}, st[3] = {s0, s1, s2};
+    int64_t sum = extra;
+    for (int i = 0; i < 3; ++i) {
+      if (n[i] > 0 && st[i] >= lim) return false;
+      sum += n[i] * st[i];  // < 2^31 * 2^32
+      if (sum >= lim) return false;
+    }
+    return true;
+  };
+  const int64_t last_t = S > 0 ? S - 1 : 0;
+  const bool o_ok = fits(a->P - 1, a->o_sp, last_t, a->o_st, a->H - 1, a->o_sh, 512);
+  const bool l_ok = !a->lse || fits(a->P - 1, a->l_sp, last_t, a->l_st, a->H - 1, a->l_sh, 1);
+  const bool g_ok = (int64_t)a->S_out * a->H * 128 < lim;
+  pl->offsets32 = (o_ok && l_ok && g_ok) ? 1 : 0;
+
   if (kp) {
     KParams &k = *kp;
     std::memset(&k, 0, sizeof k);
@@ -155,6 +174,7 @@ int32_t plan_impl(const mla_combine_uv_args *a, int32_t num_sms, mla_plan *pl, K
     k.tile = pl->tile_tokens;
     k.tiles_per_head = (kernel == MLA_KERNEL_SIMT) ? (a->S_out + 7) / 8 : (S + pl->tile_tokens - 1) / pl->tile_tokens;
     k.units = pl->units;
+    k.off32 = pl->offsets32;
   }
   return MLA_OK;
 }

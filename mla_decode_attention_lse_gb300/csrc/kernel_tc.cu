@@ -106,7 +106,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int
 
 }  // namespace
 
-template <int BN, int WFMT, int NW>
+template <int BN, int WFMT, int NW, bool O32>
 __global__ void __launch_bounds__(NW * 32, 16 / NW)
     tc_kernel(const __grid_constant__ KParams p) {
   constexpr int kWorkers = NW;             // all warps combine, drain and (one of them) issue
@@ -159,6 +159,22 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
   grid_launch_dependents();
   constexpr bool kPdlWvFirst = true;
 
+  // Element offset a * sa + b * sb + c * sc: unsigned 32-bit arithmetic when
+  // the host found every dereferenced offset below 2^32 (O32; addresses formed
+  // for tokens past S may wrap but are never dereferenced), else 64-bit.
+  auto off3 = [](int a, long long sa, int b, long long sb, int c, long long sc) -> unsigned long long {
+    if constexpr (O32)
+      return (uint32_t)((uint32_t)a * (uint32_t)sa + (uint32_t)b * (uint32_t)sb + (uint32_t)c * (uint32_t)sc);
+    else
+      return (unsigned long long)((long long)a * sa + (long long)b * sb + (long long)c * sc);
+  };
+  auto off1 = [](int a, long long sa) -> unsigned long long {
+    if constexpr (O32)
+      return (uint32_t)((uint32_t)a * (uint32_t)sa);
+    else
+      return (unsigned long long)((long long)a * sa);
+  };
+
   const int tph = p.tiles_per_head;
   const int ub = (int)((long long)blockIdx.x * p.units / gridDim.x);
   const int ue = (int)((long long)(blockIdx.x + 1) * p.units / gridDim.x);
@@ -209,7 +225,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
       const int e = rd * 8 + (lane >> 2);
       const int t = c.tile * BN + ws * CPW + e;
       act[rd] = e < CPW && t < p.S;
-      off[rd] = (long long)t * Wrow + c.h * kV + wq * 32 + v8;
+      off[rd] = (long long)off3(t, Wrow, c.h, kV, 1, wq * 32 + v8);
       g[rd] = act[rd] ? __ldg(reinterpret_cast<const uint4 *>(p.gate + off[rd])) : make_uint4(0, 0, 0, 0);
     }
     bool ok = wait_or_abort(bar_mma0 + 8 * bj, (uint32_t)(j / ST) & 1u, p.err, kErrWaitMma, s_abort);
@@ -262,7 +278,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
     lv = kNegInf;
     if (!pass && t < p.S && my_j < n) {
       const int r0 = (layout == kRequestMajor) ? (t / p.q) * p.spr : 0;
-      lv = __ldg(p.lse + (long long)(r0 + my_j) * p.l_sp + (long long)t * p.l_st + (long long)c.h * p.l_sh);
+      lv = __ldg(p.lse + off3(r0 + my_j, p.l_sp, t, p.l_st, c.h, p.l_sh));
     }
   };
 
@@ -277,7 +293,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
     const bool live = pass ? (my_j == 0 && t < p.S) : isfinite(lv);
     if (live) {
       const int r0 = (layout == kRequestMajor) ? (t / p.q) * p.spr : 0;
-      prefetch_l2_bulk(p.o + (long long)t * p.o_st + (long long)c.h * p.o_sh + (long long)(r0 + my_j) * p.o_sp,
+      prefetch_l2_bulk(p.o + off3(t, p.o_st, c.h, p.o_sh, r0 + my_j, p.o_sp),
                        kD * 2);
     }
   };
@@ -310,12 +326,12 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
     for (int tk = 0; tk < TPW; ++tk) {
       const int t = c.tile * BN + warp * TPW + tk;
       const int r0 = (layout == kRequestMajor) ? (t / p.q) * p.spr : 0;
-      const uint16_t *base = p.o + (long long)t * p.o_st + (long long)c.h * p.o_sh + (long long)(r0 + j0) * p.o_sp;
+      const uint16_t *base = p.o + off3(t, p.o_st, c.h, p.o_sh, r0 + j0, p.o_sp);
 #pragma unroll
       for (int jj = 0; jj < JB; ++jj) {
         w[jj][tk] = __shfl_sync(0xffffffffu, wg, tk * SEG + j0 + jj);  // 0 past n
         if (w[jj][tk] != 0.0f && t < p.S) {
-          const uint4 *row = reinterpret_cast<const uint4 *>(base + (long long)jj * p.o_sp);
+          const uint4 *row = reinterpret_cast<const uint4 *>(base + off1(jj, p.o_sp));
           buf[jj][tk][0] = __ldcs(row + lane);
           buf[jj][tk][1] = __ldcs(row + lane + 32);
         } else {
@@ -331,11 +347,11 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
     for (int tk = 0; tk < TPW; ++tk) {
       const int t = c.tile * BN + warp * TPW + tk;
       const int r0 = (layout == kRequestMajor) ? (t / p.q) * p.spr : 0;
-      const uint16_t *base = p.o + (long long)t * p.o_st + (long long)c.h * p.o_sh + (long long)r0 * p.o_sp;
+      const uint16_t *base = p.o + off3(t, p.o_st, c.h, p.o_sh, r0, p.o_sp);
 #pragma unroll
       for (int jj = 0; jj < JB; ++jj) {
         if (jj < n && t < p.S) {
-          const uint4 *row = reinterpret_cast<const uint4 *>(base + (long long)jj * p.o_sp);
+          const uint4 *row = reinterpret_cast<const uint4 *>(base + off1(jj, p.o_sp));
           buf[jj][tk][0] = __ldcs(row + lane);
           buf[jj][tk][1] = __ldcs(row + lane + 32);
         } else {
@@ -687,10 +703,10 @@ size_t tc_smem_bytes(int tile, int w_fmt, int n_part) {
   return 1024 + tc_layout(tile, w_fmt, tc_warps(tile, w_fmt, n_part)).total;
 }
 
-template <int BN, int WFMT, int NW>
+template <int BN, int WFMT, int NW, bool O32>
 static cudaError_t launch_one(const KParams &p, int grid, cudaStream_t s) {
   const size_t smem = 1024 + tc_layout(BN, WFMT, NW).total;
-  cudaError_t e = cudaFuncSetAttribute(tc_kernel<BN, WFMT, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(tc_kernel<BN, WFMT, NW, O32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
@@ -703,17 +719,24 @@ static cudaError_t launch_one(const KParams &p, int grid, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, tc_kernel<BN, WFMT, NW>, p);
+  e = cudaLaunchKernelEx(&cfg, tc_kernel<BN, WFMT, NW, O32>, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-cudaError_t launch_tc(const KParams &p, int grid, cudaStream_t stream) {
+template <bool O32>
+static cudaError_t launch_tc_off(const KParams &p, int grid, cudaStream_t stream) {
   const int nw = tc_warps(p.tile, p.w_fmt, p.n_part);
-  if (p.tile == 16 && p.w_fmt == 0) return launch_one<16, 0, 16>(p, grid, stream);
-  if (p.tile == 16 && p.w_fmt == 1) return nw == 8 ? launch_one<16, 1, 8>(p, grid, stream) : launch_one<16, 1, 16>(p, grid, stream);
-  if (p.tile == 32 && p.n_part <= 16) return p.w_fmt == 0 ? launch_one<32, 0, 16>(p, grid, stream) : launch_one<32, 1, 16>(p, grid, stream);
+  if (p.tile == 16 && p.w_fmt == 0) return launch_one<16, 0, 16, O32>(p, grid, stream);
+  if (p.tile == 16 && p.w_fmt == 1)
+    return nw == 8 ? launch_one<16, 1, 8, O32>(p, grid, stream) : launch_one<16, 1, 16, O32>(p, grid, stream);
+  if (p.tile == 32 && p.n_part <= 16)
+    return p.w_fmt == 0 ? launch_one<32, 0, 16, O32>(p, grid, stream) : launch_one<32, 1, 16, O32>(p, grid, stream);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_tc(const KParams &p, int grid, cudaStream_t stream) {
+  return p.off32 ? launch_tc_off<true>(p, grid, stream) : launch_tc_off<false>(p, grid, stream);
 }
 
 }  // namespace mla

@@ -31,6 +31,8 @@ struct KParams {
   int tile;          // tokens per work unit
   int tiles_per_head;
   int units;         // H * tiles_per_head
+  int off32;         // every element offset into o, lse, gate and out that is
+                     // read or written is below 2^32 (32-bit address arithmetic)
   int *err;          // device error word
 };
 

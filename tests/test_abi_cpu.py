@@ -43,7 +43,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert m.mla_abi_version() == 1
+    assert m.mla_abi_version() == 2
     for s in range(0, 10):
         assert m.mla_status_str(s) and m.mla_status_str(s) != "unknown status"
     assert m.mla_status_str(99) == "unknown status"
@@ -145,6 +145,29 @@ def test_kernel_and_tile_choice(lib):
     assert status_of(args(kernel=7)) == m.MLA_ERR_KERNEL
     p = mla_combine_uv_plan(args(S=0, S_out=5, kernel=m.MLA_KERNEL_TC), SMS)
     assert p["kernel"] == m.MLA_KERNEL_SIMT  # nothing to merge: zero rows only
+
+
+def test_offset_width_choice(lib):
+    # 32-bit address arithmetic when every dereferenced offset is below 2^32
+    assert mla_combine_uv_plan(args(S=4096, H=96, P=4, q=4, spr=4), SMS)["offsets32"] == 1
+    # the request-major decode case (P=1024 partials of a 64-token batch) still fits
+    assert mla_combine_uv_plan(args(S=64, P=1024, spr=16), SMS)["offsets32"] == 1
+    big = 1 << 32
+    a = args(S=64, P=2, spr=2)
+    a.l_sp = big  # the second partial's LSE lies 2^32 elements on
+    assert mla_combine_uv_plan(a, SMS)["offsets32"] == 0
+    a = args(S=64, P=2, spr=2)
+    a.o_sp = big - 256  # the last partial row ends past 2^32
+    assert mla_combine_uv_plan(a, SMS)["offsets32"] == 0
+    a = args(S=64, P=2, spr=2)
+    a.o_sp = big - 64 * 12 * 512 - 512  # ... and the largest that does not
+    assert mla_combine_uv_plan(a, SMS)["offsets32"] == 1
+    # out of 2^25 rows x 128 wide reaches 2^32 elements
+    assert mla_combine_uv_plan(args(S=64, S_out=1 << 25, H=1, P=2, spr=2), SMS)["offsets32"] == 0
+    # a huge stride on a dimension of extent 1 never multiplies
+    a = args(S=1, H=1, P=1, spr=0)
+    a.o_st = a.o_sh = 1 << 40
+    assert mla_combine_uv_plan(a, SMS)["offsets32"] == 1
 
 
 def test_validation_errors(lib):

@@ -201,3 +201,29 @@ def test_cluster_kernel_two_streams(lib, orc):
     a, _ = run_gpu(inp, stream=s1, kernel=KS)
     b, _ = run_gpu(inp, stream=s2, kernel=KS)
     assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("w_fmt", [0, 1])
+def test_wide_offsets_take_the_64_bit_path(lib, orc, w_fmt):
+    # an lse view whose partial stride is 2^32 elements (a 16 GiB allocation,
+    # touched only at the viewed entries): the plan must drop 32-bit address
+    # arithmetic, and that kernel instance must match the oracle too
+    import mla_decode_attention_lse_gb300 as m
+
+    base = custom(S=40, H=3, P=2, q=1, spr=2, w_fmt=w_fmt, neg_inf_frac=0.1, seed=20 + w_fmt)
+    big = torch.empty((1 << 32) + 40 * 3, dtype=torch.float32, device="cuda")
+    try:
+        lse = big.as_strided((2, 40, 3), (1 << 32, 3, 1))
+        lse.copy_(base["lse"])
+        inp = dict(base, lse=lse)
+        out = torch.empty(40, 3 * 128, dtype=torch.bfloat16, device="cuda")
+        args = m.make_args(inp["o"], lse, 1, 2, inp["w_v"], w_fmt, inp["gate"], out, inp["w_scale"])
+        assert m.mla_combine_uv_plan(args)["offsets32"] == 0
+        ref = oracle_problem(orc, dict(inp, lse=lse.contiguous())).full()
+        for kernel in (SIMT, TC, KS):
+            gpu, canary = run_gpu(inp, kernel=kernel, tile=16)
+            assert np.all(canary == CANARY)
+            compare(gpu, ref, seg_mask(inp), f"64-bit offsets, kernel {kernel}")
+    finally:
+        del big
+        torch.cuda.empty_cache()
