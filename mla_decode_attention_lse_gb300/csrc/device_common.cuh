@@ -292,6 +292,19 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_cta(uint32_t addr, uint32_t
   return old;
 }
 
+// Shared-memory compare-and-swap with acquire-release semantics at CTA
+// scope; returns the previous value.
+__device__ __forceinline__ uint32_t atom_cas_acq_rel_cta(uint32_t addr, uint32_t cmp, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.cta.shared::cta.cas.b32 %0, [%1], %2, %3;" : "=r"(old) : "r"(addr), "r"(cmp), "r"(v)
+               : "memory");
+  return old;
+}
+// Shared-memory store with release semantics at CTA scope.
+__device__ __forceinline__ void st_release_cta(uint32_t addr, uint32_t v) {
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 // Bulk prefetch of a global range into L2 (size a multiple of 16 bytes).
 __device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");

@@ -134,16 +134,18 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
   uint16_t *gE = reinterpret_cast<uint16_t *>(gbase + L.epi_off);
   uint64_t *bars = reinterpret_cast<uint64_t *>(gbase + L.bar_off);
   uint32_t *misc = reinterpret_cast<uint32_t *>(bars + 4);
-  // misc[0] TMEM base, misc[1] abort flag, misc[2] last unit whose MMAs were
-  // issued (+1), misc[4..4+ST) arrival counters (one per stage)
+  // misc[0] TMEM base, misc[1] abort flag, misc[4..4+ST) arrival counters,
+  // misc[8..8+ST) pending issues (unit + 1 of a complete unit whose MMAs wait
+  // for a claim; 0 none), misc[12..12+ST) last unit issued on each stage (+1)
   volatile int *s_abort = reinterpret_cast<volatile int *>(&misc[1]);
   const uint32_t bar_mma0 = smem_u32(&bars[0]);  // +8*b, one per stage
   const uint32_t cnt0 = smem_u32(&misc[4]);      // +4*b
+  const uint32_t pend0 = smem_u32(&misc[8]);     // +4*b
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int b = 0; b < ST; ++b) mbar_init(bar_mma0 + 8 * b, 1u);
-    for (int k = 1; k < 4 + ST; ++k) misc[k] = 0u;
+    for (int k = 1; k < 12 + ST; ++k) misc[k] = 0u;
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -158,6 +160,10 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
   // finish (its dependent work waits for this grid's completion)
   grid_launch_dependents();
   constexpr bool kPdlWvFirst = true;
+  // deferred MMA issue (see finish): bf16 W_V, whose 32 MMAs per unit are
+  // costly on the critical path (large batch 358 -> 342 us); the 8 MXFP4 MMAs
+  // measured slightly faster issued at once
+  constexpr bool kDeferIssue = (WFMT == 0);
 
   // Element offset a * sa + b * sb + c * sc: unsigned 32-bit arithmetic when
   // the host found every dereferenced offset below 2^32 (O32; addresses formed
@@ -477,7 +483,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
       }
     }
     tc_commit(bar_mma0 + 8 * b);
-    misc[2] = (uint32_t)(i + 1);
+    misc[12 + b] = (uint32_t)(i + 1);
   };
 
   int drained = 0;        // next unit whose accumulator is drained
@@ -540,21 +546,35 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
     cp_async_wait<0>();  // this thread's W_V copies, if any, have landed
     fence_proxy_async_smem();
     __syncwarp();
-    // arrivals on stage b are numbered across its uses: use i / ST takes
-    // numbers (i / ST) * kWorkers .. + kWorkers - 1; the last one issues
+    // Arrivals on stage b are numbered across its uses: use i / ST takes
+    // numbers (i / ST) * kWorkers .. + kWorkers - 1.  The last arriver, the
+    // unit's slowest warp, would issue the MMAs on the unit's critical path;
+    // instead it marks the unit pending, and the first warp to reach its next
+    // finish claims and issues it (at the latest the last arriver itself, one
+    // unit on).  A unit every warp drains right away (the last of a head, the
+    // CTA's last) is issued at once.  The claim comes before the own arrival,
+    // so the MMAs of consecutive units are issued in order.
     const uint32_t last_no = (uint32_t)(i / ST + 1) * kWorkers - 1u;
+    const bool defer = kDeferIssue && i + 1 < nu && c.tile + 1 != tph;
+    auto arrive = [&]() {  // one lane
+      if (kDeferIssue && i > 0 &&
+          atom_cas_acq_rel_cta(pend0 + 4 * ((i - 1) % ST), (uint32_t)i, 0u) == (uint32_t)i)
+        issue_mma(i - 1, i == 1 || c.tile == 1);  // unit i-1 is of the same head (else it was not deferred)
+      if (atom_add_acq_rel_cta(cnt0 + 4 * b, 1u) == last_no) {
+        if (defer)
+          st_release_cta(pend0 + 4 * b, (uint32_t)(i + 1));
+        else
+          issue_mma(i, i == 0 || c.tile == 0);
+      }
+    };
     if (WFMT != 0 && TPW == 2) {
-      // MXFP4, two tokens per warp: one elected lane arrives (acquiring the other warps'
-      // latents) and, if last, issues; the warp stays converged around it
+      // MXFP4, two tokens per warp: an elected lane of the converged warp
       // (measured faster than a divergent lane 0; with one token per warp it
       // costs registers)
-      uint32_t leader, prev = 0;
-      const bool me = elect_one(leader);
-      if (me) prev = atom_add_acq_rel_cta(cnt0 + 4 * b, 1u);
-      prev = __shfl_sync(0xffffffffu, prev, (int)leader);
-      if (prev == last_no && me) issue_mma(i, i == 0 || c.tile == 0);
+      uint32_t leader;
+      if (elect_one(leader)) arrive();
     } else if (lane == 0) {
-      if (atom_add_acq_rel_cta(cnt0 + 4 * b, 1u) == last_no) issue_mma(i, i == 0 || c.tile == 0);
+      arrive();
     }
     __syncwarp();
     // drain the accumulator of unit i - (ST - 1); before the next unit of
@@ -679,9 +699,11 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
   if (threadIdx.x == 0) {
     // drain what this CTA started (only pending after an abort): the last
     // committed MMAs
-    if (misc[2] > 0u) {
-      const int last = (int)misc[2] - 1;
-      mbar_wait(bar_mma0 + 8 * (last % ST), (uint32_t)(last / ST) & 1u, p.err, kErrWaitTeardown);
+    for (int b = 0; b < ST; ++b) {  // MMAs may come from different threads: every stage's last use
+      if (misc[12 + b] > 0u) {
+        const int last = (int)misc[12 + b] - 1;
+        mbar_wait(bar_mma0 + 8 * b, (uint32_t)(last / ST) & 1u, p.err, kErrWaitTeardown);
+      }
     }
   }
   __syncthreads();
