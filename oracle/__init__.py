@@ -54,6 +54,19 @@ class _Args(ctypes.Structure):
     ]
 
 
+class _PackArgs(ctypes.Structure):
+    _fields_ = [
+        ("S", ctypes.c_int), ("H", ctypes.c_int), ("R", ctypes.c_int), ("q", ctypes.c_int),
+        ("dst", ctypes.c_int),
+        ("o", ctypes.c_void_p), ("o_sr", ctypes.c_int64), ("o_st", ctypes.c_int64),
+        ("o_sh", ctypes.c_int64),
+        ("lse", ctypes.c_void_p), ("l_sr", ctypes.c_int64), ("l_st", ctypes.c_int64),
+        ("l_sh", ctypes.c_int64),
+        ("seq_lens", ctypes.c_void_p), ("sl_sr", ctypes.c_int64),
+        ("qsl", ctypes.c_void_p),
+    ]
+
+
 def lib():
     global _lib
     with _lock:
@@ -88,6 +101,8 @@ def lib():
                                    ctypes.c_void_p]
             L.orc_mla_combine_uv.restype = ctypes.c_int
             L.orc_mla_combine_uv.argtypes = [P(_Args), ctypes.c_void_p]
+            L.orc_dcp_pack.restype = ctypes.c_int
+            L.orc_dcp_pack.argtypes = [P(_PackArgs), ctypes.c_void_p, ctypes.c_void_p]
             _lib = L
     return _lib
 
@@ -161,6 +176,37 @@ class Problem:
         if lib().orc_latent_bf16(ctypes.byref(self.args), t, h, _ptr(lat)) < 0:
             raise ValueError("oracle rejected the problem")
         return lat
+
+
+def dcp_pack(o, lse, seq_lens, qsl, q, dst):
+    """stage_push for destination rank ``dst`` (the page's DCP producer side).
+
+    o        uint16 [R, S, R*H, 512] (bf16 bits; any strides, last dim contiguous)
+    lse      float32 [R, S, R*H]
+    seq_lens int32 [R, S/q] (contiguous rows)
+    qsl      int32 [S/q + 1]
+    Returns (cmb_o uint16 [R, S, H, 512], cmb_lse float32 [R, S, H]).
+    """
+    R, S, RH, d = o.shape
+    assert d == D and o.strides[-1] == o.itemsize and o.dtype == np.uint16 and RH % R == 0
+    assert lse.dtype == np.float32 and lse.shape == (R, S, RH)
+    seq_lens = np.ascontiguousarray(seq_lens, np.int32)
+    qsl = np.ascontiguousarray(qsl, np.int32)
+    assert seq_lens.shape == (R, S // q) and qsl.shape == (S // q + 1,)
+    H = RH // R
+    a = _PackArgs()
+    a.S, a.H, a.R, a.q, a.dst = S, H, R, q, dst
+    a.o = _ptr(o)
+    a.o_sr, a.o_st, a.o_sh, _ = _estrides(o)
+    a.lse = _ptr(lse)
+    a.l_sr, a.l_st, a.l_sh = _estrides(lse)
+    a.seq_lens, a.sl_sr = _ptr(seq_lens), S // q
+    a.qsl = _ptr(qsl)
+    cmb_o = np.empty((R, S, H, D), np.uint16)
+    cmb_lse = np.empty((R, S, H), np.float32)
+    if lib().orc_dcp_pack(ctypes.byref(a), _ptr(cmb_o), _ptr(cmb_lse)) != 0:
+        raise ValueError("oracle rejected the pack problem")
+    return cmb_o, cmb_lse
 
 
 # ---- scalar helpers for the pins ----------------------------------------

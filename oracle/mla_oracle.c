@@ -10,7 +10,7 @@
  * Source of the definition: the vLLM API page
  * "vllm.models.kimi_k3.amd.specialized_decode.mono.attention.mla_back"
  * (functions sane, combine_ranks, combine_splits, stage_combine, stage_uv,
- * wv_loads, mla_post).  The page fixes fp32 for the merge ("LSE-weighted in
+ * wv_loads, mla_post, stage_push).  The page fixes fp32 for the merge ("LSE-weighted in
  * fp32"), so the oracle computes in fp32, single-threaded, in a fixed order:
  * partials in index order, K in ascending order, one rounding per operation
  * (this file is compiled with -ffp-contract=off so no multiply-add is fused).
@@ -290,5 +290,35 @@ int orc_latent_bf16(const orc_args *a, int t, int h, uint16_t *latb) {
   float lat[ORC_D];
   if (orc_combine_latent(a, t, h, lat) < 0) return -1;
   for (int d = 0; d < ORC_D; ++d) latb[d] = orc_f32_to_bf16(lat[d]);
+  return 0;
+}
+
+/* ---- stage_push: the DCP producer side --------------------------------- */
+
+/* The page's stage_push, for one destination rank: for every source rank r,
+ * token t and head h of the destination, the row of global head dst*H + h is
+ * copied unchanged; its LSE is copied bit for bit, or replaced by -inf when
+ * rank r holds no KV of the token's request (seq_lens == 0) or the token lies
+ * past the batch (t >= qsl[S/q]).  Loops in (r, t, h, d) order. */
+int orc_dcp_pack(const orc_pack_args *a, uint16_t *cmb_o, float *cmb_lse) {
+  if (a->S < 0 || a->H < 1 || a->R < 1 || a->q < 1 || a->dst < 0 || a->dst >= a->R) return -1;
+  if (a->S % a->q) return -1;
+  const int rows = a->S > 0 ? a->qsl[a->S / a->q] : 0;
+  const uint32_t neg_inf = 0xFF800000u;
+  for (int r = 0; r < a->R; ++r) {
+    for (int t = 0; t < a->S; ++t) {
+      const int empty = a->seq_lens[(int64_t)r * a->sl_sr + t / a->q] == 0 || t >= rows;
+      for (int h = 0; h < a->H; ++h) {
+        const int64_t g = (int64_t)a->dst * a->H + h;
+        const uint16_t *src = a->o + (int64_t)r * a->o_sr + (int64_t)t * a->o_st + g * a->o_sh;
+        uint16_t *dst = cmb_o + (((int64_t)r * a->S + t) * a->H + h) * ORC_D;
+        for (int d = 0; d < ORC_D; ++d) dst[d] = src[d];
+        uint32_t bits;
+        memcpy(&bits, a->lse + (int64_t)r * a->l_sr + (int64_t)t * a->l_st + g * a->l_sh, 4);
+        if (empty) bits = neg_inf;
+        memcpy(cmb_lse + ((int64_t)r * a->S + t) * a->H + h, &bits, 4);
+      }
+    }
+  }
   return 0;
 }

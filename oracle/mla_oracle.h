@@ -4,8 +4,8 @@
  *
  * Definition followed: the vLLM API page
  * "vllm.models.kimi_k3.amd.specialized_decode.mono.attention.mla_back",
- * functions sane, combine_ranks, combine_splits, stage_combine, stage_uv and
- * mla_post.  All strides are in elements.
+ * functions sane, combine_ranks, combine_splits, stage_combine, stage_uv,
+ * mla_post and stage_push.  All strides are in elements.
  */
 #ifndef MLA_ORACLE_H
 #define MLA_ORACLE_H
@@ -40,5 +40,23 @@ int orc_latent_bf16(const orc_args *a, int t, int h, uint16_t *latb);
 int orc_row(const orc_args *a, int t, int h, uint16_t *seg);
 int orc_rows(const orc_args *a, int n, const int *ts, const int *hs, uint16_t *segs);
 int orc_mla_combine_uv(const orc_args *a, uint16_t *out);
+
+/* stage_push (the DCP producer side) on one machine: every rank's attention
+ * partials, each over all R*H global heads, packed into destination rank
+ * dst's combine buffer, the LSE masked for empty requests and rows past the
+ * batch. */
+typedef struct {
+  int S, H, R, q, dst;     /* tokens, heads per rank, ranks, queries per request, destination */
+  const uint16_t *o;       /* bf16 [R, S, R*H, 512]: source rank r, token t, global head g */
+  int64_t o_sr, o_st, o_sh;
+  const float *lse;        /* f32 [R, S, R*H]                                 */
+  int64_t l_sr, l_st, l_sh;
+  const int32_t *seq_lens; /* int32 [R, S/q]: rank r's local KV length of request j at r*sl_sr + j */
+  int64_t sl_sr;
+  const int32_t *qsl;      /* int32 [S/q + 1]: query start locations; rows >= qsl[S/q] are past the batch */
+} orc_pack_args;
+/* cmb_o bf16 [R, S, H, 512] and cmb_lse f32 [R, S, H], dense.  Returns 0, or
+ * -1 for invalid sizes. */
+int orc_dcp_pack(const orc_pack_args *a, uint16_t *cmb_o, float *cmb_lse);
 
 #endif
