@@ -160,6 +160,54 @@ int32_t mla_combine_uv_plan(const mla_combine_uv_args *args, int32_t num_sms, ml
  */
 int32_t mla_combine_uv_status(void *stream);
 
+/*
+ * The DCP producer side on one GPU -- stage_push of the vLLM page
+ * "vllm.models.kimi_k3.amd.specialized_decode.mono.attention.mla_back"
+ * (section "stage_push(c)"): with decode context parallelism over R ranks,
+ * rank r's attention leaves partials of every token for all R*H global heads;
+ * destination rank p combines, for its H heads, the R ranks' partials.  Here
+ * every rank's partials are resident on one GPU and one call packs rank p's
+ * combine buffer: packed row (r, t, h) is the partial of global head
+ * p*H + h of token t from rank r, copied unchanged; its LSE is copied bit for
+ * bit, or set to -inf when rank r holds no KV of the token's request
+ * (seq_lens[r][t/q] == 0) or the token is past the batch (t >= qsl[S/q]).
+ * The packed buffer is the compact layout mla_combine_uv reads with P = R
+ * (splits_per_request = R): cmb_o o_sp = S*H*512, o_st = H*512, o_sh = 512.
+ */
+typedef struct {
+  int32_t S;             /* token rows of the (padded) batch; S % q == 0      */
+  int32_t H;             /* heads per rank; a rank's partials have R*H heads  */
+  int32_t R;             /* ranks, >= 1; R*H <= 65535                         */
+  int32_t q_per_request; /* queries per request: token t is of request t / q  */
+  int32_t dst_rank;      /* the destination rank p, 0 <= p < R                */
+
+  const void *o;         /* bf16 [R, S, R*H, 512]: (r, t, g, d) at r*o_sr +
+                            t*o_st + g*o_sh + d; strides in elements,
+                            multiples of 8; 16-byte aligned                   */
+  int64_t o_sr, o_st, o_sh;
+  const float *lse;      /* f32 [R, S, R*H]: (r, t, g) at r*l_sr + t*l_st +
+                            g*l_sh                                            */
+  int64_t l_sr, l_st, l_sh;
+  const int32_t *seq_lens; /* int32: rank r's local KV length of request j at
+                              r*sl_sr + j (j < S/q); 0 = empty               */
+  int64_t sl_sr;
+  const int32_t *qsl;    /* int32 [S/q + 1] query start locations; rows
+                            t >= qsl[S/q] are past the batch                  */
+
+  void *cmb_o;           /* bf16 [R, S, H, 512], dense, 16-byte aligned; the
+                            caller owns it                                    */
+  float *cmb_lse;        /* f32 [R, S, H], dense                              */
+} mla_dcp_pack_args;
+
+/*
+ * mla_dcp_pack -- enqueue the pack on `stream` (a copy bound by HBM: it reads
+ * and writes R*S*H rows of 1 KiB).  Returns MLA_OK, or MLA_ERR_NULL /
+ * _SHAPE / _STRIDE / _ALIGN before anything is launched (the outputs are
+ * untouched), or MLA_ERR_CUDA.  S == 0 launches nothing.  (Added in ABI
+ * version 2.)
+ */
+int32_t mla_dcp_pack(const mla_dcp_pack_args *args, void *stream);
+
 /* A short English description of a status code (static storage). */
 const char *mla_status_str(int32_t status);
 

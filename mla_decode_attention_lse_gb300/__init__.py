@@ -37,7 +37,7 @@ MLA_ERR_TIMEOUT = 8
 MLA_ERR_KERNEL = 9
 
 EXPORTED_SYMBOLS = ("mla_combine_uv", "mla_combine_uv_plan", "mla_combine_uv_status",
-                    "mla_status_str", "mla_abi_version")
+                    "mla_dcp_pack", "mla_status_str", "mla_abi_version")
 
 
 class MlaError(RuntimeError):
@@ -75,6 +75,21 @@ class Plan(ctypes.Structure):
         return {n: getattr(self, n) for n, _ in self._fields_}
 
 
+class PackArgs(ctypes.Structure):
+    """Mirror of ``mla_dcp_pack_args``."""
+    _fields_ = [
+        ("S", ctypes.c_int32), ("H", ctypes.c_int32), ("R", ctypes.c_int32),
+        ("q_per_request", ctypes.c_int32), ("dst_rank", ctypes.c_int32),
+        ("o", ctypes.c_void_p), ("o_sr", ctypes.c_int64), ("o_st", ctypes.c_int64),
+        ("o_sh", ctypes.c_int64),
+        ("lse", ctypes.c_void_p), ("l_sr", ctypes.c_int64), ("l_st", ctypes.c_int64),
+        ("l_sh", ctypes.c_int64),
+        ("seq_lens", ctypes.c_void_p), ("sl_sr", ctypes.c_int64),
+        ("qsl", ctypes.c_void_p),
+        ("cmb_o", ctypes.c_void_p), ("cmb_lse", ctypes.c_void_p),
+    ]
+
+
 _lib = None
 
 
@@ -100,6 +115,8 @@ def load_library(path: str | None = None):
     L.mla_status_str.argtypes = [ctypes.c_int32]
     L.mla_abi_version.restype = ctypes.c_int32
     L.mla_abi_version.argtypes = []
+    L.mla_dcp_pack.restype = ctypes.c_int32
+    L.mla_dcp_pack.argtypes = [ctypes.POINTER(PackArgs), ctypes.c_void_p]
     _lib = L
     return L
 
@@ -178,6 +195,58 @@ def mla_combine_uv(o, lse, q_per_request, splits_per_request, w_v, w_fmt, gate, 
     st = load_library().mla_combine_uv(ctypes.byref(a), ctypes.c_void_p(s))
     if st != MLA_OK:
         raise MlaError(st, "mla_combine_uv")
+
+
+def make_pack_args(o, lse, seq_lens, qsl, q_per_request, dst_rank, cmb_o, cmb_lse) -> PackArgs:
+    """Fill ``mla_dcp_pack_args`` from tensors (pointers and element strides)."""
+    R, S, RH, _ = o.shape
+    a = PackArgs()
+    a.S, a.H, a.R = S, RH // R, R
+    a.q_per_request, a.dst_rank = q_per_request, dst_rank
+    a.o = _ptr(o)
+    a.o_sr, a.o_st, a.o_sh = o.stride(0), o.stride(1), o.stride(2)
+    a.lse = _ptr(lse)
+    a.l_sr, a.l_st, a.l_sh = lse.stride(0), lse.stride(1), lse.stride(2)
+    a.seq_lens, a.sl_sr = _ptr(seq_lens), seq_lens.stride(0)
+    a.qsl = _ptr(qsl)
+    a.cmb_o, a.cmb_lse = _ptr(cmb_o), _ptr(cmb_lse)
+    return a
+
+
+def mla_dcp_pack(o, lse, seq_lens, qsl, q_per_request, dst_rank, cmb_o, cmb_lse, stream=None) -> None:
+    """The DCP producer side: pack every rank's partials into rank ``dst_rank``'s
+    combine buffer on CUDA tensors.
+
+    o [R, S, R*H, 512] bf16 (unit-stride last dimension); lse [R, S, R*H] f32;
+    seq_lens [R, S/q] int32 (unit-stride rows); qsl [S/q + 1] int32; cmb_o
+    [R, S, H, 512] bf16 dense; cmb_lse [R, S, H] f32 dense.
+    """
+    import torch
+
+    R, S, RH, d = o.shape
+    if o.dtype != torch.bfloat16 or d != 512 or o.stride(3) != 1 or RH % R:
+        raise ValueError("o must be bf16 [R, S, R*H, 512] with a unit-stride last dimension")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (R, S, RH):
+        raise ValueError("lse must be float32 [R, S, R*H]")
+    if S % q_per_request:
+        raise ValueError("S must be a multiple of q_per_request")
+    if (seq_lens.dtype != torch.int32 or tuple(seq_lens.shape) != (R, S // q_per_request)
+            or seq_lens.stride(1) != 1):
+        raise ValueError("seq_lens must be int32 [R, S/q] with unit-stride rows")
+    if qsl.dtype != torch.int32 or tuple(qsl.shape) != (S // q_per_request + 1,) or not qsl.is_contiguous():
+        raise ValueError("qsl must be a dense int32 [S/q + 1] tensor")
+    H = RH // R
+    if (cmb_o.dtype != torch.bfloat16 or tuple(cmb_o.shape) != (R, S, H, 512) or not cmb_o.is_contiguous()
+            or cmb_lse.dtype != torch.float32 or tuple(cmb_lse.shape) != (R, S, H)
+            or not cmb_lse.is_contiguous()):
+        raise ValueError("cmb_o / cmb_lse must be dense bf16 [R, S, H, 512] / float32 [R, S, H]")
+    if stream is None:
+        stream = torch.cuda.current_stream(o.device)
+    s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    a = make_pack_args(o, lse, seq_lens, qsl, q_per_request, dst_rank, cmb_o, cmb_lse)
+    st = load_library().mla_dcp_pack(ctypes.byref(a), ctypes.c_void_p(s))
+    if st != MLA_OK:
+        raise MlaError(st, "mla_dcp_pack")
 
 
 def mla_combine_uv_plan(args: Args, num_sms: int = 0) -> dict:

@@ -254,6 +254,48 @@ int32_t mla_combine_uv(const mla_combine_uv_args *args, void *stream) {
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
+int32_t mla_dcp_pack(const mla_dcp_pack_args *a, void *stream) {
+  if (!a) return MLA_ERR_NULL;
+  if (a->S < 0 || a->H < 1 || a->R < 1 || a->q_per_request < 1 || a->dst_rank < 0 || a->dst_rank >= a->R)
+    return MLA_ERR_SHAPE;
+  if (a->S % a->q_per_request) return MLA_ERR_SHAPE;
+  if ((int64_t)a->R * a->H > 65535 || (int64_t)a->R * a->S * a->H * 512 >= ((int64_t)1 << 40)) return MLA_ERR_SHAPE;
+  if (a->S == 0) return MLA_OK;
+  if (!a->o || !a->lse || !a->seq_lens || !a->qsl || !a->cmb_o || !a->cmb_lse) return MLA_ERR_NULL;
+  if (!aligned(a->o, 16) || !aligned(a->cmb_o, 16)) return MLA_ERR_ALIGN;
+  if (!aligned(a->lse, 4) || !aligned(a->cmb_lse, 4) || !aligned(a->seq_lens, 4) || !aligned(a->qsl, 4))
+    return MLA_ERR_ALIGN;
+  if (a->o_sr < 0 || a->o_st < 0 || a->o_sh < 0 || a->o_sr % 8 || a->o_st % 8 || a->o_sh % 8) return MLA_ERR_STRIDE;
+  if (a->l_sr < 0 || a->l_st < 0 || a->l_sh < 0 || a->sl_sr < 0) return MLA_ERR_STRIDE;
+  int dev, sms;
+  int *err;
+  int32_t st = device_state(&dev, &sms, &err);
+  if (st != MLA_OK) return st;
+  mla::PackParams p;
+  std::memset(&p, 0, sizeof p);
+  p.S = a->S;
+  p.H = a->H;
+  p.R = a->R;
+  p.q = a->q_per_request;
+  p.dst = a->dst_rank;
+  p.o = static_cast<const uint16_t *>(a->o);
+  p.o_sr = a->o_sr;
+  p.o_st = a->o_st;
+  p.o_sh = a->o_sh;
+  p.lse = a->lse;
+  p.l_sr = a->l_sr;
+  p.l_st = a->l_st;
+  p.l_sh = a->l_sh;
+  p.seq_lens = a->seq_lens;
+  p.sl_sr = a->sl_sr;
+  p.qsl = a->qsl;
+  p.cmb_o = static_cast<uint16_t *>(a->cmb_o);
+  p.cmb_lse = a->cmb_lse;
+  const long long rows = (long long)a->R * a->S * a->H;
+  const cudaError_t e = mla::launch_pack(p, mla::pack_grid(rows, sms), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
 int32_t mla_combine_uv_status(void *stream) {
   int dev, sms;
   int *err;

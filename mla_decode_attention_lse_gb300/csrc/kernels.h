@@ -27,4 +27,9 @@ int ks_threads();
 size_t ks_smem_bytes(int w_fmt);
 cudaError_t launch_ks(const KParams &p, cudaStream_t stream);
 
+// The DCP producer side: pack every rank's partials into one rank's buffer.
+int pack_threads();
+int pack_grid(long long rows, int num_sms);
+cudaError_t launch_pack(const PackParams &p, int grid, cudaStream_t stream);
+
 }  // namespace mla

@@ -36,4 +36,18 @@ struct KParams {
   int *err;          // device error word
 };
 
+// The DCP producer side (pack into one destination rank's combine buffer).
+struct PackParams {
+  int S, H, R, q, dst;  // tokens, heads per rank, ranks, queries per request, destination
+  const uint16_t *o;    // bf16 [R, S, R*H, 512]
+  long long o_sr, o_st, o_sh;
+  const float *lse;     // f32 [R, S, R*H]
+  long long l_sr, l_st, l_sh;
+  const int32_t *seq_lens;  // int32 [R, S/q]
+  long long sl_sr;
+  const int32_t *qsl;   // int32 [S/q + 1]
+  uint16_t *cmb_o;      // bf16 [R, S, H, 512] dense
+  float *cmb_lse;       // f32 [R, S, H] dense
+};
+
 }  // namespace mla

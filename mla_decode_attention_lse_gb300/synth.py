@@ -215,6 +215,72 @@ def custom(S, H, P, q, spr, w_fmt, S_out=None, seed=0, device="cpu", lse_mean=4.
     return make(wl, device=device)
 
 
+@dataclass
+class DcpWorkload:
+    """Decode context parallelism over R ranks, all resident on one GPU: every
+    rank's attention partials over all R*H global heads, its local KV lengths
+    per request (some requests empty on some ranks), the query start
+    locations (rows past ``live`` are padding), and destination rank ``dst``'s
+    W_V heads and gate."""
+    name: str
+    R: int
+    S: int
+    live: int
+    H: int
+    q: int
+    w_fmt: int
+    lse_mean: float = 4.0
+    lse_std: float = 2.0
+    empty_frac: float = 0.05
+    dst: int = 0
+    seed: int = 0
+
+
+DCP_WORKLOADS = {
+    # 8 ranks x 12 heads (96 global), a decode batch of 264 rows of which 256
+    # are live, MXFP4 W_V: the stacked case pushed from its 8 ranks
+    "dcp8_mxfp4": DcpWorkload("dcp8_mxfp4", R=8, S=264, live=256, H=12, q=1, w_fmt=W_MXFP4,
+                              empty_frac=0.05, seed=11),
+}
+
+
+def make_dcp(wl: DcpWorkload | str, device="cpu", seed: int | None = None, w_fmt: int | None = None):
+    """Draw a DCP workload: o_all [R, S, R*H, 512] bf16, lse_all [R, S, R*H]
+    f32, seq_lens [R, S/q] int32 (0 = empty), qsl [S/q + 1] int32, and W_V,
+    its scales and the gate [S, H*128] of the destination's H heads."""
+    if isinstance(wl, str):
+        wl = DCP_WORKLOADS[wl]
+    seed = wl.seed if seed is None else seed
+    w_fmt = wl.w_fmt if w_fmt is None else w_fmt
+    g = _gen(device, seed)
+    R, S, H, q = wl.R, wl.S, wl.H, wl.q
+    nreq = S // q
+    o_all = _normal((R, S, R * H, D), 1.0, g, device, torch.bfloat16)
+    lse_all = _normal((R, S, R * H), wl.lse_std, g, device) + wl.lse_mean
+    seq_lens = torch.randint(1, 4097, (R, nreq), generator=g, device=device, dtype=torch.int32)
+    u = torch.rand((R, nreq), generator=g, device=device)
+    seq_lens[u < wl.empty_frac] = 0
+    j = torch.arange(nreq + 1, device=device, dtype=torch.int32)
+    qsl = torch.clamp(j * q, max=wl.live).to(torch.int32)
+    w = _normal((H, V, D), 1.0 / math.sqrt(D), g, device)
+    if w_fmt == W_BF16:
+        w_v, w_scale = w.to(torch.bfloat16).contiguous(), None
+    else:
+        w_v, w_scale = mxfp4_pack_weights(w)
+    gate = torch.sigmoid(_normal((S, H * V), 1.0, g, device)).to(torch.bfloat16).contiguous()
+    return dict(o_all=o_all, lse_all=lse_all, seq_lens=seq_lens, qsl=qsl, w_v=w_v, w_scale=w_scale,
+                gate=gate, R=R, S=S, S_out=S, H=H, q=q, dst=wl.dst, live=wl.live, w_fmt=w_fmt,
+                name=wl.name)
+
+
+def dcp_pack_bytes(inp) -> int:
+    """Bytes the pack must move: every packed row (1 KiB) and its LSE, read and
+    written, plus the request lengths and query starts it reads."""
+    R, S, H, q = inp["R"], inp["S"], inp["H"], inp["q"]
+    rows = R * S * H
+    return 2 * rows * (D * 2 + 4) + R * (S // q) * 4 + (S // q + 1) * 4
+
+
 def algorithmic_bytes(inp) -> int:
     """Bytes the stage must move: every partial row with a finite sanitised
     LSE (the rows whose weight can be non-zero; P == 1 reads every row), all

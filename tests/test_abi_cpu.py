@@ -69,6 +69,55 @@ def test_args_struct_layout_matches_header(lib, tmp_path):
     assert vals[-1] == ctypes.sizeof(m.Plan)
 
 
+def test_pack_args_struct_layout_matches_header(lib, tmp_path):
+    fields = [f for f, _ in m.PackArgs._fields_]
+    prog = ["#include <stdio.h>", "#include <stddef.h>", '#include "mla_combine_uv.h"',
+            "int main(void) {", 'printf("%zu\\n", sizeof(mla_dcp_pack_args));']
+    prog += [f'printf("%zu\\n", offsetof(mla_dcp_pack_args, {f}));' for f in fields]
+    prog += ["return 0; }"]
+    src = tmp_path / "probe_pack.c"
+    src.write_text("\n".join(prog))
+    exe = tmp_path / "probe_pack"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                           check=True).stdout.split()]
+    assert vals[0] == ctypes.sizeof(m.PackArgs)
+    for f, off in zip(fields, vals[1:]):
+        assert getattr(m.PackArgs, f).offset == off, f
+
+
+def pack_args(S=8, H=2, R=4, q=2, dst=1, **kw):
+    a = m.PackArgs()
+    a.S, a.H, a.R, a.q_per_request, a.dst_rank = S, H, R, q, dst
+    a.o, a.o_sr, a.o_st, a.o_sh = ALIGNED, S * R * H * 512, R * H * 512, 512
+    a.lse, a.l_sr, a.l_st, a.l_sh = ALIGNED * 2, S * R * H, R * H, 1
+    a.seq_lens, a.sl_sr = ALIGNED * 3, S // q
+    a.qsl = ALIGNED * 4
+    a.cmb_o, a.cmb_lse = ALIGNED * 5, ALIGNED * 6
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_pack_validation_errors(lib):
+    pack = lib.mla_dcp_pack
+    st = lambda a: pack(ctypes.byref(a), None)  # noqa: E731  (errors return before any CUDA call)
+    assert st(pack_args(dst=4)) == m.MLA_ERR_SHAPE
+    assert st(pack_args(dst=-1)) == m.MLA_ERR_SHAPE
+    assert st(pack_args(S=7)) == m.MLA_ERR_SHAPE  # S % q
+    assert st(pack_args(R=0)) == m.MLA_ERR_SHAPE
+    assert st(pack_args(H=0)) == m.MLA_ERR_SHAPE
+    assert st(pack_args(R=300, H=300, dst=0)) == m.MLA_ERR_SHAPE  # R*H > 65535
+    assert st(pack_args(qsl=None)) == m.MLA_ERR_NULL
+    assert st(pack_args(cmb_lse=None)) == m.MLA_ERR_NULL
+    assert st(pack_args(o=ALIGNED + 8)) == m.MLA_ERR_ALIGN
+    assert st(pack_args(cmb_o=ALIGNED + 4)) == m.MLA_ERR_ALIGN
+    assert st(pack_args(seq_lens=ALIGNED + 2)) == m.MLA_ERR_ALIGN
+    assert st(pack_args(o_sh=500)) == m.MLA_ERR_STRIDE
+    assert st(pack_args(l_st=-1)) == m.MLA_ERR_STRIDE
+    assert st(pack_args(S=0, o=None, qsl=None)) == m.MLA_OK  # nothing to do, nothing read
+
+
 # ---- planning / validation without a GPU ---------------------------------
 
 ALIGNED = 1 << 20  # fake, 16-byte aligned device addresses: never dereferenced
