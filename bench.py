@@ -422,6 +422,246 @@ def run_gpu(args):
     return line
 
 
+def dcp_oracle_rate(host, budget_s: float):
+    """The oracle's DCP step on the host: the full pack for the destination
+    rank, then the combine on a bounded sample of (t, h) rows.  Returns
+    (tokens/s, description)."""
+    import numpy as np
+
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle
+
+    import torch
+
+    def u16(t):  # bf16 bits as uint16
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    t0 = time.perf_counter()
+    cmb_o, cmb_lse = oracle.dcp_pack(u16(host["o_all"]), host["lse_all"].numpy(), host["seq_lens"].numpy(),
+                                     host["qsl"].numpy(), host["q"], host["dst"])
+    t_pack = time.perf_counter() - t0
+    ws = None if host["w_scale"] is None else host["w_scale"].numpy()
+    w = u16(host["w_v"]) if host["w_fmt"] == 0 else host["w_v"].numpy()
+    pr = oracle.Problem(cmb_o, cmb_lse, host["q"], host["R"], w, ws, host["w_fmt"], u16(host["gate"]))
+    S, H = host["S"], host["H"]
+    rng = np.random.default_rng(0)
+    t0 = time.perf_counter()
+    pr.rows(rng.integers(0, S, 8), rng.integers(0, H, 8))
+    per_row = (time.perf_counter() - t0) / 8
+    n = max(H, int(budget_s / max(per_row, 1e-6)))
+    t0 = time.perf_counter()
+    pr.rows(rng.integers(0, S, n), rng.integers(0, H, n))
+    per_row = (time.perf_counter() - t0) / n
+    step_s = t_pack + per_row * S * H
+    desc = (f"full pack for rank {host['dst']} ({t_pack:.3f} s) + combine timed on {n} random (t, h) "
+            f"rows and scaled to the step's {S * H}, single-threaded oracle")
+    return host["live"] / step_s, desc
+
+
+def run_reference_dcp(args):
+    """The oracle's DCP step (full pack + sampled combine) on the host cores."""
+    import torch
+
+    ws, rank, _ = dist_env()
+    if ws > 1:
+        dist = init_dist(ws, "gloo")
+        if rank != 0:
+            dist.barrier()
+            return
+    from mla_decode_attention_lse_gb300 import synth
+
+    wl = synth.DCP_WORKLOADS[args.workload]
+    inp = synth.make_dcp(wl, device="cpu")
+    budget = args.ref_budget / max(1, args.steps + args.warmup) / 2
+    for _ in range(args.warmup):
+        dcp_oracle_rate(inp, budget)
+    secs, desc = 0.0, ""
+    for _ in range(args.steps):
+        rate, desc = dcp_oracle_rate(inp, budget)
+        secs += inp["live"] / rate
+    value = inp["live"] * args.steps / secs
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "R": wl.R, "S": wl.S, "live": wl.live, "H": wl.H,
+                   "w_fmt": ["bf16", "mxfp4"][inp["w_fmt"]]},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def run_gpu_dcp(args):
+    """One step = the DCP pack for one destination rank + the combine on it."""
+    import torch
+
+    import mla_decode_attention_lse_gb300 as m
+    from mla_decode_attention_lse_gb300 import synth
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = init_dist(ws, "nccl") if ws > 1 else None
+    dev = torch.device("cuda", local)
+    m.load_library()
+    wl = synth.DCP_WORKLOADS[args.workload]
+    seed0 = wl.seed + rank
+    inp = synth.make_dcp(wl, device=dev, seed=seed0)
+    R, S, H, q, dst, live = inp["R"], inp["S"], inp["H"], inp["q"], inp["dst"], inp["live"]
+
+    def with_bufs(c):
+        c["cmb_o"] = torch.empty(R, S, H, 512, dtype=torch.bfloat16, device=dev)
+        c["cmb_lse"] = torch.empty(R, S, H, dtype=torch.float32, device=dev)
+        c["out"] = torch.empty(S, H * 128, dtype=torch.bfloat16, device=dev)
+        return c
+
+    def pack(c, stream=None):
+        m.mla_dcp_pack(c["o_all"], c["lse_all"], c["seq_lens"], c["qsl"], q, dst, c["cmb_o"], c["cmb_lse"],
+                       stream=stream)
+
+    def combine(c, stream=None):
+        m.mla_combine_uv(c["cmb_o"], c["cmb_lse"], q, R, c["w_v"], c["w_fmt"], c["gate"], c["out"],
+                         w_scale=c["w_scale"], stream=stream, kernel=args.kernel, tile_tokens=args.tile)
+
+    inp = with_bufs(inp)
+    pack(inp)
+    torch.cuda.synchronize()
+    cinp = dict(o=inp["cmb_o"], lse=inp["cmb_lse"], q=q, spr=R, w_v=inp["w_v"], w_scale=inp["w_scale"],
+                w_fmt=inp["w_fmt"], gate=inp["gate"], S=S, S_out=S, H=H, P=R)
+    comb_bytes = synth.algorithmic_bytes(cinp)
+    pack_bytes = synth.dcp_pack_bytes(inp)
+    nbytes = pack_bytes + comb_bytes
+    rotate = args.rotate or max(1, -(-L2_DEFEAT_BYTES // nbytes))
+    copies = [inp] + [with_bufs(synth.make_dcp(wl, device=dev, seed=seed0 + 1000 * k)) for k in range(1, rotate)]
+    a = m.make_args(inp["cmb_o"], inp["cmb_lse"], q, R, inp["w_v"], inp["w_fmt"], inp["gate"], inp["out"],
+                    inp["w_scale"], kernel=args.kernel, tile_tokens=args.tile)
+    plan = m.mla_combine_uv_plan(a)
+    kname = {m.MLA_KERNEL_TC: "tc", m.MLA_KERNEL_KSPLIT: "tc_ksplit_cluster4"}.get(plan["kernel"], "simt")
+    stream = torch.cuda.current_stream(dev)
+    for k in range(max(3, args.warmup)):
+        c = copies[k % rotate]
+        pack(c)
+        combine(c)
+    torch.cuda.synchronize()
+    assert m.mla_combine_uv_status(stream) == m.MLA_OK
+
+    def graph_of(fn):
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        with torch.cuda.graph(g, stream=cap):
+            for k in range(args.steps):
+                fn(copies[k % rotate])
+        g.replay()
+        torch.cuda.synchronize()
+        return g
+
+    def timed(g, clk=None):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    g_step = graph_of(lambda c: (pack(c), combine(c)))
+    g_pack = graph_of(pack)
+    g_comb = graph_of(combine)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall0 = time.perf_counter()
+        total_ms = timed(g_step)
+        t_wall = time.perf_counter() - t_wall0
+    clocks = clk.summary()
+    pack_ms = timed(g_pack) / args.steps
+    comb_ms = timed(g_comb) / args.steps
+    assert m.mla_combine_uv_status(stream) == m.MLA_OK
+    total_ms = reduce_max(total_ms, dist, dev)
+    value = replica_rate(live, args.steps, ws, total_ms)
+    peak, peak_kind = load_peaks()
+    kern = {"dcp_pack": (pack_ms, pack_bytes), kname: (comb_ms, comb_bytes)}
+    dom = max(kern, key=lambda k: kern[k][0])
+    achieved = kern[dom][1] / (kern[dom][0] / 1e3) / 1e9
+
+    # end to end: every input the step's calls take, pinned on the host -> device
+    pin = {}
+    for k in ("o_all", "lse_all", "seq_lens", "qsl", "gate"):
+        t = torch.empty(inp[k].shape, dtype=inp[k].dtype, pin_memory=True)
+        t.copy_(inp[k])
+        pin[k] = t
+    out_host = torch.empty(inp["out"].shape, dtype=torch.bfloat16, pin_memory=True)
+    dbuf = with_bufs({k: torch.empty_like(inp[k]) for k in pin})
+    dbuf.update(w_v=inp["w_v"], w_scale=inp["w_scale"], w_fmt=inp["w_fmt"])
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        for k in pin:
+            dbuf[k].copy_(pin[k], non_blocking=True)
+        pack(dbuf, stream=stream)
+        combine(dbuf, stream=stream)
+        out_host.copy_(dbuf["out"], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_value = replica_rate(live, e2e_steps, ws, reduce_max(e0.elapsed_time(e1), dist, dev))
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    line = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and ws == 1:
+            host = {k: (v.cpu() if hasattr(v, "cpu") else v) for k, v in inp.items()}
+            rate, desc = dcp_oracle_rate(host, args.cpu_budget)
+            cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc}
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": f"{args.workload}: decode context parallelism over {R} ranks x {H} heads "
+                                   f"({R * H} global), S={S} rows ({live} live by qsl), q={q}; one step = "
+                                   f"the pack for rank {dst} + the combine on it, "
+                                   f"{'MXFP4' if inp['w_fmt'] else 'bf16'} W_V",
+                       "R": R, "S": S, "live": live, "H": H, "w_fmt": ["bf16", "mxfp4"][inp["w_fmt"]],
+                       "parallelism": f"replicas x{ws}", "kernel": f"dcp_pack + {kname}",
+                       "grid_combine": plan["grid"],
+                       "l2": f"{rotate} independent input copies cycled, one per step: every step reads HBM",
+                       "timing": "CUDA graphs of the timed steps (step, pack alone, combine alone), "
+                                 "per-step time = replay / steps"},
+            "achieved_gbs": achieved,
+            "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": peak_kind,
+                         "traffic": traffic_from_profile(args.workload, dom),
+                         "algorithmic_bytes": kern[dom][1]},
+            "kernels": {k: {"us_per_launch": v[0] * 1e3, "algorithmic_bytes": v[1],
+                            "gbs": v[1] / (v[0] / 1e3) / 1e9} for k, v in kern.items()},
+            "tensor": {"tflops": 2 * S * H * 128 * 512 / (comb_ms / 1e3) / 1e12},
+            "kernel_ms": {"mean": total_ms / args.steps},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clocks,
+            "wall_s": t_wall,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return line
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -443,10 +683,13 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    from mla_decode_attention_lse_gb300 import synth
+
+    dcp = args.workload in synth.DCP_WORKLOADS
     if args.impl == "reference":
-        run_reference(args)
+        run_reference_dcp(args) if dcp else run_reference(args)
     else:
-        run_gpu(args)
+        run_gpu_dcp(args) if dcp else run_gpu(args)
 
 
 if __name__ == "__main__":

@@ -9,8 +9,10 @@
 // [R, S, H, 512] layout the combine reads with P = R.
 //
 // A data move, bound by HBM: one warp moves one 1-KiB row (two 16-byte
-// pieces per lane), four rows per warp and iteration, all loads issued
-// before the stores; lane 0 writes the row's LSE.  Rows are grid-strided.
+// pieces per lane) per iteration, lane 0 its LSE; rows are grid-strided over
+// 64 warps per SM.  Measured on the 8-rank decode batch: 1 row per warp at 64
+// warps per SM 10.5 us, 2 rows 10.8 us, 4 rows at 32 warps 12.4 us, 8 rows
+// 16.9 us -- many warps with little each beat deep batches per warp.
 #include <cuda_runtime.h>
 
 #include "device_common.cuh"
@@ -22,53 +24,52 @@ namespace {
 
 constexpr int kPackWarps = 8;
 constexpr int kPackThreads = kPackWarps * 32;
-constexpr int kPackRows = 4;  // rows per warp and iteration
+constexpr int kPackRows = 1;  // rows per warp and iteration
 
-__global__ void __launch_bounds__(kPackThreads, 4) pack_kernel(const __grid_constant__ PackParams p) {
+__global__ void __launch_bounds__(kPackThreads, 8) pack_kernel(const __grid_constant__ PackParams p) {
   const int lane = threadIdx.x & 31;
-  const long long nrows = (long long)p.R * p.S * p.H;
-  const long long warps = (long long)gridDim.x * kPackWarps;
-  const long long w0 = (long long)blockIdx.x * kPackWarps + (threadIdx.x >> 5);
+  // rows < 2^31 (the host bounds R*S*H*512 below 2^40): 32-bit index math
+  const uint32_t nrows = (uint32_t)p.R * (uint32_t)p.S * (uint32_t)p.H;
+  const uint32_t H = (uint32_t)p.H, S = (uint32_t)p.S;
+  const uint32_t warps = gridDim.x * kPackWarps;
+  const uint32_t w0 = blockIdx.x * kPackWarps + (threadIdx.x >> 5);
   // the partials come from the previous kernel on the stream
   grid_dependency_wait();
   grid_launch_dependents();
   const int rows_live = p.S > 0 ? __ldg(p.qsl + p.S / p.q) : 0;
   const uint32_t neg_inf = 0xFF800000u;
-  for (long long base = w0 * kPackRows; base < nrows; base += warps * kPackRows) {
+  for (uint32_t base = w0 * kPackRows; base < nrows; base += warps * kPackRows) {
     uint4 v[kPackRows][2];
-    const uint16_t *src[kPackRows];
+    uint32_t bits[kPackRows];
+    // every load of the batch first: the rows, and (lane 0) each row's
+    // request length and LSE
 #pragma unroll
     for (int k = 0; k < kPackRows; ++k) {
-      const long long row = base + k;  // packed row (r, t, h), h fastest
-      src[k] = nullptr;
+      const uint32_t row = base + k;  // packed row (r, t, h), h fastest
+      bits[k] = neg_inf;
       if (row < nrows) {
-        const int h = (int)(row % p.H);
-        const long long rt = row / p.H;
-        const int t = (int)(rt % p.S), r = (int)(rt / p.S);
-        src[k] = p.o + (long long)r * p.o_sr + (long long)t * p.o_st + (long long)(p.dst * p.H + h) * p.o_sh;
-        const uint4 *s4 = reinterpret_cast<const uint4 *>(src[k]);
+        const uint32_t rt = row / H, h = row - rt * H;
+        const uint32_t r = rt / S, t = rt - r * S;
+        const long long g = (long long)p.dst * p.H + h;
+        const uint4 *s4 = reinterpret_cast<const uint4 *>(p.o + (long long)r * p.o_sr + (long long)t * p.o_st + g * p.o_sh);
         v[k][0] = __ldcs(s4 + lane);
         v[k][1] = __ldcs(s4 + lane + 32);
+        if (lane == 0) {
+          const bool empty = __ldg(p.seq_lens + (long long)r * p.sl_sr + (long long)(t / (uint32_t)p.q)) == 0 ||
+                             (int)t >= rows_live;
+          const uint32_t b = __float_as_uint(__ldg(p.lse + (long long)r * p.l_sr + (long long)t * p.l_st + g * p.l_sh));
+          bits[k] = empty ? neg_inf : b;
+        }
       }
     }
 #pragma unroll
     for (int k = 0; k < kPackRows; ++k) {
-      const long long row = base + k;
+      const uint32_t row = base + k;
       if (row < nrows) {
-        uint4 *d4 = reinterpret_cast<uint4 *>(p.cmb_o + row * kD);
+        uint4 *d4 = reinterpret_cast<uint4 *>(p.cmb_o + (long long)row * kD);
         d4[lane] = v[k][0];
         d4[lane + 32] = v[k][1];
-        if (lane == 0) {
-          const int h = (int)(row % p.H);
-          const long long rt = row / p.H;
-          const int t = (int)(rt % p.S), r = (int)(rt / p.S);
-          const bool empty = __ldg(p.seq_lens + (long long)r * p.sl_sr + t / p.q) == 0 || t >= rows_live;
-          const uint32_t bits =
-              empty ? neg_inf
-                    : __float_as_uint(__ldg(p.lse + (long long)r * p.l_sr + (long long)t * p.l_st +
-                                            (long long)(p.dst * p.H + h) * p.l_sh));
-          reinterpret_cast<uint32_t *>(p.cmb_lse)[row] = bits;
-        }
+        if (lane == 0) reinterpret_cast<uint32_t *>(p.cmb_lse)[row] = bits[k];
       }
     }
   }
@@ -80,7 +81,7 @@ int pack_threads() { return kPackThreads; }
 int pack_grid(long long rows, int num_sms) {
   const long long per_cta = (long long)kPackWarps * kPackRows;
   long long g = (rows + per_cta - 1) / per_cta;
-  const long long cap = (long long)num_sms * 4;  // resident CTAs: 4 of 256 threads per SM
+  const long long cap = (long long)num_sms * 8;  // resident CTAs: 8 of 256 threads per SM
   if (g > cap) g = cap;
   return (int)(g < 1 ? 1 : g);
 }
