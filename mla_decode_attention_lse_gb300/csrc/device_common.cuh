@@ -310,6 +310,11 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// Prefetch of the 128-byte line holding `src` into L2 (a load-path request).
+__device__ __forceinline__ void prefetch_l2_line(const void *src) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
+}
+
 // ---- cp.async (per-thread asynchronous copies into shared memory) ----------
 
 __device__ __forceinline__ void cp_async_16(uint32_t dst_smem, const void *src) {

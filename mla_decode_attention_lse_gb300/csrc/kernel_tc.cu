@@ -160,6 +160,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
   // finish (its dependent work waits for this grid's completion)
   grid_launch_dependents();
   constexpr bool kPdlWvFirst = true;
+  constexpr bool kGatePrefetch = true;
   // deferred MMA issue (see finish): bf16 W_V, whose 32 MMAs per unit are
   // costly on the critical path (large batch 358 -> 342 us); the 8 MXFP4 MMAs
   // measured slightly faster issued at once
@@ -210,6 +211,18 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
 
   // Epilogue of a unit: TMEM accumulator -> bf16 -> (staged through shared
   // memory, token-major) * gate -> core with 16-byte accesses.
+  // L2 prefetch of the gate lines a later epilogue of unit c reads (one
+  // 128-byte-aligned line per 64-byte token segment of this warp)
+  auto prefetch_gate = [&](const Cur &c) {
+    constexpr int kRounds = (CPW + 7) / 8;
+#pragma unroll
+    for (int rd = 0; rd < kRounds; ++rd) {
+      const int e = rd * 8 + (lane >> 2);
+      const int t = c.tile * BN + ws * CPW + e;
+      if ((lane & 3) == 0 && e < CPW && t < p.S) prefetch_l2_line(p.gate + off3(t, Wrow, c.h, kV, 1, wq * 32));
+    }
+  };
+
   auto epilogue = [&](int j, const Cur &c) -> bool {
     const int bj = j % ST;
     // staging: CPW tokens x 32 V rows of bf16 (512 bytes), addressed in
@@ -581,6 +594,10 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
     // another head, drain everything (W_V is replaced once those MMAs are done)
     const bool head_change = i + 1 < nu && c.tile + 1 == tph;
     bool ok = drain_to(head_change ? i : i - (ST - 1));
+    // the gate of the unit the next finish drains, into L2 a unit ahead (large
+    // batch 315 -> 309 us MXFP4, 344 -> 327 us bf16; at a CTA's last finish
+    // the drain follows at once, so it is skipped)
+    if (kGatePrefetch && i + 1 < nu && drained < nu) prefetch_gate(cdr);
     clear_acc();
     if (ok && head_change) load_wv(c.h + 1);
     return ok;
