@@ -157,6 +157,42 @@ def replica_rate(tokens_per_step: int, steps: int, world: int, max_ms: float) ->
     return tokens_per_step * steps * world / (max_ms / 1e3)
 
 
+def host_cpu() -> dict:
+    """The host the CPU baseline ran on: core count and model name."""
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k = line.split(":")[0].strip().lower()
+                if k in ("model name", "cpu part", "hardware") and not model:
+                    model = line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+
+    parts = {"0xd4f": "Arm Neoverse V2 (CPU part 0xd4f)", "0xd40": "Arm Neoverse V1 (CPU part 0xd40)"}
+    model = parts.get(model, model)
+    return {"nproc": os.cpu_count(), "cpu": model or platform.processor() or platform.machine()}
+
+
+def cold_launch_us(fn, stream, dev) -> float:
+    """One launch after the L2 is flushed (a 256 MB write), timed with events."""
+    import torch
+
+    flush = torch.empty(L2_DEFEAT_BYTES, dtype=torch.uint8, device=dev)
+    times = []
+    for _ in range(3):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e3)
+    del flush
+    return statistics.median(times)
+
+
 def host_copy_inputs(inp):
     import torch
 
@@ -243,7 +279,7 @@ def run_reference(args):
         "config": {"workload": args.workload, "S": wl.S, "H": H, "P": wl.P,
                    "w_fmt": ["bf16", "mxfp4"][inp["w_fmt"]]},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "host": host_cpu()},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -334,6 +370,7 @@ def run_gpu(args):
         dist.barrier()
     clocks = clk.summary()
     assert m.mla_combine_uv_status(stream) == m.MLA_OK
+    cold_us = cold_launch_us(lambda: call(0), stream, dev)
 
     # max over ranks of the timed region
     total_ms = reduce_max(total_ms, dist, dev)
@@ -378,7 +415,7 @@ def run_gpu(args):
             rate, n, dt, _, _ = oracle_sample_rate(host_inp, args.cpu_budget)
             cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                    "sample": f"{n} (t, h) rows ({n // H} tokens x {H} heads) of the same "
-                             f"workload, single-threaded oracle, {dt:.1f} s"}
+                             f"workload, single-threaded oracle, {dt:.1f} s", "host": host_cpu()}
         wl = synth.WORKLOADS[args.workload]
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
@@ -408,6 +445,7 @@ def run_gpu(args):
             "tensor": {"tflops": synth.flops(inp) / avg_kern_s / 1e12},
             "kernel_ms": {"mean": statistics.mean(kern_ms), "min": min(kern_ms),
                           "max": max(kern_ms)},
+            "cold_launch_us": cold_us,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
@@ -487,7 +525,8 @@ def run_reference_dcp(args):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": args.workload, "R": wl.R, "S": wl.S, "live": wl.live, "H": wl.H,
                    "w_fmt": ["bf16", "mxfp4"][inp["w_fmt"]]},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc,
+                         "host": host_cpu()},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -579,6 +618,7 @@ def run_gpu_dcp(args):
     clocks = clk.summary()
     pack_ms = timed(g_pack) / args.steps
     comb_ms = timed(g_comb) / args.steps
+    cold_us = cold_launch_us(lambda: (pack(copies[0]), combine(copies[0])), stream, dev)
     assert m.mla_combine_uv_status(stream) == m.MLA_OK
     total_ms = reduce_max(total_ms, dist, dev)
     value = replica_rate(live, args.steps, ws, total_ms)
@@ -623,7 +663,8 @@ def run_gpu_dcp(args):
         if not args.no_cpu_baseline and ws == 1:
             host = {k: (v.cpu() if hasattr(v, "cpu") else v) for k, v in inp.items()}
             rate, desc = dcp_oracle_rate(host, args.cpu_budget)
-            cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc}
+            cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc,
+                   "host": host_cpu()}
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
@@ -648,6 +689,7 @@ def run_gpu_dcp(args):
                             "gbs": v[1] / (v[0] / 1e3) / 1e9} for k, v in kern.items()},
             "tensor": {"tflops": 2 * S * H * 128 * 512 / (comb_ms / 1e3) / 1e12},
             "kernel_ms": {"mean": total_ms / args.steps},
+            "cold_step_us": cold_us,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
