@@ -19,19 +19,25 @@
 // (group base + m / 32); for token n, lane 32q + n in every lane quadrant q;
 // each 32-bit word holds the scales of four consecutive 32-wide K blocks.
 //
-// Warp roles (512 threads, 16 warps, all alike): each warp combines BN/16 of
-// a unit's tokens into the latent buffer, then runs the epilogue of the
-// previous unit (TMEM -> registers, bf16(acc) * gate -> core).  The warp that
-// completes a unit's latents last (per-buffer monotonic arrival counters)
-// issues that unit's MMAs from one thread and commits them to an
-// mbarrier; being last also proves every warp has drained the previous
-// accumulator in that TMEM buffer.  At a head change every warp first waits
-// for the previous head's MMAs, then copies W_V[h] (and, for MXFP4, its
-// scales) into shared memory.  Latent buffers and TMEM accumulators
-// are double-buffered, so the combine of unit i overlaps the MMA of unit i-1
-// and the epilogue of unit i-2.  A warp issues all of its tokens' partial-row
-// loads of a batch at once and prefetches the next unit's LSE values while
-// they are in flight.
+// Warp roles (16 warps, all alike; 8 for MXFP4 with 16-token tiles): each
+// warp combines its tokens of a unit into the latent buffer, then runs the
+// epilogue of the unit two back (TMEM -> registers, bf16(acc) * gate ->
+// core).  The warp that completes a unit's latents last (per-stage monotonic
+// arrival counters) issues that unit's MMAs from one thread and commits them
+// to an mbarrier (with bf16 W_V it only marks the unit pending, and the
+// first warp to reach its next finish claims and issues it, off the slowest
+// warp's path); either way the issue follows every warp's drain of that TMEM
+// buffer's previous use.  At a head change every warp first waits for the
+// previous head's MMAs, then copies W_V[h] (and, for MXFP4, its scales) into
+// shared memory.  Latent buffers and TMEM accumulators have three stages, so
+// the combine of unit i overlaps the MMA of unit i-1 and the epilogue of
+// unit i-2.  A warp issues a batch of partial-row loads before merging the
+// previous one, loads LSE values three units ahead, and prefetches into L2
+// the gate lines of the unit it drains next.  Launched with programmatic
+// stream serialization: set-up and the first head's W_V copy overlap the
+// previous kernel's tail; everything that reads o, lse or gate, or writes,
+// follows griddepcontrol.wait.  Offsets are 32-bit when the host found every
+// dereferenced offset below 2^32 (the O32 instances), else 64-bit.
 //
 // Semantics follow the vLLM page "vllm.models.kimi_k3.amd.specialized_decode.
 // mono.attention.mla_back": combine_ranks / combine_splits (sane, LSE weights,
@@ -159,7 +165,6 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
   // the next launch on the stream may begin its prologue as this grid's CTAs
   // finish (its dependent work waits for this grid's completion)
   grid_launch_dependents();
-  constexpr bool kPdlWvFirst = true;
   constexpr bool kGatePrefetch = true;
   // deferred MMA issue (see finish): bf16 W_V, whose 32 MMAs per unit are
   // costly on the critical path (large batch 358 -> 342 us); the 8 MXFP4 MMAs
@@ -619,7 +624,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
   // before waiting for the previous grid on the stream, so that with a
   // programmatic dependent launch it overlaps that grid's tail; every read
   // of o, lse and gate and every write comes after the wait
-  if (kPdlWvFirst && nu > 0) load_wv(c_first.h);
+  if (nu > 0) load_wv(c_first.h);
   grid_dependency_wait();
   if (nu > 0) {
     float lse0;
@@ -636,11 +641,8 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
     }
     // the first batch is issued before its weights are known (all partials
     // of the range; rows that turn out dead are loaded but never merged), so
-    // its loads overlap the LSE and W_V round trips (bf16 W_V, copied through
-    // registers, goes first: measured faster that way)
-    if (!kPdlWvFirst && WFMT == 0) load_wv(c_first.h);
+    // its loads overlap the LSE round trip
     issue_blind(cu, bufA);
-    if (!kPdlWvFirst && WFMT != 0) load_wv(c_first.h);
     weights_of(lse0, wcur);
 #pragma unroll
     for (int jj = 0; jj < JB; ++jj)
