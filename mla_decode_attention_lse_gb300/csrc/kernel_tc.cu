@@ -24,10 +24,11 @@
 // epilogue of the unit two back (TMEM -> registers, bf16(acc) * gate ->
 // core).  The warp that completes a unit's latents last (per-stage monotonic
 // arrival counters) issues that unit's MMAs from one thread and commits them
-// to an mbarrier (with bf16 W_V it only marks the unit pending, and the
-// first warp to reach its next finish claims and issues it, off the slowest
-// warp's path); either way the issue follows every warp's drain of that TMEM
-// buffer's previous use.  At a head change every warp first waits for the
+// to an mbarrier -- or, unless every warp drains the unit at once (the last
+// of a head or of the CTA), only marks it pending, and the first warp to
+// reach its next finish claims and issues it, off the slowest warp's path;
+// either way the issue follows every warp's drain of that TMEM buffer's
+// previous use.  At a head change every warp first waits for the
 // previous head's MMAs, then copies W_V[h] (and, for MXFP4, its scales) into
 // shared memory.  Latent buffers and TMEM accumulators have three stages, so
 // the combine of unit i overlaps the MMA of unit i-1 and the epilogue of
@@ -166,10 +167,9 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
   // finish (its dependent work waits for this grid's completion)
   grid_launch_dependents();
   constexpr bool kGatePrefetch = true;
-  // deferred MMA issue (see finish): bf16 W_V, whose 32 MMAs per unit are
-  // costly on the critical path (large batch 358 -> 342 us); the 8 MXFP4 MMAs
-  // measured slightly faster issued at once
-  constexpr bool kDeferIssue = (WFMT == 0);
+  // deferred MMA issue (see finish): off the slowest warp's path (large
+  // batch bf16 358 -> 342 us, MXFP4 309 -> 304 us)
+  constexpr bool kDeferIssue = true;
 
   // Element offset a * sa + b * sb + c * sc: unsigned 32-bit arithmetic when
   // the host found every dereferenced offset below 2^32 (O32; addresses formed
