@@ -167,6 +167,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
   // finish (its dependent work waits for this grid's completion)
   grid_launch_dependents();
   constexpr bool kGatePrefetch = true;
+  constexpr bool kTwoBatchLoop = true;
   // deferred MMA issue (see finish): off the slowest warp's path (large
   // batch bf16 358 -> 342 us, MXFP4 309 -> 304 us)
   constexpr bool kDeferIssue = true;
@@ -688,18 +689,56 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
     return true;
   };
 
-  for (int k = 0; k < total; k += 2) {
-    if (*s_abort) {
-      ok = false;
-      break;
+  // Exactly two batches per unit (the large batch): batch 0 of a unit never
+  // opens a unit and never finishes one, so each copy of the loop body holds
+  // only its own half (one copy of the finish and epilogue in the hot loop).
+  auto opens_next = [&](Buf &nxt, Wts &wn) {  // batch 0 of unit i+1 (cursor cn)
+    weights_of(lse1, wnxt);
+    lse1 = lse2;
+    if (i + 2 < nu) {
+      Cur c2 = cn;
+      advance(c2);
+      prefetch_rows(c2, lse1);
     }
-    if (!step(k, bufA, wA, bufB, wB)) {
-      ok = false;
-      break;
+    if (i + 3 < nu) load_lse(cl, lse2);
+    advance(cl);
+    issue(cn, 0, nxt, wn, wnxt);
+  };
+  if (kTwoBatchLoop && nb == 2) {
+    for (int k = 0; k < total; k += 2) {
+      if (*s_abort) {
+        ok = false;
+        break;
+      }
+      // batch 0 of unit i is in bufA: send batch 1 of unit i, merge batch 0
+      issue(cn, JB, bufB, wB, wcur);
+      advance(cn);
+      consume(bufA, wA);
+      // batch 1 in bufB: send batch 0 of unit i+1, merge batch 1, finish unit i
+      if (k + 2 < total) opens_next(bufA, wA);
+      consume(bufB, wB);
+      if (!finish(i, cu, bufB)) {
+        ok = false;
+        break;
+      }
+      wcur = wnxt;
+      advance(cu);
+      ++i;
     }
-    if (k + 1 < total && !step(k + 1, bufB, wB, bufA, wA)) {
-      ok = false;
-      break;
+  } else {
+    for (int k = 0; k < total; k += 2) {
+      if (*s_abort) {
+        ok = false;
+        break;
+      }
+      if (!step(k, bufA, wA, bufB, wB)) {
+        ok = false;
+        break;
+      }
+      if (k + 1 < total && !step(k + 1, bufB, wB, bufA, wA)) {
+        ok = false;
+        break;
+      }
     }
   }
   if (ok && nu > 0 && !*s_abort) drain_to(nu - 1);
