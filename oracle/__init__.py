@@ -67,6 +67,16 @@ class _PackArgs(ctypes.Structure):
     ]
 
 
+class _AttnArgs(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int), ("q", ctypes.c_int), ("H", ctypes.c_int), ("spr", ctypes.c_int),
+        ("scale", ctypes.c_float),
+        ("qv", ctypes.c_void_p), ("q_st", ctypes.c_int64), ("q_sh", ctypes.c_int64),
+        ("kv", ctypes.c_void_p), ("kv_sb", ctypes.c_int64), ("kv_sl", ctypes.c_int64),
+        ("kv_len", ctypes.c_void_p),
+    ]
+
+
 def lib():
     global _lib
     with _lock:
@@ -103,6 +113,8 @@ def lib():
             L.orc_mla_combine_uv.argtypes = [P(_Args), ctypes.c_void_p]
             L.orc_dcp_pack.restype = ctypes.c_int
             L.orc_dcp_pack.argtypes = [P(_PackArgs), ctypes.c_void_p, ctypes.c_void_p]
+            L.orc_mla_attn_split.restype = ctypes.c_int
+            L.orc_mla_attn_split.argtypes = [P(_AttnArgs), ctypes.c_void_p, ctypes.c_void_p]
             _lib = L
     return _lib
 
@@ -207,6 +219,35 @@ def dcp_pack(o, lse, seq_lens, qsl, q, dst):
     if lib().orc_dcp_pack(ctypes.byref(a), _ptr(cmb_o), _ptr(cmb_lse)) != 0:
         raise ValueError("oracle rejected the pack problem")
     return cmb_o, cmb_lse
+
+
+def mla_attn_split(qv, kv, kv_len, q, spr, scale):
+    """Split-KV MLA decode attention (the partial producer), in double.
+
+    qv     uint16 [S, H, 576] (bf16 bits; any strides, last dim contiguous)
+    kv     uint16 [B, Lmax, 576] (bf16 bits; any strides, last dim contiguous)
+    kv_len int32 [B]; S = B * q
+    Returns (o uint16 [spr, S, H, 512], lse float32 [spr, S, H]).
+    """
+    S, H, dq = qv.shape
+    B, _, dk = kv.shape
+    assert dq == D + 64 and dk == D + 64 and S == B * q
+    assert qv.dtype == np.uint16 and kv.dtype == np.uint16
+    assert qv.strides[-1] == 2 and kv.strides[-1] == 2
+    kv_len = np.ascontiguousarray(kv_len, np.int32)
+    assert kv_len.shape == (B,) and int(kv_len.max(initial=0)) <= kv.shape[1]
+    a = _AttnArgs()
+    a.B, a.q, a.H, a.spr, a.scale = B, q, H, spr, scale
+    a.qv = _ptr(qv)
+    a.q_st, a.q_sh, _ = _estrides(qv)
+    a.kv = _ptr(kv)
+    a.kv_sb, a.kv_sl, _ = _estrides(kv)
+    a.kv_len = _ptr(kv_len)
+    o = np.empty((spr, S, H, D), np.uint16)
+    lse = np.empty((spr, S, H), np.float32)
+    if lib().orc_mla_attn_split(ctypes.byref(a), _ptr(o), _ptr(lse)) != 0:
+        raise ValueError("oracle rejected the attention problem")
+    return o, lse
 
 
 # ---- scalar helpers for the pins ----------------------------------------

@@ -322,3 +322,75 @@ int orc_dcp_pack(const orc_pack_args *a, uint16_t *cmb_o, float *cmb_lse) {
   }
   return 0;
 }
+
+/* ---- the partial producer: split-KV MLA decode attention ----------------
+ *
+ * The page names the producer of the split partials (M1c, mla_attn: o / lse
+ * of dense [splits, S, 12, 512] bf16 / [splits, S, 12] f32) but does not
+ * print it, so this is the plain definition of MLA decode attention in the
+ * absorbed form, split over the KV positions (flash decoding).  Readings
+ * (also in the design doc):
+ *  - a query row is 576 wide: the latent query (512, W_UK already absorbed)
+ *    then the rope query (64); a cached row is the latent (512) then the
+ *    rope key (64); the score is scale * (q . row) over all 576, and the
+ *    value is the row's latent (512) -- the o that the combine merges;
+ *  - the q tokens of a request are its last q cached positions: token i of
+ *    request b sees positions j < kv_len[b] - (q - 1 - i);
+ *  - split r of request b covers positions [r C, (r + 1) C) with
+ *    C = ceil(kv_len[b] / spr), cut to what the token sees; a split with no
+ *    position has lse -inf and o 0;
+ *  - lse is the natural log of sum_j exp(score_j).
+ * Computed in double, one position at a time in ascending order; o is
+ * rounded to fp32 then to bf16 (both to nearest even), lse to fp32. */
+int orc_mla_attn_split(const orc_attn_args *a, uint16_t *o, float *lse) {
+  if (a->B < 0 || a->q < 1 || a->H < 1 || a->spr < 1) return -1;
+  const int S = a->B * a->q;
+  const uint32_t neg_inf = 0xFF800000u;
+  for (int b = 0; b < a->B; ++b) {
+    const int L = a->kv_len[b];
+    if (L < 0) return -1;
+    const int C = (L + a->spr - 1) / a->spr;
+    const uint16_t *kvb = a->kv + (int64_t)b * a->kv_sb;
+    for (int i = 0; i < a->q; ++i) {
+      const int t = b * a->q + i;
+      int vis = L - (a->q - 1 - i);
+      if (vis < 0) vis = 0;
+      for (int h = 0; h < a->H; ++h) {
+        const uint16_t *qr = a->qv + (int64_t)t * a->q_st + (int64_t)h * a->q_sh;
+        for (int r = 0; r < a->spr; ++r) {
+          const int j0 = r * C;
+          const int j1 = (r + 1) * C < vis ? (r + 1) * C : vis;
+          uint16_t *orow = o + (((int64_t)r * S + t) * a->H + h) * ORC_D;
+          float *l = lse + ((int64_t)r * S + t) * a->H + h;
+          if (j1 <= j0) {
+            memset(orow, 0, ORC_D * sizeof *orow);
+            memcpy(l, &neg_inf, 4);
+            continue;
+          }
+          /* scores, their max, the sum of exp(score - max) */
+          double m = -INFINITY;
+          for (int j = j0; j < j1; ++j) {
+            const uint16_t *kr = kvb + (int64_t)j * a->kv_sl;
+            double s = 0.0;
+            for (int k = 0; k < ORC_D + 64; ++k) s += (double)orc_bf16_to_f32(qr[k]) * (double)orc_bf16_to_f32(kr[k]);
+            s *= (double)a->scale;
+            if (s > m) m = s;
+          }
+          double sum = 0.0, acc[ORC_D];
+          for (int d = 0; d < ORC_D; ++d) acc[d] = 0.0;
+          for (int j = j0; j < j1; ++j) {
+            const uint16_t *kr = kvb + (int64_t)j * a->kv_sl;
+            double s = 0.0;
+            for (int k = 0; k < ORC_D + 64; ++k) s += (double)orc_bf16_to_f32(qr[k]) * (double)orc_bf16_to_f32(kr[k]);
+            const double p = exp(s * (double)a->scale - m);
+            sum += p;
+            for (int d = 0; d < ORC_D; ++d) acc[d] += p * (double)orc_bf16_to_f32(kr[d]);
+          }
+          for (int d = 0; d < ORC_D; ++d) orow[d] = orc_f32_to_bf16((float)(acc[d] / sum));
+          *l = (float)(m + log(sum));
+        }
+      }
+    }
+  }
+  return 0;
+}

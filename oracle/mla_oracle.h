@@ -59,4 +59,20 @@ typedef struct {
  * -1 for invalid sizes. */
 int orc_dcp_pack(const orc_pack_args *a, uint16_t *cmb_o, float *cmb_lse);
 
+/* The partial producer: split-KV MLA decode attention in the absorbed form
+ * (the page's M1c, whose partials the combine merges; its kernel is not on
+ * the page, so this follows the plain definition -- see mla_oracle.c). */
+typedef struct {
+  int B, q, H, spr;        /* requests, queries per request (S = B*q), heads, splits per request */
+  float scale;             /* softmax scale applied to q . k                  */
+  const uint16_t *qv;      /* bf16 [S, H, 576]: latent query (512) then rope query (64) */
+  int64_t q_st, q_sh;
+  const uint16_t *kv;      /* bf16 [B, Lmax, 576]: latent (512) then rope key (64) per cached position */
+  int64_t kv_sb, kv_sl;
+  const int32_t *kv_len;   /* int32 [B]: cached positions of request b, its q new ones included */
+} orc_attn_args;
+/* o bf16 [spr, S, H, 512] and lse f32 [spr, S, H], dense (split r of token t
+ * at [r, t, h]).  Returns 0, or -1 for invalid sizes. */
+int orc_mla_attn_split(const orc_attn_args *a, uint16_t *o, float *lse);
+
 #endif
