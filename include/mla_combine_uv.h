@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define MLA_ABI_VERSION 2
+#define MLA_ABI_VERSION 3
 
 /* W_V storage format. */
 enum {
@@ -73,7 +73,9 @@ enum {
   MLA_ERR_CUDA = 7,    /* a CUDA runtime / driver call failed                 */
   MLA_ERR_TIMEOUT = 8, /* a kernel gave up a bounded wait (reported by
                           mla_combine_uv_status)                              */
-  MLA_ERR_KERNEL = 9   /* the requested kernel cannot run this problem        */
+  MLA_ERR_KERNEL = 9,  /* the requested kernel cannot run this problem        */
+  MLA_ERR_DATA = 10    /* a kernel met invalid device data: a kv_len outside
+                          [0, Lmax] (reported by mla_combine_uv_status)       */
 };
 
 /* Kernel selection. */
@@ -156,7 +158,8 @@ int32_t mla_combine_uv_plan(const mla_combine_uv_args *args, int32_t num_sms, ml
  * mla_combine_uv_status -- synchronise `stream`, then read and clear the
  * device-side error word of the current device.  Returns MLA_OK,
  * MLA_ERR_TIMEOUT (a kernel abandoned a bounded wait; its output is
- * undefined) or MLA_ERR_CUDA.
+ * undefined), MLA_ERR_DATA (mla_attn_split_kv met a kv_len outside
+ * [0, Lmax]) or MLA_ERR_CUDA.
  */
 int32_t mla_combine_uv_status(void *stream);
 
@@ -207,6 +210,62 @@ typedef struct {
  * version 2.)
  */
 int32_t mla_dcp_pack(const mla_dcp_pack_args *args, void *stream);
+
+/*
+ * The partial producer: split-KV MLA decode attention in the absorbed form,
+ * writing the partials mla_combine_uv merges.  The vLLM page
+ * "vllm.models.kimi_k3.amd.specialized_decode.mono.attention.mla_back" names
+ * this producer (M1c, mla_attn: o / lse of dense [splits, S, 12, 512] bf16 /
+ * [splits, S, 12] f32, a request's splits merged LSE-weighted) but does not
+ * print it; the call computes the plain definition:
+ *   S = B * q query tokens, token t = b*q + i of request b; head h's query row
+ *   qv[t][h] is 576 wide (the latent query with W_UK absorbed, then the rope
+ *   query); cached position j of request b is kv[b][j] (the latent, 512, then
+ *   the rope key, 64).  Token i sees positions j < kv_len[b] - (q - 1 - i).
+ *   Split r of request b covers [r C, (r + 1) C), C = ceil(kv_len[b] / spr).
+ *   For split r, token t, head h over the positions of the split it sees:
+ *     lse[r][t][h] = ln sum_j exp(scale * qv[t][h] . kv[b][j])   (f32)
+ *     o[r][t][h][:] = sum_j exp(scale * qv . kv[b][j] - lse) kv[b][j][0:512]
+ *   rounded to bf16; a split with no visible position has lse -inf, o 0.
+ * The outputs are the compact layout of mla_combine_uv with P = spr
+ * (splits_per_request = spr): o_sp = S*H*512, o_st = H*512, o_sh = 512.
+ * Scores accumulate in fp32 on the tensor cores, the softmax weights enter the
+ * latent sum as bf16, the sum accumulates in fp32.
+ */
+typedef struct {
+  int32_t B;             /* requests, >= 0                                    */
+  int32_t q;             /* queries per request, 1 <= q <= 32                 */
+  int32_t H;             /* heads, >= 1                                       */
+  int32_t spr;           /* splits per request, >= 1                          */
+  float scale;           /* softmax scale on q . k (finite)                   */
+  const void *qv;        /* bf16 [S, H, 576]: (t, h, k) at t*q_st + h*q_sh + k;
+                            strides in elements, multiples of 8; 16-byte
+                            aligned                                           */
+  int64_t q_st, q_sh;
+  const void *kv;        /* bf16 [B, Lmax, 576]: (b, j, k) at b*kv_sb +
+                            j*kv_sl + k; strides multiples of 8 elements;
+                            16-byte aligned.  Rows past kv_len[b] are never
+                            used (they may hold anything)                     */
+  int64_t kv_sb, kv_sl;
+  int32_t Lmax;          /* cached positions per request in kv, >= 1          */
+  const int32_t *kv_len; /* device int32 [B]: cached positions of request b,
+                            its q new tokens included; a value outside
+                            [0, Lmax] is clamped and reported as
+                            MLA_ERR_DATA by mla_combine_uv_status              */
+  void *o;               /* bf16 [spr, S, H, 512], dense, 16-byte aligned;
+                            caller-owned, every element written               */
+  float *lse;            /* f32 [spr, S, H], dense                            */
+} mla_attn_split_kv_args;
+
+/*
+ * mla_attn_split_kv -- enqueue the attention on `stream` (one CTA per
+ * request, split and group of heads; reads each cached row once per group of
+ * up to 32 / q heads).  Returns MLA_OK, or MLA_ERR_NULL / _SHAPE / _STRIDE /
+ * _ALIGN before anything is launched (outputs untouched), or MLA_ERR_CUDA.
+ * B == 0 launches nothing.  The library allocates nothing; kv_len is read on
+ * the device.  (Added in ABI version 3.)
+ */
+int32_t mla_attn_split_kv(const mla_attn_split_kv_args *args, void *stream);
 
 /* A short English description of a status code (static storage). */
 const char *mla_status_str(int32_t status);

@@ -35,9 +35,10 @@ MLA_ERR_LAYOUT = 6
 MLA_ERR_CUDA = 7
 MLA_ERR_TIMEOUT = 8
 MLA_ERR_KERNEL = 9
+MLA_ERR_DATA = 10
 
 EXPORTED_SYMBOLS = ("mla_combine_uv", "mla_combine_uv_plan", "mla_combine_uv_status",
-                    "mla_dcp_pack", "mla_status_str", "mla_abi_version")
+                    "mla_dcp_pack", "mla_attn_split_kv", "mla_status_str", "mla_abi_version")
 
 
 class MlaError(RuntimeError):
@@ -90,6 +91,19 @@ class PackArgs(ctypes.Structure):
     ]
 
 
+class AttnArgs(ctypes.Structure):
+    """Mirror of ``mla_attn_split_kv_args``."""
+    _fields_ = [
+        ("B", ctypes.c_int32), ("q", ctypes.c_int32), ("H", ctypes.c_int32), ("spr", ctypes.c_int32),
+        ("scale", ctypes.c_float),
+        ("qv", ctypes.c_void_p), ("q_st", ctypes.c_int64), ("q_sh", ctypes.c_int64),
+        ("kv", ctypes.c_void_p), ("kv_sb", ctypes.c_int64), ("kv_sl", ctypes.c_int64),
+        ("Lmax", ctypes.c_int32),
+        ("kv_len", ctypes.c_void_p),
+        ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+    ]
+
+
 _lib = None
 
 
@@ -117,6 +131,8 @@ def load_library(path: str | None = None):
     L.mla_abi_version.argtypes = []
     L.mla_dcp_pack.restype = ctypes.c_int32
     L.mla_dcp_pack.argtypes = [ctypes.POINTER(PackArgs), ctypes.c_void_p]
+    L.mla_attn_split_kv.restype = ctypes.c_int32
+    L.mla_attn_split_kv.argtypes = [ctypes.POINTER(AttnArgs), ctypes.c_void_p]
     _lib = L
     return L
 
@@ -247,6 +263,50 @@ def mla_dcp_pack(o, lse, seq_lens, qsl, q_per_request, dst_rank, cmb_o, cmb_lse,
     st = load_library().mla_dcp_pack(ctypes.byref(a), ctypes.c_void_p(s))
     if st != MLA_OK:
         raise MlaError(st, "mla_dcp_pack")
+
+
+def make_attn_args(qv, kv, kv_len, q, spr, scale, o, lse) -> AttnArgs:
+    """Fill ``mla_attn_split_kv_args`` from tensors (pointers and element strides)."""
+    S, H, _ = qv.shape
+    B, Lmax, _ = kv.shape
+    a = AttnArgs()
+    a.B, a.q, a.H, a.spr, a.scale = B, q, H, spr, float(scale)
+    a.qv, a.q_st, a.q_sh = _ptr(qv), qv.stride(0), qv.stride(1)
+    a.kv, a.kv_sb, a.kv_sl = _ptr(kv), kv.stride(0), kv.stride(1)
+    a.Lmax, a.kv_len = Lmax, _ptr(kv_len)
+    a.o, a.lse = _ptr(o), _ptr(lse)
+    return a
+
+
+def mla_attn_split_kv(qv, kv, kv_len, q, spr, scale, o, lse, stream=None) -> None:
+    """The partial producer: split-KV MLA decode attention on CUDA tensors.
+
+    qv [S, H, 576] bf16 (S = B * q; unit-stride last dimension); kv
+    [B, Lmax, 576] bf16 (unit-stride last dimension); kv_len [B] int32; o
+    [spr, S, H, 512] bf16 dense; lse [spr, S, H] f32 dense.
+    """
+    import torch
+
+    S, H, dq = qv.shape
+    B, Lmax, dk = kv.shape
+    if qv.dtype != torch.bfloat16 or dq != 576 or qv.stride(2) != 1:
+        raise ValueError("qv must be bf16 [S, H, 576] with a unit-stride last dimension")
+    if kv.dtype != torch.bfloat16 or dk != 576 or kv.stride(2) != 1:
+        raise ValueError("kv must be bf16 [B, Lmax, 576] with a unit-stride last dimension")
+    if S != B * q:
+        raise ValueError("qv must hold B * q token rows")
+    if kv_len.dtype != torch.int32 or tuple(kv_len.shape) != (B,) or not kv_len.is_contiguous():
+        raise ValueError("kv_len must be a dense int32 [B] tensor")
+    if (o.dtype != torch.bfloat16 or tuple(o.shape) != (spr, S, H, 512) or not o.is_contiguous()
+            or lse.dtype != torch.float32 or tuple(lse.shape) != (spr, S, H) or not lse.is_contiguous()):
+        raise ValueError("o / lse must be dense bf16 [spr, S, H, 512] / float32 [spr, S, H]")
+    if stream is None:
+        stream = torch.cuda.current_stream(qv.device)
+    s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    a = make_attn_args(qv, kv, kv_len, q, spr, scale, o, lse)
+    st = load_library().mla_attn_split_kv(ctypes.byref(a), ctypes.c_void_p(s))
+    if st != MLA_OK:
+        raise MlaError(st, "mla_attn_split_kv")
 
 
 def mla_combine_uv_plan(args: Args, num_sms: int = 0) -> dict:

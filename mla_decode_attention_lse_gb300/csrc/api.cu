@@ -5,9 +5,11 @@
 // (host_args / mla_post): strided o / lse rows and heads with a unit-stride
 // last dimension, dense gate / core, launch on the caller's stream, every
 // check done before anything is launched.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cmath>
 #include <cstring>
 #include <mutex>
 
@@ -179,6 +181,42 @@ int32_t plan_impl(const mla_combine_uv_args *a, int32_t num_sms, mla_plan *pl, K
   return MLA_OK;
 }
 
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link-time
+// dependency on the driver library).
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// TMA descriptor of the cache tensor [B, Lmax, 576] bf16: boxes of 64
+// elements x 128 positions x 1 request with the 128-byte swizzle (the
+// layout the tensor-core descriptors of the attention kernel read);
+// positions past Lmax read as zero.
+int32_t make_kv_tmap(const mla_attn_split_kv_args *a, CUtensorMap *tm) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+      void *fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return MLA_ERR_CUDA;
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+  }
+  cuuint64_t dims[3] = {576, (cuuint64_t)a->Lmax, (cuuint64_t)a->B};
+  cuuint64_t strides[2] = {(cuuint64_t)a->kv_sl * 2, (cuuint64_t)a->kv_sb * 2};
+  if (a->B == 1) strides[1] = (cuuint64_t)a->Lmax * (cuuint64_t)a->kv_sl * 2;  // unused dimension
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a->kv), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_STRIDE;
+}
+
 // Per-device state: SM count and the error word's device address.
 int32_t device_state(int *dev_out, int *sms_out, int **err_out) {
   int dev = 0;
@@ -216,6 +254,7 @@ const char *mla_status_str(int32_t s) {
     case MLA_ERR_CUDA: return "a CUDA call failed";
     case MLA_ERR_TIMEOUT: return "a kernel abandoned a bounded wait";
     case MLA_ERR_KERNEL: return "the requested kernel cannot run this problem";
+    case MLA_ERR_DATA: return "a kernel met invalid device data (a kv_len outside [0, Lmax])";
     default: return "unknown status";
   }
 }
@@ -296,6 +335,50 @@ int32_t mla_dcp_pack(const mla_dcp_pack_args *a, void *stream) {
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
+int32_t mla_attn_split_kv(const mla_attn_split_kv_args *a, void *stream) {
+  if (!a) return MLA_ERR_NULL;
+  if (a->B < 0 || a->q < 1 || a->q > 32 || a->H < 1 || a->H > 65535 || a->spr < 1 || a->Lmax < 1 ||
+      !std::isfinite(a->scale))
+    return MLA_ERR_SHAPE;
+  const int G = mla::attn_heads_per_cta(a->q, a->H);
+  const int groups = (a->H + G - 1) / G;
+  if ((int64_t)a->B * a->q >= ((int64_t)1 << 31) || (int64_t)a->B * a->spr * groups >= ((int64_t)1 << 31))
+    return MLA_ERR_SHAPE;
+  if (a->B == 0) return MLA_OK;
+  if (!a->qv || !a->kv || !a->kv_len || !a->o || !a->lse) return MLA_ERR_NULL;
+  if (!aligned(a->qv, 16) || !aligned(a->kv, 16) || !aligned(a->o, 16)) return MLA_ERR_ALIGN;
+  if (!aligned(a->lse, 4) || !aligned(a->kv_len, 4)) return MLA_ERR_ALIGN;
+  if (a->q_st < 0 || a->q_sh < 0 || a->q_st % 8 || a->q_sh % 8) return MLA_ERR_STRIDE;
+  if (a->kv_sl < 576 || a->kv_sl % 8 || a->kv_sb < 0 || a->kv_sb % 8 || (a->B > 1 && a->kv_sb == 0))
+    return MLA_ERR_STRIDE;
+  CUtensorMap tm;
+  int32_t st = make_kv_tmap(a, &tm);
+  if (st != MLA_OK) return st;
+  int dev, sms;
+  int *err;
+  st = device_state(&dev, &sms, &err);
+  if (st != MLA_OK) return st;
+  mla::AttnParams p;
+  std::memset(&p, 0, sizeof p);
+  p.B = a->B;
+  p.q = a->q;
+  p.H = a->H;
+  p.spr = a->spr;
+  p.G = G;
+  p.groups = groups;
+  p.Lmax = a->Lmax;
+  p.scale_log2 = a->scale * 1.4426950408889634f;
+  p.qv = static_cast<const uint16_t *>(a->qv);
+  p.q_st = a->q_st;
+  p.q_sh = a->q_sh;
+  p.kv_len = a->kv_len;
+  p.o = static_cast<uint16_t *>(a->o);
+  p.lse = a->lse;
+  p.err = err;
+  const cudaError_t e = mla::launch_attn(p, tm, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
 int32_t mla_combine_uv_status(void *stream) {
   int dev, sms;
   int *err;
@@ -307,7 +390,7 @@ int32_t mla_combine_uv_status(void *stream) {
   if (word != 0) {
     const int zero = 0;
     if (cudaMemcpy(err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return MLA_ERR_CUDA;
-    return MLA_ERR_TIMEOUT;
+    return word == mla::kErrKvLen ? MLA_ERR_DATA : MLA_ERR_TIMEOUT;
   }
   return MLA_OK;
 }

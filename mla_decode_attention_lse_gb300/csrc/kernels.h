@@ -1,6 +1,7 @@
 // kernels.h -- host-side launch entry points of the kernels (internal).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "kparams.h"
@@ -31,5 +32,14 @@ cudaError_t launch_ks(const KParams &p, cudaStream_t stream);
 int pack_threads();
 int pack_grid(long long rows, int num_sms);
 cudaError_t launch_pack(const PackParams &p, int grid, cudaStream_t stream);
+
+// The partial producer (split-KV MLA decode attention): one CTA per
+// (request, split, head group) of q * G <= 32 query rows; the cache tensor
+// [B, Lmax, 576] bf16 is read through `map` (boxes of 64 x 128 x 1, 128-byte
+// swizzle).
+int attn_heads_per_cta(int q, int H);  // G
+int attn_rows(int q, int H);           // the MMA's N: q * G rounded up to 16
+size_t attn_smem_bytes(int rows);
+cudaError_t launch_attn(const AttnParams &p, const CUtensorMap &map, cudaStream_t stream);
 
 }  // namespace mla

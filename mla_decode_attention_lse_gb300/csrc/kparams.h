@@ -10,7 +10,8 @@ enum Layout : int { kPassthrough = 0, kCompact = 1, kRequestMajor = 2 };
 // Error codes a kernel writes into the device error word (first one wins).
 enum KernelError : int { kErrNone = 0, kErrWaitLatent = 1, kErrWaitMma = 2, kErrWaitAccEmpty = 3,
                          kErrWaitWv = 4, kErrWaitTeardown = 5,
-                         kErrWaitPeer = 6 };
+                         kErrWaitPeer = 6, kErrWaitAttn = 7,
+                         kErrKvLen = 8 };
 
 struct KParams {
   int S, S_out, H;
@@ -33,6 +34,22 @@ struct KParams {
   int units;         // H * tiles_per_head
   int off32;         // every element offset into o, lse, gate and out that is
                      // read or written is below 2^32 (32-bit address arithmetic)
+  int *err;          // device error word
+};
+
+// The partial producer: split-KV MLA decode attention (absorbed form).  One
+// CTA per (request, split, head group); the cached rows come by TMA through
+// a tensor map passed beside these parameters.
+struct AttnParams {
+  int B, q, H, spr;  // requests, queries per request, heads, splits per request
+  int G, groups;     // heads per CTA, head groups (ceil(H / G))
+  int Lmax;          // cached positions per request in the cache tensor
+  float scale_log2;  // softmax scale times log2(e)
+  const uint16_t *qv;  // bf16 [S, H, 576] (latent query, then rope query)
+  long long q_st, q_sh;
+  const int32_t *kv_len;  // [B]
+  uint16_t *o;       // bf16 [spr, S, H, 512] dense
+  float *lse;        // f32 [spr, S, H] dense
   int *err;          // device error word
 };
 

@@ -310,3 +310,69 @@ def algorithmic_bytes(inp) -> int:
 
 def flops(inp) -> int:
     return 2 * inp["S"] * inp["H"] * V * D
+
+
+# ---- inputs of the partial producer (split-KV MLA decode attention) -------
+
+@dataclass(frozen=True)
+class AttnWorkload:
+    """One decode step's attention inputs: B requests of q new tokens, H heads,
+    spr splits per request, a cache tensor of Lmax positions per request.
+    Request lengths: a fraction ``short_frac`` of the requests is short
+    (1 .. 4 * spr positions, which leaves some of its splits empty), the rest
+    lies between Lmax / 2 and Lmax."""
+    name: str
+    B: int
+    q: int
+    H: int
+    spr: int
+    Lmax: int
+    short_frac: float = 0.1
+    seed: int = 0
+
+
+ATTN_WORKLOADS = {
+    # the 16-split decode step of the combine's workloads, produced from a
+    # cache of up to 4096 positions per request
+    "attn_splitkv": AttnWorkload("attn_splitkv", B=64, q=1, H=12, spr=16, Lmax=4096, short_frac=0.1, seed=21),
+}
+
+ATTN_K = D + 64  # latent then rope
+
+
+def attn_scale() -> float:
+    """Softmax scale of the MLA heads: 1 / sqrt(128 + 64), the query-key head
+    width before W_UK is absorbed."""
+    return 1.0 / math.sqrt(192.0)
+
+
+def make_attn(wl: AttnWorkload | str, device="cpu", seed: int | None = None):
+    """Draw one attention workload's inputs on ``device``: qv [B q, H, 576]
+    and kv [B, Lmax, 576] bf16 ~N(0, 1), kv_len [B] int32.  Cached rows past a
+    request's length are NaN, so a kernel that reads them shows it."""
+    if isinstance(wl, str):
+        wl = ATTN_WORKLOADS[wl]
+    seed = wl.seed if seed is None else seed
+    g = _gen(device, seed)
+    S = wl.B * wl.q
+    qv = _normal((S, wl.H, ATTN_K), 1.0, g, device, torch.bfloat16)
+    kv = _normal((wl.B, wl.Lmax, ATTN_K), 1.0, g, device, torch.bfloat16)
+    long_len = torch.randint(wl.Lmax // 2, wl.Lmax + 1, (wl.B,), generator=g, device=device, dtype=torch.int32)
+    short_len = torch.randint(1, min(4 * wl.spr, wl.Lmax) + 1, (wl.B,), generator=g, device=device,
+                              dtype=torch.int32)
+    short = torch.rand(wl.B, generator=g, device=device) < wl.short_frac
+    kv_len = torch.where(short, short_len, long_len).to(torch.int32).contiguous()
+    past = torch.arange(wl.Lmax, device=device)[None, :] >= kv_len[:, None].long()
+    kv[past] = float("nan")
+    return dict(qv=qv, kv=kv, kv_len=kv_len, q=wl.q, spr=wl.spr, scale=attn_scale(), B=wl.B, H=wl.H,
+                Lmax=wl.Lmax, wl=wl)
+
+
+def attn_bytes(inp) -> int:
+    """Algorithmic bytes of one attention call: the cached rows inside the
+    requests' lengths (576 bf16 each, once), the query rows, and the o / lse
+    partials written."""
+    B, q, H, spr = inp["B"], inp["q"], inp["H"], inp["spr"]
+    rows = int(inp["kv_len"].long().sum())
+    S = B * q
+    return rows * ATTN_K * 2 + S * H * ATTN_K * 2 + spr * S * H * (D * 2 + 4)

@@ -43,8 +43,8 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert m.mla_abi_version() == 2
-    for s in range(0, 10):
+    assert m.mla_abi_version() == 3
+    for s in range(0, 11):
         assert m.mla_status_str(s) and m.mla_status_str(s) != "unknown status"
     assert m.mla_status_str(99) == "unknown status"
 
@@ -116,6 +116,57 @@ def test_pack_validation_errors(lib):
     assert st(pack_args(o_sh=500)) == m.MLA_ERR_STRIDE
     assert st(pack_args(l_st=-1)) == m.MLA_ERR_STRIDE
     assert st(pack_args(S=0, o=None, qsl=None)) == m.MLA_OK  # nothing to do, nothing read
+
+
+def test_attn_args_struct_layout_matches_header(lib, tmp_path):
+    fields = [f for f, _ in m.AttnArgs._fields_]
+    prog = ["#include <stdio.h>", "#include <stddef.h>", '#include "mla_combine_uv.h"',
+            "int main(void) {", 'printf("%zu\\n", sizeof(mla_attn_split_kv_args));']
+    prog += [f'printf("%zu\\n", offsetof(mla_attn_split_kv_args, {f}));' for f in fields]
+    prog += ["return 0; }"]
+    src = tmp_path / "probe_attn.c"
+    src.write_text("\n".join(prog))
+    exe = tmp_path / "probe_attn"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                           check=True).stdout.split()]
+    assert vals[0] == ctypes.sizeof(m.AttnArgs)
+    for f, off in zip(fields, vals[1:]):
+        assert getattr(m.AttnArgs, f).offset == off, f
+
+
+def attn_args(B=4, q=1, H=12, spr=16, Lmax=256, **kw):
+    a = m.AttnArgs()
+    a.B, a.q, a.H, a.spr, a.scale = B, q, H, spr, 0.07
+    a.qv, a.q_st, a.q_sh = ALIGNED, H * 576, 576
+    a.kv, a.kv_sb, a.kv_sl = ALIGNED * 2, Lmax * 576, 576
+    a.Lmax, a.kv_len = Lmax, ALIGNED * 3
+    a.o, a.lse = ALIGNED * 4, ALIGNED * 5
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_attn_validation_errors(lib):
+    fn = lib.mla_attn_split_kv
+    st = lambda a: fn(ctypes.byref(a), None)  # noqa: E731  (errors return before any CUDA call)
+    assert fn(None, None) == m.MLA_ERR_NULL
+    assert st(attn_args(B=-1)) == m.MLA_ERR_SHAPE
+    assert st(attn_args(q=0)) == m.MLA_ERR_SHAPE
+    assert st(attn_args(q=33)) == m.MLA_ERR_SHAPE
+    assert st(attn_args(H=0)) == m.MLA_ERR_SHAPE
+    assert st(attn_args(spr=0)) == m.MLA_ERR_SHAPE
+    assert st(attn_args(Lmax=0)) == m.MLA_ERR_SHAPE
+    assert st(attn_args(scale=float("inf"))) == m.MLA_ERR_SHAPE
+    assert st(attn_args(kv_len=None)) == m.MLA_ERR_NULL
+    assert st(attn_args(o=None)) == m.MLA_ERR_NULL
+    assert st(attn_args(qv=ALIGNED + 8)) == m.MLA_ERR_ALIGN
+    assert st(attn_args(kv=ALIGNED + 2)) == m.MLA_ERR_ALIGN
+    assert st(attn_args(lse=ALIGNED + 2)) == m.MLA_ERR_ALIGN
+    assert st(attn_args(q_sh=580)) == m.MLA_ERR_STRIDE
+    assert st(attn_args(kv_sl=568)) == m.MLA_ERR_STRIDE  # rows overlap
+    assert st(attn_args(kv_sb=0)) == m.MLA_ERR_STRIDE    # B > 1 requests on one row set
+    assert st(attn_args(B=0, qv=None, kv=None)) == m.MLA_OK  # nothing to do, nothing read
 
 
 # ---- planning / validation without a GPU ---------------------------------
