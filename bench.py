@@ -704,6 +704,257 @@ def run_gpu_dcp(args):
     return line
 
 
+def attn_oracle_rate(host, budget_s: float):
+    """The oracle's attention step on the host: the attention of whole
+    requests (random order) until the budget is spent, scaled to the step's
+    cached rows, plus the combine on a bounded sample of (t, h) rows.
+    Returns (tokens/s, description)."""
+    import numpy as np
+
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle
+
+    import torch
+
+    def u16(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    B, q, H, spr = host["B"], host["q"], host["H"], host["spr"]
+    lens = host["kv_len"].numpy().astype(np.int64)
+    rng = np.random.default_rng(0)
+    order = rng.permutation(B)
+    done_rows, spent, reqs = 0, 0.0, 0
+    for b in order:
+        qv = u16(host["qv"][b * q:(b + 1) * q])
+        kv = u16(host["kv"][b:b + 1, :max(int(lens[b]), 1)])
+        t0 = time.perf_counter()
+        o_r, l_r = oracle.mla_attn_split(qv, kv, lens[b:b + 1].astype(np.int32), q, spr, host["scale"])
+        spent += time.perf_counter() - t0
+        done_rows += max(int(lens[b]), 1)
+        reqs += 1
+        if spent > budget_s / 2:
+            break
+    attn_s = spent * lens.clip(min=1).sum() / done_rows
+    # the combine of the partials, on sampled rows (the last request's partials stand in)
+    pr = oracle.Problem(o_r, l_r, q, spr, u16(host["w_v"]), None, 0, u16(host["gate"][:q]))
+    n = 8
+    t0 = time.perf_counter()
+    pr.rows(rng.integers(0, q, n), rng.integers(0, H, n))
+    per_row = (time.perf_counter() - t0) / n
+    step_s = attn_s + per_row * B * q * H
+    desc = (f"attention of {reqs} whole requests ({done_rows} cached rows, {spent:.2f} s) scaled to the step's "
+            f"{int(lens.clip(min=1).sum())} rows, + combine timed on {n} (t, h) rows and scaled to {B * q * H}; "
+            "single-threaded oracle")
+    return B * q / step_s, desc
+
+
+def run_reference_attn(args):
+    """The oracle's attention -> combine step on the host cores (bounded samples)."""
+    import torch
+
+    ws, rank, _ = dist_env()
+    if ws > 1:
+        dist = init_dist(ws, "gloo")
+        if rank != 0:
+            dist.barrier()
+            return
+    from mla_decode_attention_lse_gb300 import synth
+
+    wl = synth.ATTN_WORKLOADS[args.workload]
+    inp = synth.make_attn(wl, device="cpu")
+    budget = args.ref_budget / max(1, args.steps + args.warmup)
+    for _ in range(args.warmup):
+        attn_oracle_rate(inp, budget)
+    secs, desc = 0.0, ""
+    S = wl.B * wl.q
+    for _ in range(args.steps):
+        rate, desc = attn_oracle_rate(inp, budget)
+        secs += S / rate
+    value = S * args.steps / secs
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "B": wl.B, "q": wl.q, "H": wl.H, "spr": wl.spr, "Lmax": wl.Lmax},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc,
+                         "host": host_cpu()},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def run_gpu_attn(args):
+    """One step = the split-KV attention (partial producer) + the combine of
+    its partials (P = splits, compact)."""
+    import torch
+
+    import mla_decode_attention_lse_gb300 as m
+    from mla_decode_attention_lse_gb300 import synth
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = init_dist(ws, "nccl") if ws > 1 else None
+    dev = torch.device("cuda", local)
+    m.load_library()
+    wl = synth.ATTN_WORKLOADS[args.workload]
+    seed0 = wl.seed + rank
+    B, q, H, spr = wl.B, wl.q, wl.H, wl.spr
+    S = B * q
+
+    def with_bufs(c):
+        c["o"] = torch.empty(spr, S, H, 512, dtype=torch.bfloat16, device=dev)
+        c["lse"] = torch.empty(spr, S, H, dtype=torch.float32, device=dev)
+        c["out"] = torch.empty(S, H * 128, dtype=torch.bfloat16, device=dev)
+        return c
+
+    def attn(c, stream=None):
+        m.mla_attn_split_kv(c["qv"], c["kv"], c["kv_len"], q, spr, c["scale"], c["o"], c["lse"], stream=stream)
+
+    def combine(c, stream=None):
+        m.mla_combine_uv(c["o"], c["lse"], q, spr, c["w_v"], c["w_fmt"], c["gate"], c["out"],
+                         w_scale=c["w_scale"], stream=stream, kernel=args.kernel, tile_tokens=args.tile)
+
+    inp = with_bufs(synth.make_attn(wl, device=dev, seed=seed0))
+    attn(inp)
+    torch.cuda.synchronize()
+    attn_b = synth.attn_bytes(inp)
+    cinp = dict(o=inp["o"], lse=inp["lse"], q=q, spr=spr, w_v=inp["w_v"], w_scale=None, w_fmt=0,
+                gate=inp["gate"], S=S, S_out=S, H=H, P=spr)
+    comb_b = synth.algorithmic_bytes(cinp)
+    rotate = args.rotate or max(1, -(-L2_DEFEAT_BYTES // (attn_b + comb_b)))
+    copies = [inp] + [with_bufs(synth.make_attn(wl, device=dev, seed=seed0 + 1000 * k)) for k in range(1, rotate)]
+    a = m.make_args(inp["o"], inp["lse"], q, spr, inp["w_v"], 0, inp["gate"], inp["out"], None,
+                    kernel=args.kernel, tile_tokens=args.tile)
+    plan = m.mla_combine_uv_plan(a)
+    kname = {m.MLA_KERNEL_TC: "tc", m.MLA_KERNEL_KSPLIT: "tc_ksplit_cluster4"}.get(plan["kernel"], "simt")
+    stream = torch.cuda.current_stream(dev)
+    for k in range(max(3, args.warmup)):
+        c = copies[k % rotate]
+        attn(c)
+        combine(c)
+    torch.cuda.synchronize()
+    assert m.mla_combine_uv_status(stream) == m.MLA_OK
+
+    def graph_of(fn):
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        with torch.cuda.graph(g, stream=cap):
+            for k in range(args.steps):
+                fn(copies[k % rotate])
+        g.replay()
+        torch.cuda.synchronize()
+        return g
+
+    def timed(g):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    g_step = graph_of(lambda c: (attn(c), combine(c)))
+    g_attn = graph_of(attn)
+    g_comb = graph_of(combine)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall0 = time.perf_counter()
+        total_ms = timed(g_step)
+        t_wall = time.perf_counter() - t_wall0
+    clocks = clk.summary()
+    attn_ms = timed(g_attn) / args.steps
+    comb_ms = timed(g_comb) / args.steps
+    cold_us = cold_launch_us(lambda: (attn(copies[0]), combine(copies[0])), stream, dev)
+    assert m.mla_combine_uv_status(stream) == m.MLA_OK
+    total_ms = reduce_max(total_ms, dist, dev)
+    value = replica_rate(S, args.steps, ws, total_ms)
+    peak, peak_kind = load_peaks()
+    kern = {"attn_split_kv": (attn_ms, attn_b), kname: (comb_ms, comb_b)}
+    dom = max(kern, key=lambda k: kern[k][0])
+    achieved = kern[dom][1] / (kern[dom][0] / 1e3) / 1e9
+    rows = int(inp["kv_len"].long().sum())
+    attn_flops = 2.0 * 2 * rows * q * H * 576  # QK^T (576) and PV (512 of it), per visible row and query row
+
+    # end to end: the step's inputs pinned on the host -> device, the core back
+    pin = {}
+    for k in ("qv", "kv", "kv_len", "gate"):
+        t = torch.empty(inp[k].shape, dtype=inp[k].dtype, pin_memory=True)
+        t.copy_(inp[k])
+        pin[k] = t
+    out_host = torch.empty(inp["out"].shape, dtype=torch.bfloat16, pin_memory=True)
+    dbuf = with_bufs({k: torch.empty_like(inp[k]) for k in pin})
+    dbuf.update(w_v=inp["w_v"], w_scale=None, w_fmt=0, scale=inp["scale"])
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        for k in pin:
+            dbuf[k].copy_(pin[k], non_blocking=True)
+        attn(dbuf, stream=stream)
+        combine(dbuf, stream=stream)
+        out_host.copy_(dbuf["out"], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_value = replica_rate(S, e2e_steps, ws, reduce_max(e0.elapsed_time(e1), dist, dev))
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    line = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and ws == 1:
+            host = {k: (v.cpu() if hasattr(v, "cpu") else v) for k, v in inp.items()}
+            rate, desc = attn_oracle_rate(host, args.cpu_budget)
+            cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc,
+                   "host": host_cpu()}
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": f"{args.workload}: split-KV MLA decode attention of {B} requests x q={q}, "
+                                   f"H={H}, {spr} splits per request, up to {wl.Lmax} cached positions "
+                                   f"({rows} in all), then the combine of its partials (bf16 W_V)",
+                       "B": B, "q": q, "H": H, "spr": spr, "Lmax": wl.Lmax, "cached_rows": rows,
+                       "parallelism": f"replicas x{ws}", "kernel": f"attn_split_kv + {kname}",
+                       "l2": f"{rotate} independent input copies cycled, one per step: every step reads HBM",
+                       "timing": "CUDA graphs of the timed steps (step, attention alone, combine alone), "
+                                 "per-step time = replay / steps"},
+            "achieved_gbs": achieved,
+            "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": peak_kind,
+                         "traffic": traffic_from_profile(args.workload, dom),
+                         "algorithmic_bytes": kern[dom][1]},
+            "kernels": {k: {"us_per_launch": v[0] * 1e3, "algorithmic_bytes": v[1],
+                            "gbs": v[1] / (v[0] / 1e3) / 1e9} for k, v in kern.items()},
+            "tensor": {"attn_tflops": attn_flops / (attn_ms / 1e3) / 1e12},
+            "kernel_ms": {"mean": total_ms / args.steps},
+            "cold_step_us": cold_us,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clocks,
+            "wall_s": t_wall,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return line
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -727,6 +978,9 @@ def main():
         args.warmup = 3
     from mla_decode_attention_lse_gb300 import synth
 
+    if args.workload in synth.ATTN_WORKLOADS:
+        run_reference_attn(args) if args.impl == "reference" else run_gpu_attn(args)
+        return
     dcp = args.workload in synth.DCP_WORKLOADS
     if args.impl == "reference":
         run_reference_dcp(args) if dcp else run_reference(args)

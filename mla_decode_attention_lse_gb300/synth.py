@@ -364,8 +364,11 @@ def make_attn(wl: AttnWorkload | str, device="cpu", seed: int | None = None):
     kv_len = torch.where(short, short_len, long_len).to(torch.int32).contiguous()
     past = torch.arange(wl.Lmax, device=device)[None, :] >= kv_len[:, None].long()
     kv[past] = float("nan")
+    # the combine that follows: bf16 W_V ~N(0, 1/sqrt(512)), gate sigmoid(N(0, 1))
+    w_v = _normal((wl.H, V, D), 1.0 / math.sqrt(D), g, device, torch.bfloat16)
+    gate = torch.sigmoid(_normal((S, wl.H * V), 1.0, g, device)).to(torch.bfloat16).contiguous()
     return dict(qv=qv, kv=kv, kv_len=kv_len, q=wl.q, spr=wl.spr, scale=attn_scale(), B=wl.B, H=wl.H,
-                Lmax=wl.Lmax, wl=wl)
+                Lmax=wl.Lmax, wl=wl, w_v=w_v, w_fmt=W_BF16, w_scale=None, gate=gate)
 
 
 def attn_bytes(inp) -> int:
