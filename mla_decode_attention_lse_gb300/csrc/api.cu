@@ -375,7 +375,7 @@ int32_t mla_attn_split_kv(const mla_attn_split_kv_args *a, void *stream) {
   p.o = static_cast<uint16_t *>(a->o);
   p.lse = a->lse;
   p.err = err;
-  const cudaError_t e = mla::launch_attn(p, tm, static_cast<cudaStream_t>(stream));
+  const cudaError_t e = mla::launch_attn(p, tm, sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

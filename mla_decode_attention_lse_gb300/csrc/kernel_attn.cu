@@ -44,7 +44,7 @@ namespace {
 constexpr int kAttnK = kD + 64;     // query / cached row width (576)
 constexpr int kAttnTile = 128;      // positions per tile (MMA M of S^T)
 constexpr int kAttnDbl = 5;         // double-block slots (a tile needs 4)
-constexpr int kAttnThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2..5 softmax
+constexpr int kAttnThreads = 224;   // warp 0 TMA, warp 1 MMA, warps 2..5 softmax, warp 6 queries
 constexpr uint32_t kDblBytes = 2u * kAttnTile * 128u;  // 32 KiB
 constexpr uint32_t kRopeBytes = kAttnTile * 128u;      // 16 KiB
 
@@ -60,8 +60,8 @@ struct AttnLayout {
   static constexpr uint32_t row_off = (lim_off + N * 4u + 7u) & ~7u;  // long long [N]: o / lse row of a query row
   static constexpr uint32_t bar_off = row_off + N * 8u;
   // barriers: full/empty per double slot, full/empty per rope slot, then
-  // s_full, s_free, p_full, o_full, q_full
-  static constexpr int kBars = 2 * kAttnDbl + 2 * kRope + 5;
+  // s_full, s_free, p_full, o_full, q_full, q_free
+  static constexpr int kBars = 2 * kAttnDbl + 2 * kRope + 6;
   static constexpr uint32_t misc_off = bar_off + kBars * 8u;  // TMEM base, abort flag
   static constexpr uint32_t total = misc_off + 16u;
   static constexpr uint32_t tmem_cols = (5 * N <= 128) ? 128u : 256u;  // S^T (N) + O^T (4 N)
@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t *gbase = smem_raw + (sbase - raw);
   float *red = reinterpret_cast<float *>(gbase + L::red_off);
   int *lim_s = reinterpret_cast<int *>(gbase + L::lim_off);
+  long long *orow_s = reinterpret_cast<long long *>(gbase + L::row_off);
   uint32_t *misc = reinterpret_cast<uint32_t *>(gbase + L::misc_off);
   volatile int *s_abort = reinterpret_cast<volatile int *>(&misc[1]);
   const uint32_t bar0 = sbase + L::bar_off;
@@ -108,7 +109,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t s_free = s_full + 8u;   // the softmax warps have read it (4 arrivals)
   const uint32_t p_full = s_full + 16u;  // P^T written, O rescaled (4 arrivals)
   const uint32_t o_full = s_full + 24u;  // a tile's O^T MMAs are complete
-  const uint32_t q_full = s_full + 32u;  // the query rows are in shared memory (4 arrivals)
+  const uint32_t q_full = s_full + 32u;  // an item's query rows are in shared memory
+  const uint32_t q_free = s_full + 40u;  // the item's last S^T MMAs are done: Q may be replaced
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -124,7 +126,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     mbar_init(s_free, 4u);
     mbar_init(p_full, 4u);
     mbar_init(o_full, 1u);
-    mbar_init(q_full, 4u);
+    mbar_init(q_full, 1u);
+    mbar_init(q_free, 1u);
     misc[1] = 0u;
     fence_mbar_init();
   }
@@ -137,47 +140,63 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc_fence_after();
   const uint32_t tmem = misc[0];
 
-  // work item: request b, split r, head group g (the groups of one (b, r)
-  // adjacent, so that they read its cached rows from L2 together)
-  const int g = (int)(blockIdx.x % (unsigned)p.groups);
-  const int br = (int)(blockIdx.x / (unsigned)p.groups);
-  const int r = br % p.spr, b = br / p.spr;
+  // Work items (request b, split r, head group g), the groups of one (b, r)
+  // adjacent so that they read its cached rows from L2 together; CTA c takes
+  // items c, c + grid, ...  Every role walks the same items and numbers the
+  // tiles globally, so the rings and barriers run on across items.
+  const int nitems = p.B * p.spr * p.groups;
+  struct Item {
+    int b, r, g, Lb, j0, jend, ntiles;
+  };
+  auto item_of = [&](int it) {
+    Item I;
+    I.g = it % p.groups;
+    const int br = it / p.groups;
+    I.r = br % p.spr;
+    I.b = br / p.spr;
+    int Lb = __ldg(p.kv_len + I.b);
+    if (Lb < 0 || Lb > p.Lmax) {  // outside the cache tensor: recorded, clamped
+      atomicCAS(p.err, 0, kErrKvLen);
+      Lb = Lb < 0 ? 0 : p.Lmax;
+    }
+    I.Lb = Lb;
+    const int C = (Lb + p.spr - 1) / p.spr;
+    I.j0 = I.r * C;
+    I.jend = min(I.j0 + C, Lb);
+    I.ntiles = I.jend > I.j0 ? (I.jend - I.j0 + kAttnTile - 1) / kAttnTile : 0;
+    return I;
+  };
   // the query rows, the lengths and the cache come from earlier kernels
   grid_dependency_wait();
-  int Lb = __ldg(p.kv_len + b);
-  if (Lb < 0 || Lb > p.Lmax) {  // outside the cache tensor: recorded, clamped
-    if (threadIdx.x == 0) atomicCAS(p.err, 0, kErrKvLen);
-    Lb = Lb < 0 ? 0 : p.Lmax;
-  }
-  const int C = (Lb + p.spr - 1) / p.spr;
-  const int j0 = r * C;
-  const int jend = min(j0 + C, Lb);
-  const int ntiles = jend > j0 ? (jend - j0 + kAttnTile - 1) / kAttnTile : 0;
 
   if (warp == 0) {
     // ---- TMA producer: per tile four double blocks, then the rope block ----
-    if (lane == 0 && ntiles > 0) {
+    if (lane == 0) {
       bool ok = true;
-      int issued_db = 0, issued_r = 0;
-      for (int t = 0; t < ntiles && ok; ++t) {
-        const int y = j0 + t * kAttnTile;
-        for (int c = 0; c < 4 && ok; ++c) {
-          const int gb = 4 * t + c, s = gb % kAttnDbl;
-          if (gb >= kAttnDbl) ok = attn_wait(empty_db(s), (uint32_t)(gb / kAttnDbl - 1) & 1u, p.err, s_abort);
+      int T = 0;                        // tiles started
+      int issued_db = 0, issued_r = 0;  // double blocks / rope blocks whose copies were issued
+      for (int it = blockIdx.x; it < nitems && ok; it += gridDim.x) {
+        const Item I = item_of(it);
+        for (int t = 0; t < I.ntiles && ok; ++t, ++T) {
+          const int y = I.j0 + t * kAttnTile;
+          for (int c = 0; c < 4 && ok; ++c) {
+            const int gb = 4 * T + c, s = gb % kAttnDbl;
+            if (gb >= kAttnDbl) ok = attn_wait(empty_db(s), (uint32_t)(gb / kAttnDbl - 1) & 1u, p.err, s_abort);
+            if (!ok) break;
+            const uint32_t dst = sbase + L::dbl_off + (uint32_t)s * kDblBytes;
+            mbar_arrive_expect_tx(full_db(s), kDblBytes);
+            tma_load_3d(dst, &kv_map, 128 * c, y, I.b, full_db(s));
+            tma_load_3d(dst + kDblBytes / 2, &kv_map, 128 * c + 64, y, I.b, full_db(s));
+            issued_db = gb + 1;
+          }
           if (!ok) break;
-          const uint32_t dst = sbase + L::dbl_off + (uint32_t)s * kDblBytes;
-          mbar_arrive_expect_tx(full_db(s), kDblBytes);
-          tma_load_3d(dst, &kv_map, 128 * c, y, b, full_db(s));
-          tma_load_3d(dst + kDblBytes / 2, &kv_map, 128 * c + 64, y, b, full_db(s));
-          issued_db = gb + 1;
+          const int s = T % NR;
+          if (T >= NR) ok = attn_wait(empty_r(s), (uint32_t)(T / NR - 1) & 1u, p.err, s_abort);
+          if (!ok) break;
+          mbar_arrive_expect_tx(full_r(s), kRopeBytes);
+          tma_load_3d(sbase + L::rope_off + (uint32_t)s * kRopeBytes, &kv_map, kD, y, I.b, full_r(s));
+          issued_r = T + 1;
         }
-        if (!ok) break;
-        const int s = t % NR;
-        if (t >= NR) ok = attn_wait(empty_r(s), (uint32_t)(t / NR - 1) & 1u, p.err, s_abort);
-        if (!ok) break;
-        mbar_arrive_expect_tx(full_r(s), kRopeBytes);
-        tma_load_3d(sbase + L::rope_off + (uint32_t)s * kRopeBytes, &kv_map, kD, y, b, full_r(s));
-        issued_r = t + 1;
       }
       // after an abort: every copy still in flight lands before the CTA exits
       // (bounded waits; on the normal path these phases are complete)
@@ -188,214 +207,259 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else if (warp == 1) {
     // ---- MMA issuer ----
-    if (lane == 0 && ntiles > 0) {
+    if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(128, N);
       constexpr uint32_t kIdO = idesc_bf16(128, N) | (1u << 15);  // A = V^T, MN-major
       const uint32_t tS = tmem, tO = tmem + (uint32_t)N;
       const uint32_t dQ = (uint32_t)smem_desc_sw128(sbase + L::q_off);
       const uint32_t dP = (uint32_t)smem_desc_sw128(sbase + L::p_off);
-      int last_s = -1, last_o = -1;  // last tile whose S^T / O^T MMAs were committed
-      bool ok = attn_wait(q_full, 0u, p.err, s_abort);
-      for (int t = 0; t < ntiles && ok; ++t) {
-        if (t > 0) ok = attn_wait(s_free, (uint32_t)(t - 1) & 1u, p.err, s_abort);
-        // S^T[j, m] = sum_k K[j][k] Q[m][k]: the four latent double blocks ...
-        for (int c = 0; c < 4 && ok; ++c) {
-          const int gb = 4 * t + c, s = gb % kAttnDbl;
-          ok = attn_wait(full_db(s), (uint32_t)(gb / kAttnDbl) & 1u, p.err, s_abort);
+      int last_s = -1, last_o = -1, last_q = -1;  // last committed S^T / O^T tile, Q release
+      bool ok = true;
+      int T = 0, kq = 0;  // tiles, non-empty items
+      for (int it = blockIdx.x; it < nitems && ok; it += gridDim.x) {
+        const Item I = item_of(it);
+        if (I.ntiles == 0) continue;
+        ok = attn_wait(q_full, (uint32_t)kq & 1u, p.err, s_abort);
+        for (int t = 0; t < I.ntiles && ok; ++t, ++T) {
+          if (T > 0) ok = attn_wait(s_free, (uint32_t)(T - 1) & 1u, p.err, s_abort);
+          // S^T[j, m] = sum_k K[j][k] Q[m][k]: the four latent double blocks ...
+          for (int c = 0; c < 4 && ok; ++c) {
+            const int gb = 4 * T + c, s = gb % kAttnDbl;
+            ok = attn_wait(full_db(s), (uint32_t)(gb / kAttnDbl) & 1u, p.err, s_abort);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t dK = (uint32_t)smem_desc_sw128(sbase + L::dbl_off + (uint32_t)s * kDblBytes);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t box = (uint32_t)kk >> 2, k4 = (uint32_t)kk & 3u;
+              tc_mma_f16(tS, desc_sw128_at(dK, box * (kDblBytes / 2) + k4 * 32u),
+                         desc_sw128_at(dQ, (2u * c + box) * (N * 128u) + k4 * 32u), kIdS, (c | kk) ? 1u : 0u);
+            }
+          }
+          if (!ok) break;
+          // ... and the rope block
+          const int sr = T % NR;
+          ok = attn_wait(full_r(sr), (uint32_t)(T / NR) & 1u, p.err, s_abort);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t dK = (uint32_t)smem_desc_sw128(sbase + L::dbl_off + (uint32_t)s * kDblBytes);
+          const uint32_t dR = (uint32_t)smem_desc_sw128(sbase + L::rope_off + (uint32_t)sr * kRopeBytes);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t box = (uint32_t)kk >> 2, k4 = (uint32_t)kk & 3u;
-            tc_mma_f16(tS, desc_sw128_at(dK, box * (kDblBytes / 2) + k4 * 32u),
-                       desc_sw128_at(dQ, (2u * c + box) * (N * 128u) + k4 * 32u), kIdS, (c | kk) ? 1u : 0u);
+          for (int k4 = 0; k4 < 4; ++k4)
+            tc_mma_f16(tS, desc_sw128_at(dR, (uint32_t)k4 * 32u),
+                       desc_sw128_at(dQ, 8u * (N * 128u) + (uint32_t)k4 * 32u), kIdS, 1u);
+          tc_commit(s_full);
+          tc_commit(empty_r(sr));
+          last_s = T;
+          if (t == I.ntiles - 1) {
+            tc_commit(q_free);  // the next item's queries may replace these
+            last_q = kq;
           }
+          // O^T[d, m] += sum_j V^T[d][j] P^T[j, m], once P(t) is written and O
+          // rescaled (which also orders it after the previous item's epilogue)
+          ok = attn_wait(p_full, (uint32_t)T & 1u, p.err, s_abort);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint32_t vbase = sbase + L::dbl_off + (uint32_t)((4 * T + c) % kAttnDbl) * kDblBytes;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)  // 16 positions per step
+              tc_mma_f16(tO + (uint32_t)(c * N), smem_desc_mn_sw128(vbase + (uint32_t)ks * 2048u, kDblBytes / 2),
+                         desc_sw128_at(dP, ((uint32_t)ks >> 2) * (N * 128u) + ((uint32_t)ks & 3u) * 32u), kIdO,
+                         (t | ks) ? 1u : 0u);
+          }
+          tc_commit(o_full);
+          for (int c = 0; c < 4; ++c) tc_commit(empty_db((4 * T + c) % kAttnDbl));
+          last_o = T;
         }
-        if (!ok) break;
-        // ... and the rope block
-        const int sr = t % NR;
-        ok = attn_wait(full_r(sr), (uint32_t)(t / NR) & 1u, p.err, s_abort);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t dR = (uint32_t)smem_desc_sw128(sbase + L::rope_off + (uint32_t)sr * kRopeBytes);
-#pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4)
-          tc_mma_f16(tS, desc_sw128_at(dR, (uint32_t)k4 * 32u), desc_sw128_at(dQ, 8u * (N * 128u) + (uint32_t)k4 * 32u),
-                     kIdS, 1u);
-        tc_commit(s_full);
-        tc_commit(empty_r(sr));
-        last_s = t;
-        // O^T[d, m] += sum_j V^T[d][j] P^T[j, m], once P(t) is written and O rescaled
-        ok = attn_wait(p_full, (uint32_t)t & 1u, p.err, s_abort);
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint32_t vbase = sbase + L::dbl_off + (uint32_t)((4 * t + c) % kAttnDbl) * kDblBytes;
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)  // 16 positions per step
-            tc_mma_f16(tO + (uint32_t)(c * N), smem_desc_mn_sw128(vbase + (uint32_t)ks * 2048u, kDblBytes / 2),
-                       desc_sw128_at(dP, ((uint32_t)ks >> 2) * (N * 128u) + ((uint32_t)ks & 3u) * 32u), kIdO,
-                       (t | ks) ? 1u : 0u);
-        }
-        tc_commit(o_full);
-        for (int c = 0; c < 4; ++c) tc_commit(empty_db((4 * t + c) % kAttnDbl));
-        last_o = t;
+        ++kq;
       }
       // after an abort: the committed MMAs finish before TMEM is freed
       if (last_s >= 0) mbar_wait(s_full, (uint32_t)last_s & 1u, p.err, kErrWaitTeardown);
       if (last_o >= 0) mbar_wait(o_full, (uint32_t)last_o & 1u, p.err, kErrWaitTeardown);
+      if (last_q >= 0) mbar_wait(q_free, (uint32_t)last_q & 1u, p.err, kErrWaitTeardown);
+    }
+  } else if (warp == 6) {
+    // ---- query loader: an item's N rows (row m: token m / G, head g G + m % G;
+    // padded rows zero) into the K-major swizzled Q tile, by cp.async ----
+    bool ok = true;
+    int kq = 0;
+    const int qG = p.q * p.G;
+    for (int it = blockIdx.x; it < nitems && ok; it += gridDim.x) {
+      const Item I = item_of(it);
+      if (I.ntiles == 0) continue;
+      if (kq > 0) ok = attn_wait(q_free, (uint32_t)(kq - 1) & 1u, p.err, s_abort);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      for (int e = lane; e < N * (kAttnK / 8); e += 32) {
+        const int m = e / (kAttnK / 8), ch = e - m * (kAttnK / 8);
+        const int i = m / p.G, h = I.g * p.G + (m - i * p.G);
+        const uint32_t dst = sbase + L::q_off + (uint32_t)((ch >> 3) * (N * 128) + m * 128 + (((ch & 7) ^ (m & 7)) << 4));
+        if (m < qG && h < p.H)
+          cp_async_16(dst, reinterpret_cast<const uint4 *>(p.qv + (long long)(I.b * p.q + i) * p.q_st +
+                                                           (long long)h * p.q_sh) + ch);
+        else
+          *reinterpret_cast<uint4 *>(gbase + (dst - sbase)) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      cp_async_commit();
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_full);
+      ++kq;
     }
   } else {
     // ---- softmax warps 2..5: TMEM lane quadrant warp % 4, one position each ----
-    const int sw = warp - 2;        // 0..3: slot in the cross-warp reductions
-    const int qd = warp & 3;        // TMEM lane quadrant
-    const int pos = qd * 32 + lane;  // position within a tile; O^T row within a latent chunk
+    const int sw = warp - 2;          // 0..3: slot in the cross-warp reductions
+    const int qd = warp & 3;          // TMEM lane quadrant
+    const int pos = qd * 32 + lane;   // position within a tile; O^T row within a latent chunk
     const int ts = threadIdx.x - 64;  // 0..127
     const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);
     const int qG = p.q * p.G;
     const int S = p.B * p.q;
     const float kNegInf = __int_as_float(0xFF800000);
-    if (ntiles > 0) {
-      // query rows -> shared memory (K-major, 128-byte swizzle): row m is token
-      // m / G, head g G + m % G; padded rows are zero
-      for (int e = ts; e < N * (kAttnK / 8); e += 128) {
-        const int m = e / (kAttnK / 8), ch = e - m * (kAttnK / 8);
-        const int i = m / p.G, h = g * p.G + (m - i * p.G);
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (m < qG && h < p.H)
-          v = __ldg(reinterpret_cast<const uint4 *>(p.qv + (long long)(b * p.q + i) * p.q_st + (long long)h * p.q_sh) +
-                    ch);
-        *reinterpret_cast<uint4 *>(gbase + L::q_off + (ch >> 3) * (N * 128) + m * 128 + (((ch & 7) ^ (m & 7)) << 4)) = v;
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(q_full);
-    }
-    // per query row: the positions of this split it sees, counted from j0
-    if (ts < N) {
-      const int m = ts, i = m / p.G, h = g * p.G + (m - i * p.G);
-      int lim = 0;
-      if (m < qG && h < p.H) lim = min(jend, Lb - (p.q - 1 - i)) - j0;
-      lim_s[m] = lim < 0 ? 0 : lim;
-    }
-    named_barrier(1, 128);
-
-    float m_run[N], l_part[N];  // running column max (log2 units), this position's share of the sums
-#pragma unroll
-    for (int m = 0; m < N; ++m) {
-      m_run[m] = kNegInf;
-      l_part[m] = 0.0f;
-    }
+    constexpr float kLn2 = 0.6931471805599453f;
     // Every exit decision is taken by all four warps together (an AND over
     // the named barrier), so that no warp waits at a barrier another left.
     bool ok = true;
-    for (int t = 0; t < ntiles; ++t) {
-      bool got = ok && attn_wait(s_full, (uint32_t)t & 1u, p.err, s_abort);
-      got = __all_sync(0xffffffffu, got);
-      uint32_t sr[N];
-#pragma unroll
-      for (int m = 0; m < N; ++m) sr[m] = 0u;
-      if (got) {
-        tc_fence_after();
-        tmem_ld_x16(trow, *reinterpret_cast<uint32_t(*)[16]>(&sr[0]));
-        if constexpr (N == 32) tmem_ld_x16(trow + 16u, *reinterpret_cast<uint32_t(*)[16]>(&sr[16]));
-        tc_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(s_free);
+    int T = 0;  // tiles
+    for (int it = blockIdx.x; it < nitems && ok; it += gridDim.x) {
+      const Item I = item_of(it);
+      named_barrier(1, 128);  // the previous item's readers of lim_s / orow_s are done
+      // per query row: the positions of this split it sees (counted from j0)
+      // and its o / lse row (-1: a padded row)
+      if (ts < N) {
+        const int m = ts, i = m / p.G, h = I.g * p.G + (m - i * p.G);
+        int lim = 0;
+        long long row = -1;
+        if (m < qG && h < p.H) {
+          lim = min(I.jend, I.Lb - (p.q - 1 - i)) - I.j0;
+          row = ((long long)I.r * S + (I.b * p.q + i)) * p.H + h;
+        }
+        lim_s[m] = lim < 0 ? 0 : lim;
+        orow_s[m] = row;
       }
-      // scores in log2 units, masked; the tile's column max over 128 positions
-      const int jr = t * kAttnTile + pos;
-      float sc[N];
-      float *rd = red + (t & 1) * 4 * N;
-#pragma unroll
-      for (int m = 0; m < N; ++m) {
-        sc[m] = (jr < lim_s[m]) ? __uint_as_float(sr[m]) * p.scale_log2 : kNegInf;
-        float mx = sc[m];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        if (lane == (m & 31)) rd[sw * N + m] = mx;
-      }
-      ok = named_barrier_and(1, 128, got);
-      if (!ok) break;
-      float alpha[N];
-      bool moved = false;
-#pragma unroll
-      for (int m = 0; m < N; ++m) {
-        const float tmax = fmaxf(fmaxf(rd[m], rd[N + m]), fmaxf(rd[2 * N + m], rd[3 * N + m]));
-        const float mn = fmaxf(m_run[m], tmax);
-        alpha[m] = (mn == kNegInf) ? 1.0f : ex2_approx(m_run[m] - mn);
-        moved |= alpha[m] != 1.0f;
-        m_run[m] = mn;
-        sc[m] = (sc[m] == kNegInf) ? 0.0f : ex2_approx(sc[m] - mn);  // P
-        l_part[m] = __fmaf_rn(l_part[m], alpha[m], sc[m]);
-      }
-      // the previous tile's O^T MMAs are done before P and O are touched (a
-      // failed wait is shared at the next tile's barrier or after the loop)
-      if (t > 0) {
-        ok = attn_wait(o_full, (uint32_t)(t - 1) & 1u, p.err, s_abort);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) continue;
-        tc_fence_after();
-      }
-      // P^T row m, column pos (K-major, 128-byte swizzle, K blocks of 64 positions)
-      {
-        uint8_t *pb = gbase + L::p_off + (pos >> 6) * (N * 128);
-        const int x2 = (pos & 63) * 2;
+      named_barrier(1, 128);
+      if (I.ntiles == 0) {  // the split holds no position: lse -inf, o 0
+        if (ts < N && orow_s[ts] >= 0) p.lse[orow_s[ts]] = kNegInf;
 #pragma unroll
         for (int m = 0; m < N; ++m) {
-          const __nv_bfloat16 v = __float2bfloat16_rn(sc[m]);
-          *reinterpret_cast<__nv_bfloat16 *>(pb + m * 128 + (((x2 >> 4) ^ (m & 7)) << 4) + (x2 & 15)) = v;
+          const long long row = orow_s[m];
+          if (row >= 0)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) p.o[row * kD + 128 * c + pos] = 0;
         }
+        continue;
       }
-      // a cached row past kv_len (inside the cache tensor) may hold anything:
-      // its latent is zeroed so that 0 * it stays 0 in O
-      if (j0 + jr >= Lb && j0 + jr < p.Lmax) {
+      float m_run[N], l_part[N];  // running column max (log2 units), this position's share of the sums
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint8_t *row = gbase + L::dbl_off + (size_t)((4 * t + c) % kAttnDbl) * kDblBytes + pos * 128;
+      for (int m = 0; m < N; ++m) {
+        m_run[m] = kNegInf;
+        l_part[m] = 0.0f;
+      }
+      for (int t = 0; t < I.ntiles; ++t, ++T) {
+        bool got = ok && attn_wait(s_full, (uint32_t)T & 1u, p.err, s_abort);
+        got = __all_sync(0xffffffffu, got);
+        uint32_t sr[N];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            reinterpret_cast<uint4 *>(row)[k] = make_uint4(0u, 0u, 0u, 0u);
-            reinterpret_cast<uint4 *>(row + kDblBytes / 2)[k] = make_uint4(0u, 0u, 0u, 0u);
+        for (int m = 0; m < N; ++m) sr[m] = 0u;
+        if (got) {
+          tc_fence_after();
+          tmem_ld_x16(trow, *reinterpret_cast<uint32_t(*)[16]>(&sr[0]));
+          if constexpr (N == 32) tmem_ld_x16(trow + 16u, *reinterpret_cast<uint32_t(*)[16]>(&sr[16]));
+          tc_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(s_free);
+        }
+        // scores in log2 units, masked; the tile's column max over 128 positions
+        const int jr = t * kAttnTile + pos;
+        float sc[N];
+        float *rd = red + (T & 1) * 4 * N;
+#pragma unroll
+        for (int m = 0; m < N; ++m) {
+          sc[m] = (jr < lim_s[m]) ? __uint_as_float(sr[m]) * p.scale_log2 : kNegInf;
+          float mx = sc[m];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          if (lane == (m & 31)) rd[sw * N + m] = mx;
+        }
+        ok = named_barrier_and(1, 128, got);
+        if (!ok) break;
+        float alpha[N];
+        bool moved = false;
+#pragma unroll
+        for (int m = 0; m < N; ++m) {
+          const float tmax = fmaxf(fmaxf(rd[m], rd[N + m]), fmaxf(rd[2 * N + m], rd[3 * N + m]));
+          const float mn = fmaxf(m_run[m], tmax);
+          alpha[m] = (mn == kNegInf) ? 1.0f : ex2_approx(m_run[m] - mn);
+          moved |= alpha[m] != 1.0f;
+          m_run[m] = mn;
+          sc[m] = (sc[m] == kNegInf) ? 0.0f : ex2_approx(sc[m] - mn);  // P
+          l_part[m] = __fmaf_rn(l_part[m], alpha[m], sc[m]);
+        }
+        // the previous tile's O^T MMAs are done before P and O are touched (a
+        // failed wait is shared at the next barrier)
+        if (T > 0) {
+          ok = attn_wait(o_full, (uint32_t)(T - 1) & 1u, p.err, s_abort);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) continue;
+          tc_fence_after();
+        }
+        // P^T row m, column pos (K-major, 128-byte swizzle, K blocks of 64 positions)
+        {
+          uint8_t *pb = gbase + L::p_off + (pos >> 6) * (N * 128);
+          const int x2 = (pos & 63) * 2;
+#pragma unroll
+          for (int m = 0; m < N; ++m) {
+            const __nv_bfloat16 v = __float2bfloat16_rn(sc[m]);
+            *reinterpret_cast<__nv_bfloat16 *>(pb + m * 128 + (((x2 >> 4) ^ (m & 7)) << 4) + (x2 & 15)) = v;
           }
         }
-      }
-      // a column whose max moved: its accumulated O^T scaled by alpha
-      if (t > 0 && moved) {
+        // a cached row past kv_len (inside the cache tensor) may hold anything:
+        // its latent is zeroed so that 0 * it stays 0 in O
+        if (I.j0 + jr >= I.Lb && I.j0 + jr < p.Lmax) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 4; ++c) {
+            uint8_t *rowp = gbase + L::dbl_off + (size_t)((4 * T + c) % kAttnDbl) * kDblBytes + pos * 128;
 #pragma unroll
-          for (int hh = 0; hh < N / 16; ++hh) {
-            const uint32_t ta = trow + (uint32_t)(N + c * N + 16 * hh);
-            uint32_t ov[16];
-            tmem_ld_x16(ta, ov);
-            tc_wait_ld();
-#pragma unroll
-            for (int x = 0; x < 16; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * alpha[16 * hh + x]);
-            tmem_st_x16(ta, ov);
+            for (int k = 0; k < 8; ++k) {
+              reinterpret_cast<uint4 *>(rowp)[k] = make_uint4(0u, 0u, 0u, 0u);
+              reinterpret_cast<uint4 *>(rowp + kDblBytes / 2)[k] = make_uint4(0u, 0u, 0u, 0u);
+            }
           }
         }
-        tc_wait_st();
+        // a column whose max moved: its accumulated O^T scaled by alpha
+        if (t > 0 && moved) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+#pragma unroll
+            for (int hh = 0; hh < N / 16; ++hh) {
+              const uint32_t ta = trow + (uint32_t)(N + c * N + 16 * hh);
+              uint32_t ov[16];
+              tmem_ld_x16(ta, ov);
+              tc_wait_ld();
+#pragma unroll
+              for (int x = 0; x < 16; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * alpha[16 * hh + x]);
+              tmem_st_x16(ta, ov);
+            }
+          }
+          tc_wait_st();
+        }
+        tc_fence_before();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
       }
-      tc_fence_before();
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
-    }
-    if (ok && ntiles > 0) {
-      ok = attn_wait(o_full, (uint32_t)(ntiles - 1) & 1u, p.err, s_abort);
-      ok = __all_sync(0xffffffffu, ok);
-      if (ok) tc_fence_after();
-    }
-    // the next kernel on the stream may start its prologue
-    grid_launch_dependents();
-    // column sums over the 128 positions (fixed order), then o and lse
-    long long *orow_s = reinterpret_cast<long long *>(gbase + L::row_off);
-    {
-      float *rd = red + (ntiles & 1) * 4 * N;
+      if (!ok) {  // left the tile loop early (or a late wait failed): shared, then stop
+        named_barrier_and(1, 128, false);
+        break;
+      }
+      // the item's last O^T MMAs, then the column sums over the positions (fixed order)
+      bool fin = attn_wait(o_full, (uint32_t)(T - 1) & 1u, p.err, s_abort);
+      fin = __all_sync(0xffffffffu, fin);
+      if (fin) tc_fence_after();
+      float *rd = red + (T & 1) * 4 * N;
 #pragma unroll
       for (int m = 0; m < N; ++m) {
         float l = l_part[m];
@@ -403,37 +467,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
         if (lane == (m & 31)) rd[sw * N + m] = l;
       }
-      ok = named_barrier_and(1, 128, ok);  // one decision for all four warps
-      constexpr float kLn2 = 0.6931471805599453f;
-      float inv[N];  // 1 / column sum; 0 where the row sees nothing (or after an abort)
+      ok = named_barrier_and(1, 128, fin);
+      if (!ok) break;
+      float inv[N];  // 1 / column sum; 0 where the row sees nothing
 #pragma unroll
       for (int m = 0; m < N; ++m) {
         const float l = (rd[m] + rd[N + m]) + (rd[2 * N + m] + rd[3 * N + m]);
-        const bool live = ok && l > 0.0f;
-        inv[m] = live ? __frcp_rn(l) : 0.0f;
-        if (m == ts) {
-          const int i = m / p.G, h = g * p.G + (m - i * p.G);
-          long long row = -1;
-          if (m < qG && h < p.H) {
-            row = ((long long)r * S + (b * p.q + i)) * p.H + h;
-            p.lse[row] = live ? (m_run[m] + lg2_approx(l)) * kLn2 : kNegInf;
-          }
-          orow_s[m] = row;
-        }
+        inv[m] = l > 0.0f ? __frcp_rn(l) : 0.0f;
+        if (m == ts && orow_s[m] >= 0) p.lse[orow_s[m]] = l > 0.0f ? (m_run[m] + lg2_approx(l)) * kLn2 : kNegInf;
       }
-      named_barrier(1, 128);
       // o[row][128 c + pos] for every query row: a warp writes 64 contiguous bytes
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t ov[N];
-        if (ntiles > 0 && ok) {
-          tmem_ld_x16(trow + (uint32_t)(N + c * N), *reinterpret_cast<uint32_t(*)[16]>(&ov[0]));
-          if constexpr (N == 32) tmem_ld_x16(trow + (uint32_t)(N + c * N + 16), *reinterpret_cast<uint32_t(*)[16]>(&ov[16]));
-          tc_wait_ld();
-        } else {
-#pragma unroll
-          for (int m = 0; m < N; ++m) ov[m] = 0u;
-        }
+        tmem_ld_x16(trow + (uint32_t)(N + c * N), *reinterpret_cast<uint32_t(*)[16]>(&ov[0]));
+        if constexpr (N == 32) tmem_ld_x16(trow + (uint32_t)(N + c * N + 16), *reinterpret_cast<uint32_t(*)[16]>(&ov[16]));
+        tc_wait_ld();
 #pragma unroll
         for (int m = 0; m < N; ++m) {
           const long long row = orow_s[m];
@@ -444,7 +493,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
         }
       }
+      tc_fence_before();
     }
+    // the next kernel on the stream may start its prologue
+    grid_launch_dependents();
   }
   tc_fence_before();
   __syncthreads();
@@ -480,13 +532,15 @@ static cudaError_t launch_attn_n(const AttnParams &p, const CUtensorMap &map, un
   return cudaGetLastError();
 }
 
-cudaError_t launch_attn(const AttnParams &p, const CUtensorMap &map, cudaStream_t stream) {
-  const long long grid = (long long)p.B * p.spr * p.groups;
-  if (grid <= 0 || grid >= (1LL << 31)) return cudaErrorInvalidValue;
+// Persistent: one CTA per SM (the shared-memory plan fills an SM), at most
+// one per work item.
+cudaError_t launch_attn(const AttnParams &p, const CUtensorMap &map, int num_sms, cudaStream_t stream) {
+  const long long items = (long long)p.B * p.spr * p.groups;
+  if (items <= 0 || items >= (1LL << 31) || num_sms < 1) return cudaErrorInvalidValue;
+  const unsigned grid = (unsigned)(items < num_sms ? items : num_sms);
   const int rows = ((p.q * p.G + 15) / 16) * 16;  // the host keeps q G <= 32
   if (rows > 32) return cudaErrorInvalidValue;
-  return rows <= 16 ? launch_attn_n<16>(p, map, (unsigned)grid, stream)
-                    : launch_attn_n<32>(p, map, (unsigned)grid, stream);
+  return rows <= 16 ? launch_attn_n<16>(p, map, grid, stream) : launch_attn_n<32>(p, map, grid, stream);
 }
 
 }  // namespace mla

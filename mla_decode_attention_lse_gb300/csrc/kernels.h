@@ -40,6 +40,6 @@ cudaError_t launch_pack(const PackParams &p, int grid, cudaStream_t stream);
 int attn_heads_per_cta(int q, int H);  // G
 int attn_rows(int q, int H);           // the MMA's N: q * G rounded up to 16
 size_t attn_smem_bytes(int rows);
-cudaError_t launch_attn(const AttnParams &p, const CUtensorMap &map, cudaStream_t stream);
+cudaError_t launch_attn(const AttnParams &p, const CUtensorMap &map, int num_sms, cudaStream_t stream);
 
 }  // namespace mla
