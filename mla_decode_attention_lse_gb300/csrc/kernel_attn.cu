@@ -44,7 +44,8 @@ namespace {
 constexpr int kAttnK = kD + 64;     // query / cached row width (576)
 constexpr int kAttnTile = 128;      // positions per tile (MMA M of S^T)
 constexpr int kAttnDbl = 5;         // double-block slots (a tile needs 4)
-constexpr int kAttnThreads = 224;   // warp 0 TMA, warp 1 MMA, warps 2..5 softmax, warp 6 queries
+constexpr int kAttnSmx = 8;         // softmax warps: two per TMEM lane quadrant, half the query rows each
+constexpr int kAttnThreads = (3 + kAttnSmx) * 32;  // warp 0 TMA, warp 1 MMA, softmax warps, one query warp
 constexpr uint32_t kDblBytes = 2u * kAttnTile * 128u;  // 32 KiB
 constexpr uint32_t kRopeBytes = kAttnTile * 128u;      // 16 KiB
 
@@ -106,8 +107,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   auto full_r = [&](int s) { return bar0 + 8u * (uint32_t)(2 * kAttnDbl + s); };
   auto empty_r = [&](int s) { return bar0 + 8u * (uint32_t)(2 * kAttnDbl + NR + s); };
   const uint32_t s_full = bar0 + 8u * (uint32_t)(2 * kAttnDbl + 2 * NR);  // S^T of a tile is in TMEM
-  const uint32_t s_free = s_full + 8u;   // the softmax warps have read it (4 arrivals)
-  const uint32_t p_full = s_full + 16u;  // P^T written, O rescaled (4 arrivals)
+  const uint32_t s_free = s_full + 8u;   // the softmax warps have read it (one arrival per warp)
+  const uint32_t p_full = s_full + 16u;  // P^T written, O rescaled (one arrival per softmax warp)
   const uint32_t o_full = s_full + 24u;  // a tile's O^T MMAs are complete
   const uint32_t q_full = s_full + 32u;  // an item's query rows are in shared memory
   const uint32_t q_free = s_full + 40u;  // the item's last S^T MMAs are done: Q may be replaced
@@ -123,8 +124,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(empty_r(s), 1u);
     }
     mbar_init(s_full, 1u);
-    mbar_init(s_free, 4u);
-    mbar_init(p_full, 4u);
+    mbar_init(s_free, (uint32_t)kAttnSmx);
+    mbar_init(p_full, (uint32_t)kAttnSmx);
     mbar_init(o_full, 1u);
     mbar_init(q_full, 1u);
     mbar_init(q_free, 1u);
@@ -267,9 +268,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
               tc_mma_f16(tO + (uint32_t)(c * N), smem_desc_mn_sw128(vbase + (uint32_t)ks * 2048u, kDblBytes / 2),
                          desc_sw128_at(dP, ((uint32_t)ks >> 2) * (N * 128u) + ((uint32_t)ks & 3u) * 32u), kIdO,
                          (t | ks) ? 1u : 0u);
+            tc_commit(empty_db((4 * T + c) % kAttnDbl));  // this latent chunk's slot is free once its MMAs are
           }
           tc_commit(o_full);
-          for (int c = 0; c < 4; ++c) tc_commit(empty_db((4 * T + c) % kAttnDbl));
           last_o = T;
         }
         ++kq;
@@ -279,7 +280,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (last_o >= 0) mbar_wait(o_full, (uint32_t)last_o & 1u, p.err, kErrWaitTeardown);
       if (last_q >= 0) mbar_wait(q_free, (uint32_t)last_q & 1u, p.err, kErrWaitTeardown);
     }
-  } else if (warp == 6) {
+  } else if (warp == 2 + kAttnSmx) {
     // ---- query loader: an item's N rows (row m: token m / G, head g G + m % G;
     // padded rows zero) into the K-major swizzled Q tile, by cp.async ----
     bool ok = true;
@@ -309,23 +310,29 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       ++kq;
     }
   } else {
-    // ---- softmax warps 2..5: TMEM lane quadrant warp % 4, one position each ----
-    const int sw = warp - 2;          // 0..3: slot in the cross-warp reductions
-    const int qd = warp & 3;          // TMEM lane quadrant
-    const int pos = qd * 32 + lane;   // position within a tile; O^T row within a latent chunk
-    const int ts = threadIdx.x - 64;  // 0..127
+    // ---- softmax warps 2 .. 2 + kAttnSmx - 1: TMEM lane quadrant warp % 4 (a
+    // thread per position), query rows c0 .. c0 + NC - 1 of the N ----
+    constexpr int NC = N / 2;                     // query rows per softmax warp
+    constexpr uint32_t kSmxThreads = kAttnSmx * 32;
+    const int qd = warp & 3;                      // TMEM lane quadrant
+    const int c0 = ((warp - 2) >> 2) * NC;        // this warp's first query row
+    const int pos = qd * 32 + lane;               // position within a tile; O^T row within a latent chunk
+    const int ts = threadIdx.x - 64;              // 0 .. kSmxThreads - 1
     const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);
     const int qG = p.q * p.G;
     const int S = p.B * p.q;
     const float kNegInf = __int_as_float(0xFF800000);
     constexpr float kLn2 = 0.6931471805599453f;
-    // Every exit decision is taken by all four warps together (an AND over
+    // a column's reference max moves only when a tile's max exceeds it by more
+    // than 2^8 (the weights then stay below 256): O is rescaled rarely
+    constexpr float kSlack = 8.0f;
+    // Every exit decision is taken by all softmax warps together (an AND over
     // the named barrier), so that no warp waits at a barrier another left.
     bool ok = true;
     int T = 0;  // tiles
     for (int it = blockIdx.x; it < nitems && ok; it += gridDim.x) {
       const Item I = item_of(it);
-      named_barrier(1, 128);  // the previous item's readers of lim_s / orow_s are done
+      named_barrier(1, kSmxThreads);  // the previous item's readers of lim_s / orow_s are done
       // per query row: the positions of this split it sees (counted from j0)
       // and its o / lse row (-1: a padded row)
       if (ts < N) {
@@ -339,34 +346,38 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         lim_s[m] = lim < 0 ? 0 : lim;
         orow_s[m] = row;
       }
-      named_barrier(1, 128);
+      named_barrier(1, kSmxThreads);
       if (I.ntiles == 0) {  // the split holds no position: lse -inf, o 0
         if (ts < N && orow_s[ts] >= 0) p.lse[orow_s[ts]] = kNegInf;
 #pragma unroll
-        for (int m = 0; m < N; ++m) {
-          const long long row = orow_s[m];
+        for (int x = 0; x < NC; ++x) {
+          const long long row = orow_s[c0 + x];
           if (row >= 0)
 #pragma unroll
             for (int c = 0; c < 4; ++c) p.o[row * kD + 128 * c + pos] = 0;
         }
         continue;
       }
-      float m_run[N], l_part[N];  // running column max (log2 units), this position's share of the sums
+      int lim[NC];
+      float m_ref[NC], l_part[NC];  // reference max (log2 units), this position's share of the sums
 #pragma unroll
-      for (int m = 0; m < N; ++m) {
-        m_run[m] = kNegInf;
-        l_part[m] = 0.0f;
+      for (int x = 0; x < NC; ++x) {
+        lim[x] = lim_s[c0 + x];
+        m_ref[x] = kNegInf;
+        l_part[x] = 0.0f;
       }
       for (int t = 0; t < I.ntiles; ++t, ++T) {
         bool got = ok && attn_wait(s_full, (uint32_t)T & 1u, p.err, s_abort);
         got = __all_sync(0xffffffffu, got);
-        uint32_t sr[N];
+        uint32_t sr[NC];
 #pragma unroll
-        for (int m = 0; m < N; ++m) sr[m] = 0u;
+        for (int x = 0; x < NC; ++x) sr[x] = 0u;
         if (got) {
           tc_fence_after();
-          tmem_ld_x16(trow, *reinterpret_cast<uint32_t(*)[16]>(&sr[0]));
-          if constexpr (N == 32) tmem_ld_x16(trow + 16u, *reinterpret_cast<uint32_t(*)[16]>(&sr[16]));
+          if constexpr (NC == 16)
+            tmem_ld_x16(trow + (uint32_t)c0, *reinterpret_cast<uint32_t(*)[16]>(&sr[0]));
+          else
+            tmem_ld_x8(trow + (uint32_t)c0, *reinterpret_cast<uint32_t(*)[8]>(&sr[0]));
           tc_wait_ld();
           tc_fence_before();
           __syncwarp();
@@ -374,30 +385,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         // scores in log2 units, masked; the tile's column max over 128 positions
         const int jr = t * kAttnTile + pos;
-        float sc[N];
+        float sc[NC];
         float *rd = red + (T & 1) * 4 * N;
 #pragma unroll
-        for (int m = 0; m < N; ++m) {
-          sc[m] = (jr < lim_s[m]) ? __uint_as_float(sr[m]) * p.scale_log2 : kNegInf;
-          float mx = sc[m];
+        for (int x = 0; x < NC; ++x) {
+          sc[x] = (jr < lim[x]) ? __uint_as_float(sr[x]) * p.scale_log2 : kNegInf;
+          float mx = sc[x];
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-          if (lane == (m & 31)) rd[sw * N + m] = mx;
+          if (lane == x) rd[qd * N + c0 + x] = mx;
         }
-        ok = named_barrier_and(1, 128, got);
+        ok = named_barrier_and(1, kSmxThreads, got);
         if (!ok) break;
-        float alpha[N];
+        float alpha[NC];
         bool moved = false;
 #pragma unroll
-        for (int m = 0; m < N; ++m) {
+        for (int x = 0; x < NC; ++x) {
+          const int m = c0 + x;
           const float tmax = fmaxf(fmaxf(rd[m], rd[N + m]), fmaxf(rd[2 * N + m], rd[3 * N + m]));
-          const float mn = fmaxf(m_run[m], tmax);
-          alpha[m] = (mn == kNegInf) ? 1.0f : ex2_approx(m_run[m] - mn);
-          moved |= alpha[m] != 1.0f;
-          m_run[m] = mn;
-          sc[m] = (sc[m] == kNegInf) ? 0.0f : ex2_approx(sc[m] - mn);  // P
-          l_part[m] = __fmaf_rn(l_part[m], alpha[m], sc[m]);
+          const float mn = (tmax > m_ref[x] + kSlack) ? tmax : m_ref[x];
+          alpha[x] = (mn == m_ref[x]) ? 1.0f : ex2_approx(m_ref[x] - mn);  // 0 when m_ref was -inf
+          moved |= (alpha[x] != 1.0f) && (m_ref[x] != kNegInf);
+          m_ref[x] = mn;
+          sc[x] = (sc[x] == kNegInf) ? 0.0f : ex2_approx(sc[x] - mn);  // P
+          l_part[x] = __fmaf_rn(l_part[x], alpha[x], sc[x]);
         }
+        moved = __any_sync(0xffffffffu, moved);
         // the previous tile's O^T MMAs are done before P and O are touched (a
         // failed wait is shared at the next barrier)
         if (T > 0) {
@@ -411,14 +424,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           uint8_t *pb = gbase + L::p_off + (pos >> 6) * (N * 128);
           const int x2 = (pos & 63) * 2;
 #pragma unroll
-          for (int m = 0; m < N; ++m) {
-            const __nv_bfloat16 v = __float2bfloat16_rn(sc[m]);
+          for (int x = 0; x < NC; ++x) {
+            const int m = c0 + x;
+            const __nv_bfloat16 v = __float2bfloat16_rn(sc[x]);
             *reinterpret_cast<__nv_bfloat16 *>(pb + m * 128 + (((x2 >> 4) ^ (m & 7)) << 4) + (x2 & 15)) = v;
           }
         }
         // a cached row past kv_len (inside the cache tensor) may hold anything:
-        // its latent is zeroed so that 0 * it stays 0 in O
-        if (I.j0 + jr >= I.Lb && I.j0 + jr < p.Lmax) {
+        // its latent is zeroed (by one warp of the quadrant) so that 0 * it
+        // stays 0 in O
+        if (c0 == 0 && I.j0 + jr >= I.Lb && I.j0 + jr < p.Lmax) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint8_t *rowp = gbase + L::dbl_off + (size_t)((4 * T + c) % kAttnDbl) * kDblBytes + pos * 128;
@@ -429,20 +444,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
           }
         }
-        // a column whose max moved: its accumulated O^T scaled by alpha
+        // a column whose reference max moved: its accumulated O^T scaled by alpha
         if (t > 0 && moved) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
+            const uint32_t ta = trow + (uint32_t)(N + c * N + c0);
+            uint32_t ov[NC];
+            if constexpr (NC == 16)
+              tmem_ld_x16(ta, *reinterpret_cast<uint32_t(*)[16]>(&ov[0]));
+            else
+              tmem_ld_x8(ta, *reinterpret_cast<uint32_t(*)[8]>(&ov[0]));
+            tc_wait_ld();
 #pragma unroll
-            for (int hh = 0; hh < N / 16; ++hh) {
-              const uint32_t ta = trow + (uint32_t)(N + c * N + 16 * hh);
-              uint32_t ov[16];
-              tmem_ld_x16(ta, ov);
-              tc_wait_ld();
-#pragma unroll
-              for (int x = 0; x < 16; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * alpha[16 * hh + x]);
-              tmem_st_x16(ta, ov);
-            }
+            for (int x = 0; x < NC; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * alpha[x]);
+            if constexpr (NC == 16)
+              tmem_st_x16(ta, *reinterpret_cast<uint32_t(*)[16]>(&ov[0]));
+            else
+              tmem_st_x8(ta, *reinterpret_cast<uint32_t(*)[8]>(&ov[0]));
           }
           tc_wait_st();
         }
@@ -452,7 +470,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (lane == 0) mbar_arrive(p_full);
       }
       if (!ok) {  // left the tile loop early (or a late wait failed): shared, then stop
-        named_barrier_and(1, 128, false);
+        named_barrier_and(1, kSmxThreads, false);
         break;
       }
       // the item's last O^T MMAs, then the column sums over the positions (fixed order)
@@ -461,33 +479,38 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (fin) tc_fence_after();
       float *rd = red + (T & 1) * 4 * N;
 #pragma unroll
-      for (int m = 0; m < N; ++m) {
-        float l = l_part[m];
+      for (int x = 0; x < NC; ++x) {
+        float l = l_part[x];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-        if (lane == (m & 31)) rd[sw * N + m] = l;
+        if (lane == x) rd[qd * N + c0 + x] = l;
       }
-      ok = named_barrier_and(1, 128, fin);
+      ok = named_barrier_and(1, kSmxThreads, fin);
       if (!ok) break;
-      float inv[N];  // 1 / column sum; 0 where the row sees nothing
+      float inv[NC];  // 1 / column sum; 0 where the row sees nothing
 #pragma unroll
-      for (int m = 0; m < N; ++m) {
+      for (int x = 0; x < NC; ++x) {
+        const int m = c0 + x;
         const float l = (rd[m] + rd[N + m]) + (rd[2 * N + m] + rd[3 * N + m]);
-        inv[m] = l > 0.0f ? __frcp_rn(l) : 0.0f;
-        if (m == ts && orow_s[m] >= 0) p.lse[orow_s[m]] = l > 0.0f ? (m_run[m] + lg2_approx(l)) * kLn2 : kNegInf;
+        inv[x] = l > 0.0f ? __frcp_rn(l) : 0.0f;
+        if (qd == 0 && lane == x && orow_s[m] >= 0)
+          p.lse[orow_s[m]] = l > 0.0f ? (m_ref[x] + lg2_approx(l)) * kLn2 : kNegInf;
       }
-      // o[row][128 c + pos] for every query row: a warp writes 64 contiguous bytes
+      // o[row][128 c + pos] for this warp's query rows: a warp writes 64 contiguous bytes
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t ov[N];
-        tmem_ld_x16(trow + (uint32_t)(N + c * N), *reinterpret_cast<uint32_t(*)[16]>(&ov[0]));
-        if constexpr (N == 32) tmem_ld_x16(trow + (uint32_t)(N + c * N + 16), *reinterpret_cast<uint32_t(*)[16]>(&ov[16]));
+        uint32_t ov[NC];
+        const uint32_t ta = trow + (uint32_t)(N + c * N + c0);
+        if constexpr (NC == 16)
+          tmem_ld_x16(ta, *reinterpret_cast<uint32_t(*)[16]>(&ov[0]));
+        else
+          tmem_ld_x8(ta, *reinterpret_cast<uint32_t(*)[8]>(&ov[0]));
         tc_wait_ld();
 #pragma unroll
-        for (int m = 0; m < N; ++m) {
-          const long long row = orow_s[m];
+        for (int x = 0; x < NC; ++x) {
+          const long long row = orow_s[c0 + x];
           if (row >= 0) {
-            const float v = (inv[m] != 0.0f) ? __uint_as_float(ov[m]) * inv[m] : 0.0f;
+            const float v = (inv[x] != 0.0f) ? __uint_as_float(ov[x]) * inv[x] : 0.0f;
             const __nv_bfloat16 hv = __float2bfloat16_rn(v);
             p.o[row * kD + 128 * c + pos] = *reinterpret_cast<const uint16_t *>(&hv);
           }
