@@ -176,3 +176,22 @@ def test_attn_errors(lib):
     with pytest.raises(m.MlaError) as e:
         m.mla_attn_split_kv(inp["qv"], odd, inp["kv_len"], 1, 2, 0.1, o, lse)
     assert e.value.status == m.MLA_ERR_ALIGN
+
+
+@pytest.mark.parametrize("case", range(16))
+def test_attn_fuzz(lib, orc, case):
+    # seeded random shapes: queries per request, heads (one or several head
+    # groups), splits, lengths (empty, short, tile edges, long), strided views
+    rng = np.random.default_rng(3000 + case)
+    q = int(rng.choice([1, 1, 2, 3, 4, 8]))
+    H = int(rng.integers(1, 25))
+    B = int(rng.integers(1, 6))
+    spr = int(rng.choice([1, 2, 3, 5, 16, 20]))
+    Lmax = int(rng.choice([16, 64, 129, 300, 700]))
+    lens = [int(rng.choice([0, 1, q, int(rng.integers(1, Lmax + 1)), Lmax])) for _ in range(B)]
+    lens = [min(L, Lmax) for L in lens]
+    inp = problem(B, q, H, spr, Lmax, lens, seed=case, kv_pad=int(rng.choice([0, 8, 64])),
+                  q_pad=int(rng.choice([0, 1])))
+    o, lse = run_attn(inp)
+    o_ref, lse_ref = oracle(orc, inp)
+    check(o, lse, o_ref, lse_ref, f"fuzz {case}: B={B} q={q} H={H} spr={spr} Lmax={Lmax} lens={lens}")
