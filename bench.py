@@ -46,10 +46,20 @@ def load_peaks():
     return 6800.0, "fallback"
 
 
-def kernel_source_hash() -> str:
+# the source file of each kernel named in a bench line; the shared headers
+# (device helpers, parameter structs, launch declarations) count for every one
+KERNEL_FILES = {"tc": "kernel_tc.cu", "tc_ksplit_cluster4": "kernel_ks.cu", "simt": "kernel_simt.cu",
+                "dcp_pack": "kernel_pack.cu", "attn_split_kv": "kernel_attn.cu"}
+SHARED_SOURCES = ("device_common.cuh", "kernels.h", "kparams.h")
+
+
+def kernel_source_hash(kernel: str | None = None) -> str:
+    """Hash of the sources a kernel is built from (all of csrc/ when no kernel
+    is named)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_decode_attention_lse_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    files = sorted(os.listdir(csrc)) if kernel is None else sorted(SHARED_SOURCES + (KERNEL_FILES[kernel],))
+    for f in files:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode())
             h.update(fh.read())
@@ -65,7 +75,7 @@ def traffic_from_profile(workload: str, kernel: str):
     with open(p) as f:
         d = json.load(f)
     e = d.get(f"{workload}/{kernel}")
-    if not e or e.get("source_hash") != kernel_source_hash():
+    if not e or kernel not in KERNEL_FILES or e.get("source_hash") != kernel_source_hash(kernel):
         return None
     return e.get("dram_bytes_per_launch")
 
