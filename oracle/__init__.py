@@ -77,6 +77,14 @@ class _AttnArgs(ctypes.Structure):
     ]
 
 
+class _OprojArgs(ctypes.Structure):
+    _fields_ = [
+        ("S", ctypes.c_int), ("K", ctypes.c_int), ("Nout", ctypes.c_int),
+        ("x", ctypes.c_void_p), ("x_st", ctypes.c_int64),
+        ("w", ctypes.c_void_p), ("w_sj", ctypes.c_int64),
+    ]
+
+
 def lib():
     global _lib
     with _lock:
@@ -115,6 +123,8 @@ def lib():
             L.orc_dcp_pack.argtypes = [P(_PackArgs), ctypes.c_void_p, ctypes.c_void_p]
             L.orc_mla_attn_split.restype = ctypes.c_int
             L.orc_mla_attn_split.argtypes = [P(_AttnArgs), ctypes.c_void_p, ctypes.c_void_p]
+            L.orc_o_proj.restype = ctypes.c_int
+            L.orc_o_proj.argtypes = [P(_OprojArgs), ctypes.c_void_p]
             _lib = L
     return _lib
 
@@ -248,6 +258,26 @@ def mla_attn_split(qv, kv, kv_len, q, spr, scale):
     if lib().orc_mla_attn_split(ctypes.byref(a), _ptr(o), _ptr(lse)) != 0:
         raise ValueError("oracle rejected the attention problem")
     return o, lse
+
+
+def o_proj(x, w):
+    """This rank's o_proj shard in double: out[t][j] = sum_k x[t][k] w[j][k].
+
+    x uint16 [S, K] (bf16 bits, unit-stride rows), w uint16 [Nout, K].
+    Returns out uint16 [S, Nout] (bf16 bits).
+    """
+    S, K = x.shape
+    Nout, K2 = w.shape
+    assert K == K2 and x.dtype == np.uint16 and w.dtype == np.uint16
+    assert x.strides[1] == 2 and w.strides[1] == 2
+    a = _OprojArgs()
+    a.S, a.K, a.Nout = S, K, Nout
+    a.x, a.x_st = _ptr(x), x.strides[0] // 2
+    a.w, a.w_sj = _ptr(w), w.strides[0] // 2
+    out = np.empty((S, Nout), np.uint16)
+    if lib().orc_o_proj(ctypes.byref(a), _ptr(out)) != 0:
+        raise ValueError("oracle rejected the o_proj problem")
+    return out
 
 
 # ---- scalar helpers for the pins ----------------------------------------

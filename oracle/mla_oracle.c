@@ -394,3 +394,25 @@ int orc_mla_attn_split(const orc_attn_args *a, uint16_t *o, float *lse) {
   }
   return 0;
 }
+
+/* ---- downstream: the o_proj shard of this rank ---------------------------
+ *
+ * The page's stage ends at "o_proj's input" (core).  o_proj is a row-parallel
+ * linear layer: this rank's shard multiplies its core row (H*128 wide) by its
+ * slice of the weight, out[t][j] = sum_k core[t][k] * W[j][k] (W stored
+ * [hidden, H*128] as a linear layer's weight), and the ranks' outputs are
+ * summed by the tensor-parallel all-reduce (multi-GPU, not here).  Computed in
+ * double, k ascending; out rounded to fp32 then to bf16. */
+int orc_o_proj(const orc_oproj_args *a, uint16_t *out) {
+  if (a->S < 0 || a->K < 1 || a->Nout < 1) return -1;
+  for (int t = 0; t < a->S; ++t) {
+    const uint16_t *x = a->x + (int64_t)t * a->x_st;
+    for (int j = 0; j < a->Nout; ++j) {
+      const uint16_t *w = a->w + (int64_t)j * a->w_sj;
+      double acc = 0.0;
+      for (int k = 0; k < a->K; ++k) acc += (double)orc_bf16_to_f32(x[k]) * (double)orc_bf16_to_f32(w[k]);
+      out[(int64_t)t * a->Nout + j] = orc_f32_to_bf16((float)acc);
+    }
+  }
+  return 0;
+}

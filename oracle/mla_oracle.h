@@ -75,4 +75,15 @@ typedef struct {
  * at [r, t, h]).  Returns 0, or -1 for invalid sizes. */
 int orc_mla_attn_split(const orc_attn_args *a, uint16_t *o, float *lse);
 
+/* Downstream: this rank's o_proj shard, out[t][j] = sum_k core[t][k] W[j][k]
+ * (see mla_oracle.c).  out bf16 [S, Nout] dense. */
+typedef struct {
+  int S, K, Nout;          /* tokens, input width (H*128), output features      */
+  const uint16_t *x;       /* bf16 [S, K] (core), row stride x_st               */
+  int64_t x_st;
+  const uint16_t *w;       /* bf16 [Nout, K], row stride w_sj                   */
+  int64_t w_sj;
+} orc_oproj_args;
+int orc_o_proj(const orc_oproj_args *a, uint16_t *out);
+
 #endif
