@@ -49,7 +49,7 @@ def load_peaks():
 # the source file of each kernel named in a bench line; the shared headers
 # (device helpers, parameter structs, launch declarations) count for every one
 KERNEL_FILES = {"tc": "kernel_tc.cu", "tc_ksplit_cluster4": "kernel_ks.cu", "simt": "kernel_simt.cu",
-                "dcp_pack": "kernel_pack.cu", "attn_split_kv": "kernel_attn.cu"}
+                "dcp_pack": "kernel_pack.cu", "attn_split_kv": "kernel_attn.cu", "o_proj": "kernel_oproj.cu"}
 SHARED_SOURCES = ("device_common.cuh", "kernels.h", "kparams.h")
 
 
@@ -965,6 +965,184 @@ def run_gpu_attn(args):
     return line
 
 
+def oproj_oracle_rate(host, budget_s: float):
+    """The oracle's o_proj on a bounded sample of token rows (all outputs of
+    each), scaled to the call.  Returns (tokens/s, description)."""
+    import numpy as np
+
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle
+
+    import torch
+
+    def u16(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    x, w = u16(host["x"]), u16(host["w"])
+    n, spent = 0, 0.0
+    while spent < budget_s and n < host["S"]:
+        t0 = time.perf_counter()
+        oracle.o_proj(x[n:n + 1].copy(), w)
+        spent += time.perf_counter() - t0
+        n += 1
+    return n / spent, f"{n} token rows x {host['Nout']} outputs x K={host['K']}, single-threaded oracle"
+
+
+def run_reference_oproj(args):
+    """The oracle's o_proj shard on the host cores (bounded sample)."""
+    import torch
+
+    ws, rank, _ = dist_env()
+    if ws > 1:
+        dist = init_dist(ws, "gloo")
+        if rank != 0:
+            dist.barrier()
+            return
+    from mla_decode_attention_lse_gb300 import synth
+
+    wl = synth.OPROJ_WORKLOADS[args.workload]
+    inp = synth.make_oproj(wl, device="cpu")
+    budget = args.ref_budget / max(1, args.steps + args.warmup)
+    for _ in range(args.warmup):
+        oproj_oracle_rate(inp, budget)
+    secs, desc = 0.0, ""
+    for _ in range(args.steps):
+        rate, desc = oproj_oracle_rate(inp, budget)
+        secs += wl.S / rate
+    value = wl.S * args.steps / secs
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "S": wl.S, "K": wl.K, "Nout": wl.Nout},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc,
+                         "host": host_cpu()},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def run_gpu_oproj(args):
+    """One step = this rank's o_proj shard on the decode step's core rows."""
+    import torch
+
+    import mla_decode_attention_lse_gb300 as m
+    from mla_decode_attention_lse_gb300 import synth
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = init_dist(ws, "nccl") if ws > 1 else None
+    dev = torch.device("cuda", local)
+    m.load_library()
+    wl = synth.OPROJ_WORKLOADS[args.workload]
+    seed0 = wl.seed + rank
+
+    def with_out(c):
+        c["out"] = torch.empty(wl.S, wl.Nout, dtype=torch.bfloat16, device=dev)
+        return c
+
+    def call(c, stream=None):
+        m.mla_o_proj(c["x"], c["w"], c["out"], stream=stream)
+
+    inp = with_out(synth.make_oproj(wl, device=dev, seed=seed0))
+    nbytes = synth.oproj_bytes(inp)
+    rotate = args.rotate or max(1, -(-L2_DEFEAT_BYTES // nbytes))
+    copies = [inp] + [with_out(synth.make_oproj(wl, device=dev, seed=seed0 + 1000 * k)) for k in range(1, rotate)]
+    stream = torch.cuda.current_stream(dev)
+    for k in range(max(3, args.warmup)):
+        call(copies[k % rotate])
+    torch.cuda.synchronize()
+    assert m.mla_combine_uv_status(stream) == m.MLA_OK
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    with torch.cuda.graph(g, stream=cap):
+        for k in range(args.steps):
+            call(copies[k % rotate])
+    g.replay()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        t_wall0 = time.perf_counter()
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    clocks = clk.summary()
+    total_ms = reduce_max(e0.elapsed_time(e1), dist, dev)
+    cold_us = cold_launch_us(lambda: call(copies[0]), stream, dev)
+    assert m.mla_combine_uv_status(stream) == m.MLA_OK
+    ms = total_ms / args.steps
+    value = replica_rate(wl.S, args.steps, ws, total_ms)
+    peak, peak_kind = load_peaks()
+    achieved = nbytes / (ms / 1e3) / 1e9
+    # end to end: the core rows from pinned host memory, the output back (the
+    # weight stays resident, as a model's would)
+    x_host = torch.empty(inp["x"].shape, dtype=torch.bfloat16, pin_memory=True)
+    x_host.copy_(inp["x"])
+    out_host = torch.empty(inp["out"].shape, dtype=torch.bfloat16, pin_memory=True)
+    dbuf = with_out({"x": torch.empty_like(inp["x"]), "w": inp["w"]})
+    e2e_steps = max(3, min(args.steps, 50))
+
+    def e2e_step():
+        dbuf["x"].copy_(x_host, non_blocking=True)
+        call(dbuf, stream=stream)
+        out_host.copy_(dbuf["out"], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_value = replica_rate(wl.S, e2e_steps, ws, reduce_max(e0.elapsed_time(e1), dist, dev))
+    line = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and ws == 1:
+            host = {k: (v.cpu() if hasattr(v, "cpu") else v) for k, v in inp.items()}
+            rate, desc = oproj_oracle_rate(host, args.cpu_budget)
+            cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc,
+                   "host": host_cpu()}
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": f"{args.workload}: this rank's o_proj shard, {wl.S} tokens x K={wl.K} "
+                                   f"(core rows) times the weight slice [{wl.Nout}, {wl.K}]",
+                       "S": wl.S, "K": wl.K, "Nout": wl.Nout, "parallelism": f"replicas x{ws}",
+                       "kernel": "o_proj",
+                       "l2": f"{rotate} independent input copies cycled, one per launch: every launch reads HBM",
+                       "timing": "CUDA graph of the timed launches, per-launch time = replay / steps"},
+            "achieved_gbs": achieved,
+            "roofline": {"bound": "hbm", "kernel": "o_proj", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": peak_kind,
+                         "traffic": traffic_from_profile(args.workload, "o_proj"), "algorithmic_bytes": nbytes},
+            "tensor": {"tflops": 2.0 * wl.S * wl.K * wl.Nout / (ms / 1e3) / 1e12},
+            "kernel_ms": {"mean": ms},
+            "cold_launch_us": cold_us,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "tokens/s",
+                    "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": out_host.numel() * 2,
+                    "steps": e2e_steps},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "wall_s": t_wall,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return line
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -988,6 +1166,9 @@ def main():
         args.warmup = 3
     from mla_decode_attention_lse_gb300 import synth
 
+    if args.workload in synth.OPROJ_WORKLOADS:
+        run_reference_oproj(args) if args.impl == "reference" else run_gpu_oproj(args)
+        return
     if args.workload in synth.ATTN_WORKLOADS:
         run_reference_attn(args) if args.impl == "reference" else run_gpu_attn(args)
         return

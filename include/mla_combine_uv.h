@@ -267,6 +267,40 @@ typedef struct {
  */
 int32_t mla_attn_split_kv(const mla_attn_split_kv_args *args, void *stream);
 
+/*
+ * Downstream of the stage: this rank's o_proj shard.  The vLLM page
+ * "vllm.models.kimi_k3.amd.specialized_decode.mono.attention.mla_back" ends
+ * the stage at "o_proj's input" (core); o_proj is a row-parallel linear layer,
+ * so the rank computes out[t][j] = sum_k core[t][k] * W[j][k] over its own
+ * H*128 inputs and the tensor-parallel all-reduce (multi-GPU, not part of
+ * this library) sums the ranks' outputs.  Accumulation in fp32 on the tensor
+ * cores, out rounded to bf16 once.
+ */
+typedef struct {
+  int32_t S;             /* tokens, >= 0                                      */
+  int32_t K;             /* input width (H*128), a multiple of 64             */
+  int32_t Nout;          /* output features, a multiple of 64                 */
+  const void *x;         /* bf16 [S, K] (core): row stride x_st (elements, a
+                            multiple of 8, >= K); 16-byte aligned             */
+  int64_t x_st;
+  const void *w;         /* bf16 [Nout, K] (the linear layer's weight slice):
+                            row stride w_sj (a multiple of 8, >= K); 16-byte
+                            aligned                                           */
+  int64_t w_sj;
+  void *out;             /* bf16 [S, Nout]: row stride out_st (>= Nout);
+                            caller-owned, every element written               */
+  int64_t out_st;
+} mla_o_proj_args;
+
+/*
+ * mla_o_proj -- enqueue the o_proj shard on `stream` (a persistent
+ * tensor-core GEMM; at decode sizes it streams the weight from HBM).
+ * Returns MLA_OK, or MLA_ERR_NULL / _SHAPE / _STRIDE / _ALIGN before anything
+ * is launched (out untouched), or MLA_ERR_CUDA.  S == 0 launches nothing.
+ * (Added in ABI version 3.)
+ */
+int32_t mla_o_proj(const mla_o_proj_args *args, void *stream);
+
 /* A short English description of a status code (static storage). */
 const char *mla_status_str(int32_t status);
 

@@ -38,7 +38,7 @@ MLA_ERR_KERNEL = 9
 MLA_ERR_DATA = 10
 
 EXPORTED_SYMBOLS = ("mla_combine_uv", "mla_combine_uv_plan", "mla_combine_uv_status",
-                    "mla_dcp_pack", "mla_attn_split_kv", "mla_status_str", "mla_abi_version")
+                    "mla_dcp_pack", "mla_attn_split_kv", "mla_o_proj", "mla_status_str", "mla_abi_version")
 
 
 class MlaError(RuntimeError):
@@ -104,6 +104,16 @@ class AttnArgs(ctypes.Structure):
     ]
 
 
+class OprojArgs(ctypes.Structure):
+    """Mirror of ``mla_o_proj_args``."""
+    _fields_ = [
+        ("S", ctypes.c_int32), ("K", ctypes.c_int32), ("Nout", ctypes.c_int32),
+        ("x", ctypes.c_void_p), ("x_st", ctypes.c_int64),
+        ("w", ctypes.c_void_p), ("w_sj", ctypes.c_int64),
+        ("out", ctypes.c_void_p), ("out_st", ctypes.c_int64),
+    ]
+
+
 _lib = None
 
 
@@ -133,6 +143,8 @@ def load_library(path: str | None = None):
     L.mla_dcp_pack.argtypes = [ctypes.POINTER(PackArgs), ctypes.c_void_p]
     L.mla_attn_split_kv.restype = ctypes.c_int32
     L.mla_attn_split_kv.argtypes = [ctypes.POINTER(AttnArgs), ctypes.c_void_p]
+    L.mla_o_proj.restype = ctypes.c_int32
+    L.mla_o_proj.argtypes = [ctypes.POINTER(OprojArgs), ctypes.c_void_p]
     _lib = L
     return L
 
@@ -307,6 +319,40 @@ def mla_attn_split_kv(qv, kv, kv_len, q, spr, scale, o, lse, stream=None) -> Non
     st = load_library().mla_attn_split_kv(ctypes.byref(a), ctypes.c_void_p(s))
     if st != MLA_OK:
         raise MlaError(st, "mla_attn_split_kv")
+
+
+def make_oproj_args(x, w, out) -> OprojArgs:
+    """Fill ``mla_o_proj_args`` from tensors (pointers and element strides)."""
+    a = OprojArgs()
+    a.S, a.K = x.shape
+    a.Nout = w.shape[0]
+    a.x, a.x_st = _ptr(x), x.stride(0)
+    a.w, a.w_sj = _ptr(w), w.stride(0)
+    a.out, a.out_st = _ptr(out), out.stride(0)
+    return a
+
+
+def mla_o_proj(x, w, out, stream=None) -> None:
+    """This rank's o_proj shard on CUDA tensors: out = x @ w.T.
+
+    x [S, K] bf16 (core rows, unit-stride rows), w [Nout, K] bf16 (the linear
+    layer's weight slice), out [S, Nout] bf16 (unit-stride rows).
+    """
+    import torch
+
+    if x.dtype != torch.bfloat16 or w.dtype != torch.bfloat16 or out.dtype != torch.bfloat16:
+        raise ValueError("x, w and out must be bf16")
+    if x.dim() != 2 or w.dim() != 2 or out.dim() != 2 or x.shape[1] != w.shape[1]:
+        raise ValueError("x [S, K], w [Nout, K], out [S, Nout]")
+    if tuple(out.shape) != (x.shape[0], w.shape[0]) or x.stride(1) != 1 or w.stride(1) != 1 or out.stride(1) != 1:
+        raise ValueError("out must be [S, Nout]; every last dimension unit-stride")
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    a = make_oproj_args(x, w, out)
+    st = load_library().mla_o_proj(ctypes.byref(a), ctypes.c_void_p(s))
+    if st != MLA_OK:
+        raise MlaError(st, "mla_o_proj")
 
 
 def mla_combine_uv_plan(args: Args, num_sms: int = 0) -> dict:

@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libmla_combine_uv.so")
-SOURCES = ["api.cu", "kernel_simt.cu", "kernel_tc.cu", "kernel_ks.cu", "kernel_pack.cu", "kernel_attn.cu"]
+SOURCES = ["api.cu", "kernel_simt.cu", "kernel_tc.cu", "kernel_ks.cu", "kernel_pack.cu", "kernel_attn.cu", "kernel_oproj.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

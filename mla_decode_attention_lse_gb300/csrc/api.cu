@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "mla_combine_uv.h"
+#include "kernel_oproj.h"
 #include "kernels.h"
 
 namespace {
@@ -217,6 +218,33 @@ int32_t make_kv_tmap(const mla_attn_split_kv_args *a, CUtensorMap *tm) {
   return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_STRIDE;
 }
 
+// TMA descriptor of a bf16 matrix [rows, cols] (row stride in elements) as
+// a 3-D map with a unit third dimension: boxes of 64 columns x box_rows rows,
+// 128-byte swizzle; rows past the matrix read as zero.
+int32_t make_rows_tmap(const void *base, int64_t rows, int64_t cols, int64_t row_stride, int box_rows,
+                       CUtensorMap *tm) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+      void *fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return MLA_ERR_CUDA;
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+  }
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, 1};
+  cuuint64_t strides[2] = {(cuuint64_t)row_stride * 2, (cuuint64_t)row_stride * 2 * (cuuint64_t)rows};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_STRIDE;
+}
+
 // Per-device state: SM count and the error word's device address.
 int32_t device_state(int *dev_out, int *sms_out, int **err_out) {
   int dev = 0;
@@ -376,6 +404,36 @@ int32_t mla_attn_split_kv(const mla_attn_split_kv_args *a, void *stream) {
   p.lse = a->lse;
   p.err = err;
   const cudaError_t e = mla::launch_attn(p, tm, sms, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int32_t mla_o_proj(const mla_o_proj_args *a, void *stream) {
+  if (!a) return MLA_ERR_NULL;
+  if (a->S < 0 || a->K < 64 || a->K % 64 || a->Nout < 64 || a->Nout % 64) return MLA_ERR_SHAPE;
+  if (a->S == 0) return MLA_OK;
+  if (!a->x || !a->w || !a->out) return MLA_ERR_NULL;
+  if (!aligned(a->x, 16) || !aligned(a->w, 16) || !aligned(a->out, 2)) return MLA_ERR_ALIGN;
+  if (a->x_st < a->K || a->x_st % 8 || a->w_sj < a->K || a->w_sj % 8 || a->out_st < a->Nout) return MLA_ERR_STRIDE;
+  const int nt = mla::oproj_tokens_per_unit(a->S);
+  CUtensorMap wm, xm;
+  int32_t st = make_rows_tmap(a->w, a->Nout, a->K, a->w_sj, 64, &wm);
+  if (st != MLA_OK) return st;
+  st = make_rows_tmap(a->x, a->S, a->K, a->x_st, nt, &xm);
+  if (st != MLA_OK) return st;
+  int dev, sms;
+  int *err;
+  st = device_state(&dev, &sms, &err);
+  if (st != MLA_OK) return st;
+  mla::OprojParams p;
+  std::memset(&p, 0, sizeof p);
+  p.S = a->S;
+  p.K = a->K;
+  p.Nout = a->Nout;
+  p.nt = nt;
+  p.out = static_cast<uint16_t *>(a->out);
+  p.out_st = a->out_st;
+  p.err = err;
+  const cudaError_t e = mla::launch_oproj(p, wm, xm, sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

@@ -1,0 +1,263 @@
+// kernel_oproj.cu -- downstream of the stage: this rank's o_proj shard.
+//
+// The vLLM page "vllm.models.kimi_k3.amd.specialized_decode.mono.attention.
+// mla_back" ends its stage at "o_proj's input" (core, [S, H*128]).  o_proj is
+// a row-parallel linear layer: the rank multiplies its core rows by its slice
+// of the weight, out[t][j] = sum_k core[t][k] W[j][k], and the tensor-parallel
+// all-reduce (multi-GPU) sums the ranks' outputs.  At decode sizes (64 tokens,
+// K = 1536, 7168 outputs) the shard streams 22 MB of weight for 64 tokens: an
+// HBM-bound GEMM.
+//
+// Work units are (64 output features, NT tokens); a persistent grid of one
+// CTA per SM walks them.  Warp 0 (one lane) brings, per 64-wide K block, the
+// W box [64 rows x 64] and the core box [NT rows x 64] by TMA into a ring of
+// stages; warp 1 (one lane) issues D[j, t] += W x^T as four kind::f16 MMAs
+// of M = 64, N = NT, K = 16 per stage into one of two TMEM accumulators (D row
+// i of an M = 64 MMA sits in TMEM lane 32 (i / 16) + i % 16); warps 2..5
+// read the accumulator (lanes 0..15 of their quadrant), round to bf16 and
+// store out.  The W copies of the first stages go out before the wait for
+// the previous kernel (a weight no earlier kernel writes); the core rows and
+// every store come after it.  Every wait is bounded.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "device_common.cuh"
+#include "kernel_oproj.h"
+#include "kparams.h"
+
+namespace mla {
+
+namespace {
+
+constexpr int kOpM = 64;       // output features per unit (MMA M)
+constexpr int kOpThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr uint32_t kOpABytes = kOpM * 128u;  // a W box: 64 rows x 128 B
+
+template <int NT>
+struct OpLayout {
+  static constexpr uint32_t stage = kOpABytes + (uint32_t)NT * 128u;
+  static constexpr int kStages = (NT == 64) ? 12 : (NT == 128) ? 8 : 5;
+  static constexpr uint32_t bar_off = kStages * stage;  // full[ST], empty[ST], acc_full[2], acc_empty[2]
+  static constexpr uint32_t misc_off = bar_off + (2 * kStages + 4) * 8u;
+  static constexpr uint32_t total = misc_off + 16u;
+  static constexpr uint32_t tmem_cols = 2u * NT < 32u ? 32u : 2u * NT;
+};
+static_assert(OpLayout<64>::total + 1024 <= 227u * 1024u, "shared memory (NT = 64)");
+static_assert(OpLayout<128>::total + 1024 <= 227u * 1024u, "shared memory (NT = 128)");
+static_assert(OpLayout<256>::total + 1024 <= 227u * 1024u, "shared memory (NT = 256)");
+
+__device__ __forceinline__ bool op_wait(uint32_t bar, uint32_t parity, int *err, volatile int *abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > kWaitNs) {
+      atomicCAS(err, 0, kErrWaitMma);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+}  // namespace
+
+template <int NT>
+__global__ void __launch_bounds__(kOpThreads, 1)
+    oproj_kernel(const __grid_constant__ OprojParams p, const __grid_constant__ CUtensorMap wmap,
+                 const __grid_constant__ CUtensorMap xmap) {
+  using L = OpLayout<NT>;
+  constexpr int ST = L::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;  // swizzle atoms: 1024-byte aligned
+  uint8_t *gbase = smem_raw + (sbase - raw);
+  uint32_t *misc = reinterpret_cast<uint32_t *>(gbase + L::misc_off);
+  volatile int *s_abort = reinterpret_cast<volatile int *>(&misc[1]);
+  const uint32_t bar0 = sbase + L::bar_off;
+  auto full = [&](int s) { return bar0 + 8u * (uint32_t)s; };
+  auto empty = [&](int s) { return bar0 + 8u * (uint32_t)(ST + s); };
+  auto acc_full = [&](int b) { return bar0 + 8u * (uint32_t)(2 * ST + b); };
+  auto acc_empty = [&](int b) { return bar0 + 8u * (uint32_t)(2 * ST + 2 + b); };
+  auto sA = [&](int s) { return sbase + (uint32_t)s * L::stage; };
+  auto sB = [&](int s) { return sbase + (uint32_t)s * L::stage + kOpABytes; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(full(s), 1u);
+      mbar_init(empty(s), 1u);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full(b), 1u);
+      mbar_init(acc_empty(b), 4u);
+    }
+    misc[1] = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&misc[0]), L::tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  // unit u: output features 64 (u % MT) .., tokens NT (u / MT) ..
+  const int MT = p.Nout / kOpM, units = MT * ((p.S + NT - 1) / NT), KB = p.K / 64;
+
+  if (warp == 0) {
+    // ---- TMA producer ----
+    if (lane == 0) {
+      bool ok = true;
+      int issued = 0;  // stages whose copies were issued
+      const int u0 = blockIdx.x;
+      // the first stages' weight boxes go out before the wait for the previous
+      // kernel (no earlier kernel writes the weight); their core boxes after it
+      const int pre = u0 < units ? min(ST, KB) : 0;
+      for (int g = 0; g < pre; ++g) {
+        mbar_arrive_expect_tx(full(g), L::stage);
+        tma_load_3d(sA(g), &wmap, 64 * g, (u0 % MT) * kOpM, 0, full(g));
+      }
+      grid_dependency_wait();
+      for (int g = 0; g < pre; ++g) tma_load_3d(sB(g), &xmap, 64 * g, (u0 / MT) * NT, 0, full(g));
+      issued = pre;
+      int g = 0;
+      for (int u = u0; u < units && ok; u += gridDim.x) {
+        const int mt = u % MT, nt = u / MT;
+        for (int kb = 0; kb < KB; ++kb, ++g) {
+          if (g < pre) continue;  // issued above
+          const int s = g % ST;
+          if (g >= ST) ok = op_wait(empty(s), (uint32_t)(g / ST - 1) & 1u, p.err, s_abort);
+          if (!ok) break;
+          mbar_arrive_expect_tx(full(s), L::stage);
+          tma_load_3d(sA(s), &wmap, 64 * kb, mt * kOpM, 0, full(s));
+          tma_load_3d(sB(s), &xmap, 64 * kb, nt * NT, 0, full(s));
+          issued = g + 1;
+        }
+      }
+      // after an abort: the copies still in flight land before the CTA exits
+      for (int q = issued - ST < 0 ? 0 : issued - ST; q < issued; ++q)
+        mbar_wait(full(q % ST), (uint32_t)(q / ST) & 1u, p.err, kErrWaitTeardown);
+    }
+  } else if (warp == 1) {
+    // ---- MMA issuer: D[j, t] += W[j, k] x[t, k], two accumulators ----
+    if (lane == 0) {
+      constexpr uint32_t kId = idesc_bf16(kOpM, NT);
+      bool ok = true;
+      int g = 0, i = 0, last0 = -1, last1 = -1;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++i) {
+        const int b = i & 1;
+        if (i >= 2) ok = op_wait(acc_empty(b), (uint32_t)((i >> 1) - 1) & 1u, p.err, s_abort);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(b * NT);
+        for (int kb = 0; kb < KB; ++kb, ++g) {
+          const int s = g % ST;
+          ok = op_wait(full(s), (uint32_t)(g / ST) & 1u, p.err, s_abort);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t dA = (uint32_t)smem_desc_sw128(sA(s)), dB = (uint32_t)smem_desc_sw128(sB(s));
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4)
+            tc_mma_f16(d, desc_sw128_at(dA, (uint32_t)k4 * 32u), desc_sw128_at(dB, (uint32_t)k4 * 32u), kId,
+                       (kb | k4) ? 1u : 0u);
+          tc_commit(empty(s));
+        }
+        if (!ok) break;
+        tc_commit(acc_full(b));
+        if (b == 0)
+          last0 = i;
+        else
+          last1 = i;
+      }
+      // after an abort: the committed MMAs finish before TMEM is freed
+      if (last0 >= 0) mbar_wait(acc_full(0), (uint32_t)(last0 >> 1) & 1u, p.err, kErrWaitTeardown);
+      if (last1 >= 0) mbar_wait(acc_full(1), (uint32_t)(last1 >> 1) & 1u, p.err, kErrWaitTeardown);
+    }
+  } else {
+    // ---- epilogue warps 2..5: quadrant warp % 4; an M = 64 accumulator has
+    // row 16 q + l in lane l < 16 of quadrant q ----
+    const int qd = warp & 3;
+    const bool act = lane < 16;
+    const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);
+    grid_dependency_wait();  // out may still be read by the kernel before
+    int i = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++i) {
+      const int b = i & 1, mt = u % MT, nt = u / MT;
+      bool ok = op_wait(acc_full(b), (uint32_t)(i >> 1) & 1u, p.err, s_abort);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const int j = mt * kOpM + qd * 16 + (lane & 15);
+#pragma unroll 1
+      for (int c = 0; c < NT; c += 16) {
+        uint32_t r[16];
+        tmem_ld_x16(trow + (uint32_t)(b * NT + c), r);
+        tc_wait_ld();
+        if (act) {
+#pragma unroll
+          for (int x = 0; x < 16; ++x) {
+            const int t = nt * NT + c + x;
+            if (t < p.S) {
+              const __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(r[x]));
+              p.out[(long long)t * p.out_st + j] = *reinterpret_cast<const uint16_t *>(&h);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty(b));
+    }
+    grid_launch_dependents();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::tmem_cols);
+  }
+}
+
+int oproj_tokens_per_unit(int S) { return S <= 64 ? 64 : S <= 128 ? 128 : 256; }
+size_t oproj_smem_bytes(int nt) {
+  return 1024 + (nt == 64 ? OpLayout<64>::total : nt == 128 ? OpLayout<128>::total : OpLayout<256>::total);
+}
+
+template <int NT>
+static cudaError_t launch_oproj_n(const OprojParams &p, const CUtensorMap &wmap, const CUtensorMap &xmap,
+                                  unsigned grid, cudaStream_t stream) {
+  const size_t smem = 1024 + OpLayout<NT>::total;
+  cudaError_t e = cudaFuncSetAttribute(oproj_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kOpThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, oproj_kernel<NT>, p, wmap, xmap);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+// Persistent: one CTA per SM (the stage ring fills an SM), at most one per unit.
+cudaError_t launch_oproj(const OprojParams &p, const CUtensorMap &wmap, const CUtensorMap &xmap, int num_sms,
+                         cudaStream_t stream) {
+  if (p.S < 1 || p.K < 64 || p.K % 64 || p.Nout < kOpM || p.Nout % kOpM || num_sms < 1) return cudaErrorInvalidValue;
+  if (p.nt != oproj_tokens_per_unit(p.S)) return cudaErrorInvalidValue;
+  const long long units = (long long)(p.Nout / kOpM) * ((p.S + p.nt - 1) / p.nt);
+  if (units >= (1LL << 31)) return cudaErrorInvalidValue;
+  const unsigned grid = (unsigned)(units < num_sms ? units : num_sms);
+  if (p.nt == 64) return launch_oproj_n<64>(p, wmap, xmap, grid, stream);
+  if (p.nt == 128) return launch_oproj_n<128>(p, wmap, xmap, grid, stream);
+  return launch_oproj_n<256>(p, wmap, xmap, grid, stream);
+}
+
+}  // namespace mla

@@ -379,3 +379,40 @@ def attn_bytes(inp) -> int:
     rows = int(inp["kv_len"].long().sum())
     S = B * q
     return rows * ATTN_K * 2 + S * H * ATTN_K * 2 + spr * S * H * (D * 2 + 4)
+
+
+# ---- inputs of the downstream o_proj shard ---------------------------------
+
+@dataclass(frozen=True)
+class OprojWorkload:
+    """One rank's o_proj shard: S tokens of core (K = H * 128 wide) times the
+    rank's weight slice [Nout, K]."""
+    name: str
+    S: int
+    K: int
+    Nout: int
+    seed: int = 0
+
+
+OPROJ_WORKLOADS = {
+    # the decode step: 64 tokens, 12 heads per rank (K = 1536), 7168 outputs
+    "oproj_decode": OprojWorkload("oproj_decode", S=64, K=12 * V, Nout=7168, seed=31),
+}
+
+
+def make_oproj(wl: OprojWorkload | str, device="cpu", seed: int | None = None):
+    """core rows x ~ sigmoid(N(0,1)) * N(0,1) (a gated latent) and the weight
+    W ~ N(0, 1/sqrt(K)), both bf16."""
+    if isinstance(wl, str):
+        wl = OPROJ_WORKLOADS[wl]
+    seed = wl.seed if seed is None else seed
+    g = _gen(device, seed)
+    x = (_normal((wl.S, wl.K), 1.0, g, device) * torch.sigmoid(_normal((wl.S, wl.K), 1.0, g, device)))
+    x = x.to(torch.bfloat16).contiguous()
+    w = _normal((wl.Nout, wl.K), 1.0 / math.sqrt(wl.K), g, device, torch.bfloat16)
+    return dict(x=x, w=w, S=wl.S, K=wl.K, Nout=wl.Nout, wl=wl)
+
+
+def oproj_bytes(inp) -> int:
+    """Algorithmic bytes of one o_proj call: the weight, the core rows, the output."""
+    return 2 * (inp["Nout"] * inp["K"] + inp["S"] * inp["K"] + inp["S"] * inp["Nout"])

@@ -169,6 +169,49 @@ def test_attn_validation_errors(lib):
     assert st(attn_args(B=0, qv=None, kv=None)) == m.MLA_OK  # nothing to do, nothing read
 
 
+def test_oproj_args_struct_layout_matches_header(lib, tmp_path):
+    fields = [f for f, _ in m.OprojArgs._fields_]
+    prog = ["#include <stdio.h>", "#include <stddef.h>", '#include "mla_combine_uv.h"',
+            "int main(void) {", 'printf("%zu\\n", sizeof(mla_o_proj_args));']
+    prog += [f'printf("%zu\\n", offsetof(mla_o_proj_args, {f}));' for f in fields]
+    prog += ["return 0; }"]
+    src = tmp_path / "probe_oproj.c"
+    src.write_text("\n".join(prog))
+    exe = tmp_path / "probe_oproj"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                           check=True).stdout.split()]
+    assert vals[0] == ctypes.sizeof(m.OprojArgs)
+    for f, off in zip(fields, vals[1:]):
+        assert getattr(m.OprojArgs, f).offset == off, f
+
+
+def oproj_args(S=64, K=1536, Nout=7168, **kw):
+    a = m.OprojArgs()
+    a.S, a.K, a.Nout = S, K, Nout
+    a.x, a.x_st = ALIGNED, K
+    a.w, a.w_sj = ALIGNED * 2, K
+    a.out, a.out_st = ALIGNED * 3, Nout
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_oproj_validation_errors(lib):
+    fn = lib.mla_o_proj
+    st = lambda a: fn(ctypes.byref(a), None)  # noqa: E731  (errors return before any CUDA call)
+    assert fn(None, None) == m.MLA_ERR_NULL
+    assert st(oproj_args(S=-1)) == m.MLA_ERR_SHAPE
+    assert st(oproj_args(K=100)) == m.MLA_ERR_SHAPE
+    assert st(oproj_args(Nout=100)) == m.MLA_ERR_SHAPE
+    assert st(oproj_args(w=None)) == m.MLA_ERR_NULL
+    assert st(oproj_args(x=ALIGNED + 8)) == m.MLA_ERR_ALIGN
+    assert st(oproj_args(x_st=1000)) == m.MLA_ERR_STRIDE   # below K
+    assert st(oproj_args(w_sj=1540)) == m.MLA_ERR_STRIDE   # not a multiple of 8
+    assert st(oproj_args(out_st=100)) == m.MLA_ERR_STRIDE  # below Nout
+    assert st(oproj_args(S=0, x=None, w=None, out=None)) == m.MLA_OK  # nothing to do
+
+
 # ---- planning / validation without a GPU ---------------------------------
 
 ALIGNED = 1 << 20  # fake, 16-byte aligned device addresses: never dereferenced
