@@ -49,7 +49,8 @@ def load_peaks():
 # the source file of each kernel named in a bench line; the shared headers
 # (device helpers, parameter structs, launch declarations) count for every one
 KERNEL_FILES = {"tc": "kernel_tc.cu", "tc_ksplit_cluster4": "kernel_ks.cu", "simt": "kernel_simt.cu",
-                "dcp_pack": "kernel_pack.cu", "attn_split_kv": "kernel_attn.cu", "o_proj": "kernel_oproj.cu"}
+                "dcp_pack": "kernel_pack.cu", "attn_split_kv": "kernel_attn.cu",
+                "o_proj": ("kernel_oproj.cu", "kernel_oproj.h")}
 SHARED_SOURCES = ("device_common.cuh", "kernels.h", "kparams.h")
 
 
@@ -58,7 +59,11 @@ def kernel_source_hash(kernel: str | None = None) -> str:
     is named)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_decode_attention_lse_gb300", "csrc")
-    files = sorted(os.listdir(csrc)) if kernel is None else sorted(SHARED_SOURCES + (KERNEL_FILES[kernel],))
+    if kernel is None:
+        files = sorted(os.listdir(csrc))
+    else:
+        own = KERNEL_FILES[kernel]
+        files = sorted(SHARED_SOURCES + (own if isinstance(own, tuple) else (own,)))
     for f in files:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode())
