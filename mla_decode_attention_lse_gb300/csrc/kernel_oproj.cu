@@ -104,6 +104,9 @@ __global__ void __launch_bounds__(kOpThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
+  // the next launch on the stream may begin its prologue while this grid
+  // runs (its dependent work waits for this grid's completion)
+  grid_launch_dependents();
   // unit u: output features 64 (u % MT) .., tokens NT (u / MT) ..
   const int MT = p.Nout / kOpM, units = MT * ((p.S + NT - 1) / NT), KB = p.K / 64;
 
@@ -211,7 +214,6 @@ __global__ void __launch_bounds__(kOpThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty(b));
     }
-    grid_launch_dependents();
   }
   tc_fence_before();
   __syncthreads();
