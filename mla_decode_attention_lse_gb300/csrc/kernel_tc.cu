@@ -366,16 +366,16 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
     }
   };
 
-  // The first JB partials of a unit, for every valid token, without weights.
-  auto issue_blind = [&](const Cur &c, Buf &buf) {
+  // Partials j0 .. j0+JB-1 of a unit, for every valid token, without weights.
+  auto issue_blind = [&](const Cur &c, int j0, Buf &buf) {
 #pragma unroll
     for (int tk = 0; tk < TPW; ++tk) {
       const int t = c.tile * BN + warp * TPW + tk;
       const int r0 = (layout == kRequestMajor) ? (t / p.q) * p.spr : 0;
-      const uint16_t *base = p.o + off3(t, p.o_st, c.h, p.o_sh, r0, p.o_sp);
+      const uint16_t *base = p.o + off3(t, p.o_st, c.h, p.o_sh, r0 + j0, p.o_sp);
 #pragma unroll
       for (int jj = 0; jj < JB; ++jj) {
-        if (jj < n && t < p.S) {
+        if (j0 + jj < n && t < p.S) {
           const uint4 *row = reinterpret_cast<const uint4 *>(base + off1(jj, p.o_sp));
           buf[jj][tk][0] = __ldcs(row + lane);
           buf[jj][tk][1] = __ldcs(row + lane + 32);
@@ -616,6 +616,15 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
   float wcur = 0.0f, wnxt = 0.0f;       // weights of units i and i+1
   Buf bufA, bufB;
   Wts wA, wB;
+  // MXFP4, 32-token tiles, two batches per unit (the large batch): the first
+  // unit's second batch is issued blind with the first, so both register
+  // buffers load during the LSE round trip.  Measured 291 -> 282 us per
+  // launch, more than one unit of ~80 per CTA can save: the gain is in the
+  // code generated for the loop.  bf16 (319 -> 322 us) and the decode-size
+  // instances (stacked MXFP4 8.24 -> 8.78 us in the even-batch loop) measured
+  // slower with it, so their code stays without it.
+  const bool pair_loop = kTwoBatchLoop && (nb == 2 || (!(WFMT != 0 && BN == 16 && NW == 16) && nb % 2 == 0));
+  const bool blind2 = kTwoBatchLoop && WFMT != 0 && BN == 32 && nb == 2;
   Cur cu = c_first;    // unit i (being merged)
   Cur cn = c_first;    // unit of the next batch to issue
   Cur cl = c_first;    // next unit whose LSE is loaded (i+3)
@@ -643,12 +652,19 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
     // the first batch is issued before its weights are known (all partials
     // of the range; rows that turn out dead are loaded but never merged), so
     // its loads overlap the LSE round trip
-    issue_blind(cu, bufA);
+    issue_blind(cu, 0, bufA);
+    if (blind2) issue_blind(cu, JB, bufB);
     weights_of(lse0, wcur);
 #pragma unroll
     for (int jj = 0; jj < JB; ++jj)
 #pragma unroll
       for (int tk = 0; tk < TPW; ++tk) wA[jj][tk] = __shfl_sync(0xffffffffu, wcur, tk * SEG + jj);
+    if (blind2) {
+#pragma unroll
+      for (int jj = 0; jj < JB; ++jj)
+#pragma unroll
+        for (int tk = 0; tk < TPW; ++tk) wB[jj][tk] = __shfl_sync(0xffffffffu, wcur, tk * SEG + JB + jj);
+    }
     if (nbi == nb) {
       nbi = 0;
       advance(cn);
@@ -720,8 +736,9 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
         ok = false;
         break;
       }
-      // batch 0 of unit i is in bufA: send batch 1 of unit i, merge batch 0
-      issue(cn, JB, bufB, wB, wcur);
+      // batch 0 of unit i is in bufA: send batch 1 of unit i (the first
+      // unit's went out blind), merge batch 0
+      if (!(blind2 && k == 0)) issue(cn, JB, bufB, wB, wcur);
       advance(cn);
       consume(bufA, wA);
       // batch 1 in bufB: send batch 0 of unit i+1, merge batch 1, finish unit i
@@ -735,7 +752,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
       advance(cu);
       ++i;
     }
-  } else if (kTwoBatchLoop && !(WFMT != 0 && BN == 16 && NW == 16) && nb % 2 == 0) {
+  } else if (pair_loop) {
     // an even number of batches per unit (decode sizes with more partials):
     // batch pairs, the unit's finish once after its last pair (decode 2%
     // faster; not for the one-token-per-warp MXFP4 instance, where it spills)
