@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define MLA_ABI_VERSION 3
+#define MLA_ABI_VERSION 4
 
 /* W_V storage format. */
 enum {
@@ -82,7 +82,8 @@ enum {
 enum {
   MLA_KERNEL_AUTO = 0, /* pick by size (the plan says which)                  */
   MLA_KERNEL_SIMT = 1, /* CUDA-core kernel: any P; the small-batch path       */
-  MLA_KERNEL_TC = 2,   /* fused tcgen05 kernel: partials per token <= 32       */
+  MLA_KERNEL_TC = 2,   /* fused tcgen05 kernel: partials per token <= 32
+                          (<= 16 with 32-token tiles)                        */
   MLA_KERNEL_KSPLIT = 3 /* a (head, 16-token) unit per 4-CTA cluster, the
                           512 latents split over the cluster and the partial
                           GEMMs summed through distributed shared memory;
@@ -120,7 +121,9 @@ typedef struct {
   void *out;                  /* bf16 [S_out, H*128], dense row-major        */
 
   int32_t kernel;             /* MLA_KERNEL_*; 0 = automatic                  */
-  int32_t tile_tokens;        /* tensor-core token tile (16 or 32); 0 = auto  */
+  int32_t tile_tokens;        /* tensor-core token tile (8, 16 or 32; 8 added
+                                 in ABI version 4: two warps per token, each
+                                 merging half of its latents); 0 = auto      */
 } mla_combine_uv_args;
 
 /* What a call would launch (host-side planning only). */

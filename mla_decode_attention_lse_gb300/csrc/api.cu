@@ -80,7 +80,8 @@ int32_t plan_impl(const mla_combine_uv_args *a, int32_t num_sms, mla_plan *pl, K
   if (kernel != MLA_KERNEL_AUTO && kernel != MLA_KERNEL_SIMT && kernel != MLA_KERNEL_TC &&
       kernel != MLA_KERNEL_KSPLIT)
     return MLA_ERR_KERNEL;
-  if (a->tile_tokens != 0 && a->tile_tokens != 16 && a->tile_tokens != 32) return MLA_ERR_KERNEL;
+  if (a->tile_tokens != 0 && a->tile_tokens != 8 && a->tile_tokens != 16 && a->tile_tokens != 32)
+    return MLA_ERR_KERNEL;
   if (kernel == MLA_KERNEL_TC && n_part > mla::kTcMaxPart) return MLA_ERR_KERNEL;
   if (kernel == MLA_KERNEL_KSPLIT && (n_part > mla::kKsMaxPart || S == 0 ||
                                       (a->tile_tokens != 0 && a->tile_tokens != 16)))
@@ -115,10 +116,22 @@ int32_t plan_impl(const mla_combine_uv_args *a, int32_t num_sms, mla_plan *pl, K
   } else {
     if (num_sms <= 0) return MLA_ERR_SHAPE;
     int tile = a->tile_tokens;
-    // 32-token tiles once they give every SM a unit, else 16-token tiles
-    // (with MXFP4 W_V on two CTAs per SM); more than 16 partials per token
-    // need 16-token tiles
-    if (tile == 0) tile = ((int64_t)a->H * ((S + 31) / 32) >= num_sms && n_part <= 16) ? 32 : 16;
+    // 32-token tiles once they give every SM a unit; with bf16 W_V and 16
+    // or more partials per token, 8-token tiles (two warps per token, half a
+    // row each) when those still fit one unit per SM and make more units than
+    // 16-token tiles (a split-KV decode step: the partial rows spread over
+    // twice the SMs; with one partial, as many CTAs each copying W_V measured
+    // slower); else 16-token tiles (with MXFP4 W_V on two CTAs per SM).  More
+    // than 16 partials per token need 8- or 16-token tiles.
+    if (tile == 0) {
+      const int64_t u8 = (int64_t)a->H * ((S + 7) / 8);
+      if ((int64_t)a->H * ((S + 31) / 32) >= num_sms && n_part <= 16)
+        tile = 32;
+      else if (a->w_fmt == MLA_W_BF16 && n_part >= 16 && u8 <= num_sms && u8 > units16)
+        tile = 8;
+      else
+        tile = 16;
+    }
     if (n_part > mla::tc_max_part(tile, a->w_fmt)) return MLA_ERR_KERNEL;
     pl->tile_tokens = tile;
     pl->units = a->H * ((S + tile - 1) / tile);

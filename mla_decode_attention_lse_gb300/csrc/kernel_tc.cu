@@ -113,18 +113,29 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int
 
 }  // namespace
 
-template <int BN, int WFMT, int NW, bool O32>
+template <int BN, int WFMT, int NW, bool O32, bool HR>
 __global__ void __launch_bounds__(NW * 32, 16 / NW)
     tc_kernel(const __grid_constant__ KParams p) {
   constexpr int kWorkers = NW;             // all warps combine, drain and (one of them) issue
   constexpr int NT = NW * 32;              // threads
-  constexpr int TPW = BN / NW;             // tokens per warp per unit
-  constexpr int JB = 4 / TPW;              // partials per batch: 4 rows (8 x 16 B per lane)
+  // HR (half rows; 8-token tiles for split-KV decode steps with few units): a
+  // unit is BN / 2 tokens and two warps share a token, each merging one half
+  // of its 512 latents, so twice as many CTAs share the partial rows.  The
+  // MMA keeps N = BN: the latent rows of the absent tokens are never written,
+  // and their accumulator columns are computed from whatever those rows hold
+  // and never stored.  (The HR branches below are `if constexpr`, so the
+  // other instances compile exactly as without them: this kernel's speed was
+  // measured to depend on the code generated for its loop.)
+  constexpr int UT = HR ? BN / 2 : BN;     // tokens per unit
+  constexpr int TPW = HR ? 1 : BN / NW;    // tokens per warp per unit
+  constexpr int NCH = HR ? 1 : 2;          // 16-byte chunks per lane and partial row
+  constexpr int JB = HR ? 8 : 4 / TPW;     // partials per batch (8 x 16 B per lane)
   constexpr int CPW = 4 * BN / NW;         // TMEM columns each warp drains
   constexpr TcLayout L = tc_layout(BN, WFMT, NW);
   constexpr uint32_t kCols = L.tmem_cols;
   constexpr int ST = tc_stages(BN, WFMT);
   static_assert(TPW >= 1 && BN % NW == 0 && JB >= 1 && NW % 4 == 0, "tile must split over the warps");
+  static_assert(!HR || NW == 2 * UT, "half rows: two warps per token");
   static_assert(CPW == 4 || CPW == 8 || CPW == 16, "epilogue drains 4, 8 or 16 columns per warp");
 
   extern __shared__ uint8_t smem_raw[];
@@ -224,8 +235,14 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
 #pragma unroll
     for (int rd = 0; rd < kRounds; ++rd) {
       const int e = rd * 8 + (lane >> 2);
-      const int t = c.tile * BN + ws * CPW + e;
-      if ((lane & 3) == 0 && e < CPW && t < p.S) prefetch_l2_line(p.gate + off3(t, Wrow, c.h, kV, 1, wq * 32));
+      if constexpr (HR) {
+        const int t = c.tile * UT + ws * CPW + e;
+        if ((lane & 3) == 0 && e < CPW && ws * CPW + e < UT && t < p.S)
+          prefetch_l2_line(p.gate + off3(t, Wrow, c.h, kV, 1, wq * 32));
+      } else {
+        const int t = c.tile * BN + ws * CPW + e;
+        if ((lane & 3) == 0 && e < CPW && t < p.S) prefetch_l2_line(p.gate + off3(t, Wrow, c.h, kV, 1, wq * 32));
+      }
     }
   };
 
@@ -248,8 +265,11 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
 #pragma unroll
     for (int rd = 0; rd < kRounds; ++rd) {
       const int e = rd * 8 + (lane >> 2);
-      const int t = c.tile * BN + ws * CPW + e;
-      act[rd] = e < CPW && t < p.S;
+      const int t = c.tile * UT + ws * CPW + e;
+      if constexpr (HR)
+        act[rd] = e < CPW && ws * CPW + e < UT && t < p.S;
+      else
+        act[rd] = e < CPW && t < p.S;
       off[rd] = (long long)off3(t, Wrow, c.h, kV, 1, wq * 32 + v8);
       g[rd] = act[rd] ? __ldg(reinterpret_cast<const uint4 *>(p.gate + off[rd])) : make_uint4(0, 0, 0, 0);
     }
@@ -299,7 +319,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
 
   // This lane's LSE (-inf past n or past S; sanitised when used).
   auto load_lse = [&](const Cur &c, float &lv) {
-    const int t = c.tile * BN + warp * TPW + my_tk;
+    const int t = HR ? c.tile * UT + (warp >> 1) + my_tk : c.tile * BN + warp * TPW + my_tk;
     lv = kNegInf;
     if (!pass && t < p.S && my_j < n) {
       const int r0 = (layout == kRequestMajor) ? (t / p.q) * p.spr : 0;
@@ -314,12 +334,15 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
   // loads) it measured slower and is left out.
   auto prefetch_rows = [&](const Cur &c, float lv) {
     if (WFMT != 0) return;
-    const int t = c.tile * BN + warp * TPW + my_tk;
+    const int t = HR ? c.tile * UT + (warp >> 1) + my_tk : c.tile * BN + warp * TPW + my_tk;
     const bool live = pass ? (my_j == 0 && t < p.S) : isfinite(lv);
     if (live) {
       const int r0 = (layout == kRequestMajor) ? (t / p.q) * p.spr : 0;
-      prefetch_l2_bulk(p.o + off3(t, p.o_st, c.h, p.o_sh, r0 + my_j, p.o_sp),
-                       kD * 2);
+      if constexpr (HR)  // this warp's half of the row
+        prefetch_l2_bulk(p.o + off3(t, p.o_st, c.h, p.o_sh, r0 + my_j, p.o_sp) + (warp & 1) * (kD / 2), kD);
+      else
+        prefetch_l2_bulk(p.o + off3(t, p.o_st, c.h, p.o_sh, r0 + my_j, p.o_sp),
+                         kD * 2);
     }
   };
 
@@ -341,7 +364,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
     wg = (e == 0.0f) ? 0.0f : __fmul_rn(e, inv);
   };
 
-  using Buf = uint4[JB][TPW][2];
+  using Buf = uint4[JB][TPW][NCH];
   using Wts = float[JB][TPW];
 
   // Issue the loads of one batch: unit at cursor c, partials j0 .. j0+JB-1
@@ -349,7 +372,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
   auto issue = [&](const Cur &c, int j0, Buf &buf, Wts &w, float wg) {
 #pragma unroll
     for (int tk = 0; tk < TPW; ++tk) {
-      const int t = c.tile * BN + warp * TPW + tk;
+      const int t = HR ? c.tile * UT + (warp >> 1) + tk : c.tile * BN + warp * TPW + tk;
       const int r0 = (layout == kRequestMajor) ? (t / p.q) * p.spr : 0;
       const uint16_t *base = p.o + off3(t, p.o_st, c.h, p.o_sh, r0 + j0, p.o_sp);
 #pragma unroll
@@ -357,10 +380,17 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
         w[jj][tk] = __shfl_sync(0xffffffffu, wg, tk * SEG + j0 + jj);  // 0 past n
         if (w[jj][tk] != 0.0f && t < p.S) {
           const uint4 *row = reinterpret_cast<const uint4 *>(base + off1(jj, p.o_sp));
-          buf[jj][tk][0] = __ldcs(row + lane);
-          buf[jj][tk][1] = __ldcs(row + lane + 32);
+          if constexpr (HR) {
+            buf[jj][tk][0] = __ldcs(row + (warp & 1) * 32 + lane);
+          } else {
+            buf[jj][tk][0] = __ldcs(row + lane);
+            buf[jj][tk][1] = __ldcs(row + lane + 32);
+          }
         } else {
-          buf[jj][tk][0] = buf[jj][tk][1] = make_uint4(0, 0, 0, 0);
+          if constexpr (HR)
+            buf[jj][tk][0] = make_uint4(0, 0, 0, 0);
+          else
+            buf[jj][tk][0] = buf[jj][tk][1] = make_uint4(0, 0, 0, 0);
         }
       }
     }
@@ -370,28 +400,35 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
   auto issue_blind = [&](const Cur &c, int j0, Buf &buf) {
 #pragma unroll
     for (int tk = 0; tk < TPW; ++tk) {
-      const int t = c.tile * BN + warp * TPW + tk;
+      const int t = HR ? c.tile * UT + (warp >> 1) + tk : c.tile * BN + warp * TPW + tk;
       const int r0 = (layout == kRequestMajor) ? (t / p.q) * p.spr : 0;
       const uint16_t *base = p.o + off3(t, p.o_st, c.h, p.o_sh, r0 + j0, p.o_sp);
 #pragma unroll
       for (int jj = 0; jj < JB; ++jj) {
         if (j0 + jj < n && t < p.S) {
           const uint4 *row = reinterpret_cast<const uint4 *>(base + off1(jj, p.o_sp));
-          buf[jj][tk][0] = __ldcs(row + lane);
-          buf[jj][tk][1] = __ldcs(row + lane + 32);
+          if constexpr (HR) {
+            buf[jj][tk][0] = __ldcs(row + (warp & 1) * 32 + lane);
+          } else {
+            buf[jj][tk][0] = __ldcs(row + lane);
+            buf[jj][tk][1] = __ldcs(row + lane + 32);
+          }
         } else {
-          buf[jj][tk][0] = buf[jj][tk][1] = make_uint4(0, 0, 0, 0);
+          if constexpr (HR)
+            buf[jj][tk][0] = make_uint4(0, 0, 0, 0);
+          else
+            buf[jj][tk][0] = buf[jj][tk][1] = make_uint4(0, 0, 0, 0);
         }
       }
     }
   };
 
-  uint64_t acc[TPW][8];  // fp32 pairs: elements (2q, 2q+1) of chunk q/4
+  uint64_t acc[TPW][4 * NCH];  // fp32 pairs: elements (2q, 2q+1) of chunk q/4
   auto clear_acc = [&]() {
 #pragma unroll
     for (int tk = 0; tk < TPW; ++tk)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[tk][e] = 0ull;
+      for (int e = 0; e < 4 * NCH; ++e) acc[tk][e] = 0ull;
   };
 
   // Merge one batch in partial order: acc += w * o, one rounding per op.
@@ -403,7 +440,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
         if (w[jj][tk] == 0.0f) continue;
         const uint64_t w2 = f2_pack(w[jj][tk], w[jj][tk]);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < NCH; ++c) {
           const uint32_t uu[4] = {buf[jj][tk][c].x, buf[jj][tk][c].y, buf[jj][tk][c].z, buf[jj][tk][c].w};
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -524,10 +561,12 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
     uint8_t *gB = gB0 + (size_t)b * L.b_bytes;
 #pragma unroll
     for (int tk = 0; tk < TPW; ++tk) {
-      const bool valid = c.tile * BN + warp * TPW + tk < p.S;
-      const int row = warp * TPW + tk;
+      const bool valid = HR ? c.tile * UT + (warp >> 1) + tk < p.S : c.tile * BN + warp * TPW + tk < p.S;
+      const int row = HR ? (warp >> 1) + tk : warp * TPW + tk;
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
+      for (int cc = 0; cc < NCH; ++cc) {
+        // HR: this warp's half of the row (a 256-latent K block of MXFP4 codes)
+        const int kh = HR ? (warp & 1) : cc;
         uint4 x;
         if (pass) {
           x = raw_rows[0][tk][cc];
@@ -543,20 +582,20 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
         }
         if (WFMT == 0) {
           if (!valid) x = make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4 *>(gB + sw128_offset(row, lane + 32 * cc, BN)) = x;
+          *reinterpret_cast<uint4 *>(gB + sw128_offset(row, lane + 32 * kh, BN)) = x;
         } else {
-          // codes of elements 256cc + 8 lane .. +7: K block cc of the row,
-          // bytes 4 lane .. 4 lane + 3; the scale of block 8cc + lane/4
+          // codes of elements 256kh + 8 lane .. +7: K block kh of the row,
+          // bytes 4 lane .. 4 lane + 3; the scale of block 8kh + lane/4
           uint32_t sc;
           uint32_t w = mx_codes(x, sc);
           if (!valid) {
             w = 0u;
             sc = 127u;
           }
-          *reinterpret_cast<uint32_t *>(gB + cc * (BN * 128) + row * 128 + ((((lane >> 2) ^ (row & 7))) << 4) +
+          *reinterpret_cast<uint32_t *>(gB + kh * (BN * 128) + row * 128 + ((((lane >> 2) ^ (row & 7))) << 4) +
                                         4 * (lane & 3)) = w;
           if ((lane & 3) == 0) {
-            const int blk = 8 * cc + (lane >> 2);
+            const int blk = 8 * kh + (lane >> 2);
             gSFB0[(size_t)b * 2048 + (blk >> 2) * 512 + row * 16 + (blk & 3)] = (uint8_t)sc;
           }
         }
@@ -723,10 +762,13 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
       // the new unit's second batch into L2 (live rows): it is merged only
       // one batch after it is issued (large MXFP4 batch 291.4 -> 289.4 us;
       // bf16 prefetches whole units ahead instead)
-      const int t = cn.tile * BN + warp * TPW + my_tk;
+      const int t = HR ? cn.tile * UT + (warp >> 1) + my_tk : cn.tile * BN + warp * TPW + my_tk;
       if (my_j >= JB && my_j < 2 * JB && wnxt != 0.0f && t < p.S) {
         const int r0 = (layout == kRequestMajor) ? (t / p.q) * p.spr : 0;
-        prefetch_l2_bulk(p.o + off3(t, p.o_st, cn.h, p.o_sh, r0 + my_j, p.o_sp), kD * 2);
+        if constexpr (HR)  // this warp's half of the row
+          prefetch_l2_bulk(p.o + off3(t, p.o_st, cn.h, p.o_sh, r0 + my_j, p.o_sp) + (warp & 1) * (kD / 2), kD);
+        else
+          prefetch_l2_bulk(p.o + off3(t, p.o_st, cn.h, p.o_sh, r0 + my_j, p.o_sp), kD * 2);
       }
     }
   };
@@ -831,19 +873,21 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
 // Warps per CTA: 16, except MXFP4 W_V with 16-token tiles and at most 16
 // partials per token, which runs two 8-warp CTAs per SM (about 60 KiB of
 // shared memory each, independent pipelines).  A warp owns BN / warps tokens;
-// with two tokens a warp holds at most 16 partials per token.
+// with two tokens a warp holds at most 16 partials per token.  8-token tiles
+// are the half-row instance of the 16-token kernel: 16 warps, two per token.
 int tc_warps(int tile, int w_fmt, int n_part) { return (w_fmt && tile == 16 && n_part <= 16) ? 8 : 16; }
 int tc_ctas_per_sm(int tile, int w_fmt, int n_part) { return tc_warps(tile, w_fmt, n_part) == 8 ? 2 : 1; }
-int tc_max_part(int tile, int /*w_fmt*/) { return tile == 16 ? 32 : 16; }
+int tc_max_part(int tile, int /*w_fmt*/) { return tile == 32 ? 16 : 32; }
 
 size_t tc_smem_bytes(int tile, int w_fmt, int n_part) {
-  return 1024 + tc_layout(tile, w_fmt, tc_warps(tile, w_fmt, n_part)).total;
+  const int bn = tile == 8 ? 16 : tile;
+  return 1024 + tc_layout(bn, w_fmt, tc_warps(tile, w_fmt, n_part)).total;
 }
 
-template <int BN, int WFMT, int NW, bool O32>
+template <int BN, int WFMT, int NW, bool O32, bool HR = false>
 static cudaError_t launch_one(const KParams &p, int grid, cudaStream_t s) {
   const size_t smem = 1024 + tc_layout(BN, WFMT, NW).total;
-  cudaError_t e = cudaFuncSetAttribute(tc_kernel<BN, WFMT, NW, O32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(tc_kernel<BN, WFMT, NW, O32, HR>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
@@ -856,7 +900,7 @@ static cudaError_t launch_one(const KParams &p, int grid, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, tc_kernel<BN, WFMT, NW, O32>, p);
+  e = cudaLaunchKernelEx(&cfg, tc_kernel<BN, WFMT, NW, O32, HR>, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -864,6 +908,9 @@ static cudaError_t launch_one(const KParams &p, int grid, cudaStream_t s) {
 template <bool O32>
 static cudaError_t launch_tc_off(const KParams &p, int grid, cudaStream_t stream) {
   const int nw = tc_warps(p.tile, p.w_fmt, p.n_part);
+  if (p.tile == 8)
+    return p.w_fmt == 0 ? launch_one<16, 0, 16, O32, true>(p, grid, stream)
+                        : launch_one<16, 1, 16, O32, true>(p, grid, stream);
   if (p.tile == 16 && p.w_fmt == 0) return launch_one<16, 0, 16, O32>(p, grid, stream);
   if (p.tile == 16 && p.w_fmt == 1)
     return nw == 8 ? launch_one<16, 1, 8, O32>(p, grid, stream) : launch_one<16, 1, 16, O32>(p, grid, stream);

@@ -12,7 +12,7 @@ namespace mla {
 size_t simt_smem_bytes(int n_part);
 cudaError_t launch_simt(const KParams &p, cudaStream_t stream);
 
-// Fused tcgen05 kernel: tile = 16 or 32 tokens, n_part <= 32.
+// Fused tcgen05 kernel: tile = 8, 16 or 32 tokens, n_part <= 32 (16 for 32-token tiles).
 constexpr int kTcMaxPart = 32;
 int tc_warps(int tile, int w_fmt, int n_part);        // warps per CTA
 int tc_ctas_per_sm(int tile, int w_fmt, int n_part);  // resident CTAs per SM the grid is sized for

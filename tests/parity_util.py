@@ -84,12 +84,14 @@ def compare(gpu_bits, ref_bits, zero_mask_rows=None, what=""):
     assert g.shape == r.shape
     nan_r, nan_g = np.isnan(r), np.isnan(g)
     assert np.array_equal(nan_r, nan_g), f"{what}: NaN positions differ ({nan_g.sum()} vs {nan_r.sum()})"
-    ok = ~nan_r
+    inf_r, inf_g = np.isinf(r), np.isinf(g)
+    assert np.array_equal(inf_r, inf_g) and np.array_equal(r[inf_r], g[inf_g]), f"{what}: infinities differ"
+    ok = ~(nan_r | inf_r)
     err = np.abs(g[ok] - r[ok])
     bound = ATOL + RTOL * np.abs(r[ok])
     bad = err > bound
     if bad.any():
-        idx = np.argwhere(~nan_r)[np.argmax(err - bound)]
+        idx = np.argwhere(ok)[np.argmax(err - bound)]
         raise AssertionError(f"{what}: {bad.sum()} elements out of tolerance; worst at {tuple(idx)}: "
                              f"gpu {g[tuple(idx)]} oracle {r[tuple(idx)]}")
     if zero_mask_rows is not None:

@@ -43,7 +43,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert m.mla_abi_version() == 3
+    assert m.mla_abi_version() == 4
     for s in range(0, 11):
         assert m.mla_status_str(s) and m.mla_status_str(s) != "unknown status"
     assert m.mla_status_str(99) == "unknown status"
@@ -255,12 +255,27 @@ def test_layouts(lib):
 
 def test_kernel_and_tile_choice(lib):
     # even tiny token counts run on the persistent tensor-core kernel (a
-    # 16-token tile, mostly empty); decode sizes: 16-token tiles when 32 would
-    # not fill the GPU
+    # 16-token tile, mostly empty); split-KV decode sizes with bf16 W_V and
+    # 16+ partials: 8-token tiles (two warps per token) while those give each
+    # unit its own SM, else 16-token tiles when 32 would not fill the GPU
     p = mla_combine_uv_plan(args(S=4, H=2, P=4, q=2, spr=2), SMS)
     assert (p["kernel"], p["tile_tokens"], p["units"]) == (m.MLA_KERNEL_TC, 16, 2)
     p = mla_combine_uv_plan(args(S=64, P=16, spr=16), SMS)
-    assert (p["kernel"], p["tile_tokens"], p["units"], p["grid"]) == (m.MLA_KERNEL_TC, 16, 48, 48)
+    assert (p["kernel"], p["tile_tokens"], p["units"], p["grid"], p["threads"]) == (m.MLA_KERNEL_TC, 8, 96, 96, 512)
+    assert p["smem_bytes"] <= 227 * 1024
+    p = mla_combine_uv_plan(args(S=64, P=1, spr=0), SMS)  # one partial: 16-token tiles
+    assert (p["tile_tokens"], p["units"]) == (16, 48)
+    p = mla_combine_uv_plan(args(S=64, P=8, spr=8), SMS)  # fewer than 16 partials: 16-token tiles
+    assert (p["tile_tokens"], p["units"]) == (16, 48)
+    p = mla_combine_uv_plan(args(S=64, P=16, spr=16, w_fmt=1), SMS)  # MXFP4: 8-token tiles on request only
+    assert (p["tile_tokens"], p["units"], p["threads"]) == (16, 48, 256)
+    p = mla_combine_uv_plan(args(S=64, P=16, spr=16, w_fmt=1, tile=8), SMS)
+    assert (p["tile_tokens"], p["units"], p["threads"]) == (8, 96, 512)
+    p = mla_combine_uv_plan(args(S=128, P=16, spr=16), SMS)  # 192 8-token units > SMS: 16-token tiles
+    assert (p["tile_tokens"], p["units"]) == (16, 96)
+    p = mla_combine_uv_plan(args(S=64, P=32, spr=32, tile=8), SMS)
+    assert (p["tile_tokens"], p["n_part"]) == (8, 32)
+    assert status_of(args(S=64, P=33, spr=33, kernel=m.MLA_KERNEL_TC, tile=8)) == m.MLA_ERR_KERNEL
     # the cluster kernel on request: 4 CTAs of 256 threads per 16-token unit
     p = mla_combine_uv_plan(args(S=64, P=16, spr=16, kernel=m.MLA_KERNEL_KSPLIT), SMS)
     assert (p["kernel"], p["tile_tokens"], p["units"], p["grid"], p["threads"]) == (m.MLA_KERNEL_KSPLIT, 16, 48, 192, 256)
@@ -269,6 +284,7 @@ def test_kernel_and_tile_choice(lib):
     assert p["smem_bytes"] <= 227 * 1024
     assert status_of(args(S=64, P=20, spr=20, kernel=m.MLA_KERNEL_KSPLIT)) == m.MLA_ERR_KERNEL
     assert status_of(args(S=64, kernel=m.MLA_KERNEL_KSPLIT, tile=32)) == m.MLA_ERR_KERNEL
+    assert status_of(args(S=64, kernel=m.MLA_KERNEL_KSPLIT, tile=8)) == m.MLA_ERR_KERNEL
     assert status_of(args(S=0, S_out=4, kernel=m.MLA_KERNEL_KSPLIT)) == m.MLA_ERR_KERNEL
     # the large batch: 32-token tiles over a persistent grid of SMS CTAs
     p = mla_combine_uv_plan(args(S=4096, H=96, P=4, q=4, spr=4), SMS)

@@ -80,6 +80,19 @@ def test_fuzz_combine(lib, orc, case):
     compare(gpu, ref, seg_mask(inp), f"fuzz {case}: {c}")
 
 
+@pytest.mark.parametrize("case", range(16))
+def test_fuzz_combine_eight_token_tiles(lib, orc, case):
+    # the half-row instance (two warps per token) on random problems
+    rng = np.random.default_rng(3000 + case)
+    c = draw_case(rng)  # at most 16 partials per token
+    c["kernel"], c["tile"] = TC, 8
+    inp = make_case(c)
+    gpu, canary = run_gpu(inp, kernel=TC, tile=8)
+    assert np.all(canary == CANARY), c
+    ref = oracle_problem(orc, inp).full()
+    compare(gpu, ref, seg_mask(inp), f"fuzz 8-token tiles {case}: {c}")
+
+
 @pytest.mark.parametrize("case", range(12))
 def test_fuzz_pack(lib, orc, case):
     import mla_decode_attention_lse_gb300 as m

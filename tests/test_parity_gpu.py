@@ -51,6 +51,10 @@ CASES = [
     ("stacked_mxfp4", TC, 32),
     ("tiny_split", KS, 0), ("nosplit", KS, 0), ("splitkv", KS, 0), ("splitkv_rm", KS, 0),
     ("stacked_mxfp4", KS, 0),
+    # 8-token tiles (two warps per token, half a row each): the automatic
+    # choice for the bf16 split-KV decode steps, on request elsewhere
+    ("nosplit", 0, 0), ("tiny_split", TC, 8), ("nosplit", TC, 8), ("splitkv", TC, 8), ("splitkv", TC, 16),
+    ("splitkv_rm", TC, 8), ("stacked_mxfp4", TC, 8),
 ]
 
 
@@ -227,3 +231,50 @@ def test_wide_offsets_take_the_64_bit_path(lib, orc, w_fmt):
     finally:
         del big
         torch.cuda.empty_cache()
+
+
+# ---- 8-token tiles: two warps per token, each merging half of the row ------
+
+@pytest.mark.parametrize("w_fmt", [0, 1])
+@pytest.mark.parametrize("S,S_out,P,q,spr", [
+    (1, 1, 3, 1, 3),        # one token
+    (7, 9, 7, 1, 7),        # one batch per unit, padded rows
+    (9, 9, 16, 1, 16),      # two batches per unit, a ragged second tile
+    (47, 50, 1, 1, 0),      # passthrough
+    (18, 18, 30, 3, 5),     # request-major, q = 3
+    (24, 26, 24, 1, 24),    # three batches per unit
+    (40, 40, 32, 1, 32),    # 32 partials: four batches per unit
+])
+def test_eight_token_tiles(lib, orc, w_fmt, S, S_out, P, q, spr):
+    pas = P == 1
+    inp = custom(S=S, S_out=S_out, H=3, P=P, q=q, spr=spr, w_fmt=w_fmt, neg_inf_frac=0.0 if pas else 0.2,
+                 nan_frac=0.0 if pas else 0.05, lse_unused=pas, seed=100 + S + P + w_fmt)
+    if not pas:  # dead partials' rows poisoned: they must never be read
+        inp["o"][~torch.isfinite(inp["lse"])] = float("nan")
+    check_full(orc, inp, TC, 8, f"8-token tiles S={S} P={P} w_fmt={w_fmt}")
+
+
+@pytest.mark.parametrize("w_fmt", [0, 1])
+def test_eight_token_tiles_dead_rows_strided_heads(lib, orc, w_fmt):
+    s = synth()
+    # all-dead rows with NaN planted in the dead partials
+    inp = custom(S=32, H=4, P=4, q=1, spr=4, w_fmt=w_fmt, dead_rows=10, neg_inf_frac=0.3, seed=70 + w_fmt)
+    inp["o"][~torch.isfinite(inp["lse"])] = float("nan")
+    check_full(orc, inp, TC, 8, "8-token tiles, planted NaN")
+    # strided o / lse / W_V views
+    base = s.custom(S=40, H=6, P=3, q=1, spr=3, w_fmt=0, seed=80, device="cuda")
+    big = torch.randn(3, 40, 10, 512, device="cuda").to(torch.bfloat16)
+    big[:, :, 2:8] = base["o"]
+    lse_big = torch.randn(40, 6, 3, device="cuda")
+    lse_big.copy_(base["lse"].permute(1, 2, 0))
+    wbig = torch.zeros(6, 256, 512, dtype=torch.bfloat16, device="cuda")
+    wbig[:, ::2] = base["w_v"]
+    inp = dict(base, o=big[:, :, 2:8], lse=lse_big.permute(2, 0, 1), w_v=wbig[:, ::2])
+    check_full(orc, inp, TC, 8, "8-token tiles, strided")
+    # more units than SMs: CTAs walk across head boundaries
+    inp = custom(S=400, H=12, P=2, q=1, spr=2, w_fmt=w_fmt, neg_inf_frac=0.05, seed=90 + w_fmt)
+    check_full(orc, inp, TC, 8, f"8-token tiles, head changes w_fmt={w_fmt}")
+    # an Inf latent in the passthrough (its MX block's scale is NaN)
+    inp = custom(S=16, H=2, P=1, q=1, spr=0, w_fmt=w_fmt, lse_unused=True, seed=95)
+    inp["o"][0, 3, 1, 300] = float("inf")
+    check_full(orc, inp, TC, 8, "8-token tiles, inf latent")
