@@ -1161,7 +1161,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA cores, 2 tensor cores (persistent), "
                     "3 tensor cores with the latents split over a 4-CTA cluster")
-    ap.add_argument("--tile", type=int, default=0, help="tensor-core token tile (16/32; 0 auto)")
+    ap.add_argument("--tile", type=int, default=0, help="tensor-core token tile (8/16/32; 0 auto)")
     ap.add_argument("--rotate", type=int, default=0,
                     help="independent input copies cycled per step (0: enough to exceed L2)")
     ap.add_argument("--graph", action=argparse.BooleanOptionalAction, default=None,
