@@ -15,7 +15,7 @@
  * partials in index order, K in ascending order, one rounding per operation
  * (this file is compiled with -ffp-contract=off so no multiply-add is fused).
  *
- * Readings taken where the page is silent (each also listed in the design doc):
+ * Readings taken where the page is silent:
  *  - LSE is a natural log: weights are exp2((lse - m) * log2(e)).
  *  - exp2 is the C library's exp2f; the reciprocal is a true division.
  *  - bf16 rounding is round-to-nearest-even.
@@ -328,8 +328,7 @@ int orc_dcp_pack(const orc_pack_args *a, uint16_t *cmb_o, float *cmb_lse) {
  * The page names the producer of the split partials (M1c, mla_attn: o / lse
  * of dense [splits, S, 12, 512] bf16 / [splits, S, 12] f32) but does not
  * print it, so this is the plain definition of MLA decode attention in the
- * absorbed form, split over the KV positions (flash decoding).  Readings
- * (also in the design doc):
+ * absorbed form, split over the KV positions (flash decoding).  Readings:
  *  - a query row is 576 wide: the latent query (512, W_UK already absorbed)
  *    then the rope query (64); a cached row is the latent (512) then the
  *    rope key (64); the score is scale * (q . row) over all 576, and the
