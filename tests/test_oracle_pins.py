@@ -137,6 +137,48 @@ def test_mx_scale_puts_amax_in_top_binade(orc):
     assert orc.mx_scale_code(tiny) == 1
 
 
+def test_e8m0_values_follow_the_ocp_encoding(orc):
+    # OCP MX v1.0: an E8M0 scale is 2^(code - 127) for codes 0..254; 0xFF is NaN
+    for code in (0, 1, 100, 127, 128, 200, 254):
+        assert orc.e8m0_value(code) == 2.0 ** (code - 127)
+    assert math.isnan(orc.e8m0_value(255))
+
+
+def test_mx_nonfinite_block_scale_is_nan(orc):
+    # a block whose amax is Inf or NaN has no finite scale: its code is the
+    # E8M0 NaN (0xFF), so every element of that block dequantises to NaN; the
+    # largest finite bf16 still gets a finite code (floor(log2 amax) = 127)
+    for bad in (np.inf, -np.inf, np.nan):
+        vals = np.linspace(-3.0, 3.0, BLK)
+        vals[7] = bad
+        blk = to_bf16_bits(vals)
+        assert orc.mx_scale_code(blk) == 255
+        _, sc = orc.mx_quant_block(blk)
+        assert sc == 255
+    big = np.zeros(BLK)
+    big[0] = 3.3895314e38
+    assert orc.mx_scale_code(to_bf16_bits(big)) == 127 - 2 + 127
+
+
+def test_mxfp4_inf_latent_poisons_only_its_row(orc):
+    # one passthrough latent is +inf: its MX block's scale is NaN, so every
+    # output of that (token, head) is NaN (each sums over all 512 latents);
+    # every other row stays finite
+    from mla_decode_attention_lse_gb300 import synth
+
+    rng = np.random.default_rng(21)
+    S, H = 3, 2
+    of = rng.standard_normal((1, S, H, D))
+    of[0, 1, 0, 300] = np.inf
+    wf = torch.from_numpy(rng.standard_normal((H, V, D)) / math.sqrt(D)).float()
+    codes, scales = (t.numpy() for t in synth.mxfp4_pack_weights(wf))
+    out = bits_to_f32(problem(orc, of, spr=0, w=codes, w_scale=scales, w_fmt=1).full()).reshape(S, H, V)
+    assert np.all(np.isnan(out[1, 0]))
+    keep = np.ones((S, H), bool)
+    keep[1, 0] = False
+    assert np.all(np.isfinite(out[keep]))
+
+
 # ---- layout rule ------------------------------------------------------------
 
 def test_partial_set_layouts(orc):
