@@ -366,3 +366,55 @@ def test_make_args_from_strided_views(lib):
     assert a.o == o.data_ptr()
     p = mla_combine_uv_plan(a, SMS)
     assert p["layout"] == 1
+
+
+def test_plan_invariants_on_random_problems(lib):
+    """Seeded random problems through the planner: every call either returns
+    one of the documented errors or a plan whose launch respects the kernel
+    limits (units cover every token, grid no larger than units or resident
+    CTAs, shared memory within 227 KB, 32-token tiles only up to 16 partials,
+    automatic 8-token tiles only where documented)."""
+    import numpy as np
+
+    rng = np.random.default_rng(77)
+    errors = {m.MLA_ERR_LAYOUT, m.MLA_ERR_KERNEL, m.MLA_ERR_SHAPE}
+    seen = set()
+    for _ in range(3000):
+        q = int(rng.choice([1, 2, 3, 4]))
+        S = int(rng.integers(0, 80)) * q if rng.random() < 0.8 else int(rng.integers(0, 5000))
+        H = int(rng.choice([1, 2, 3, 12, 96, 128]))
+        layout = rng.choice(["pass", "compact", "request_major", "bad"])
+        spr = int(rng.integers(1, 48))
+        P = {"pass": 1, "compact": spr, "request_major": max(1, S // q) * spr,
+             "bad": spr + 1}[layout]
+        if layout == "pass":
+            spr = 0
+        w_fmt = int(rng.integers(0, 2))
+        kernel = int(rng.choice([0, 0, m.MLA_KERNEL_SIMT, m.MLA_KERNEL_TC, m.MLA_KERNEL_KSPLIT]))
+        tile = int(rng.choice([0, 0, 8, 16, 32]))
+        a = args(S=S, S_out=S + int(rng.integers(0, 4)), H=H, P=P, q=q, spr=spr, w_fmt=w_fmt,
+                 kernel=kernel, tile=tile)
+        try:
+            p = mla_combine_uv_plan(a, SMS)
+        except MlaError as e:
+            assert e.status in errors, (e.status, S, H, P, q, spr, kernel, tile)
+            continue
+        n = p["n_part"]
+        seen.add((p["kernel"], p["tile_tokens"]))
+        assert p["smem_bytes"] <= 227 * 1024
+        if p["kernel"] == m.MLA_KERNEL_TC:
+            t = p["tile_tokens"]
+            assert t in (8, 16, 32) and (tile == 0 or t == tile)
+            assert p["units"] == H * -(-S // t) and 1 <= p["grid"] <= min(p["units"], 2 * SMS)
+            assert n <= (16 if t == 32 else 32)
+            assert p["threads"] == (256 if (w_fmt and t == 16 and n <= 16) else 512)
+            if tile == 0 and t == 8:
+                assert w_fmt == 0 and n >= 16 and H * -(-S // 8) <= SMS
+        elif p["kernel"] == m.MLA_KERNEL_KSPLIT:
+            assert p["tile_tokens"] == 16 and n <= 16 and p["grid"] == 4 * p["units"]
+        else:
+            assert p["kernel"] == m.MLA_KERNEL_SIMT and p["grid"] == p["units"]
+    # the random draws reached every kernel and every tensor-core tile
+    assert {(m.MLA_KERNEL_TC, 8), (m.MLA_KERNEL_TC, 16), (m.MLA_KERNEL_TC, 32),
+            (m.MLA_KERNEL_KSPLIT, 16)} <= seen
+    assert any(k == m.MLA_KERNEL_SIMT for k, _ in seen)
