@@ -37,6 +37,13 @@ DEFAULT_WORKLOAD = "mtp_mxfp4"
 L2_DEFEAT_BYTES = 256 << 20  # working set per rotation, about twice the 129 MB L2
 
 
+# nominal figures, for the labelled second fraction only (the measured peaks
+# are the denominators of `frac`)
+NOMINAL_HBM_GBS = 7900.0            # HBM3e, nominal
+NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25  # dense tensor-core rates, nominal
+DECODE_WORKLOADS = ("tiny_split", "nosplit", "splitkv", "splitkv_rm", "stacked_mxfp4")
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -44,6 +51,22 @@ def load_peaks():
             d = json.load(f)
         return d.get("hbm_gbs", 6800.0), "measured"
     return 6800.0, "fallback"
+
+
+def tensor_peak(w_fmt: int):
+    """(TFLOP/s, description) of the tensor-core peak for the W_UV contraction
+    of a W_V format: the measured bf16 burst rate, times the nominal FP4:bf16
+    ratio for MXFP4."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    bf16, src = 1900.0, "fallback bf16 1900 TFLOP/s"
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if "bf16_tflops" in d:
+            bf16, src = d["bf16_tflops"], f"measured bf16 {d['bf16_tflops']} TFLOP/s (burst)"
+    if w_fmt == 1:
+        return bf16 * NOMINAL_FP4_OVER_BF16, f"{src} x {NOMINAL_FP4_OVER_BF16:g} (nominal FP4:bf16 ratio)"
+    return bf16, src
 
 
 # the source file of each kernel named in a bench line; the shared headers
@@ -225,12 +248,9 @@ def oracle_sample_rate(inp, budget_s: float, rows_hint: int | None = None):
     workload's (t, h) rows; returns (tokens/s, rows timed, seconds)."""
     import numpy as np
 
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
     import oracle
-    from parity_util import host_inputs, oracle_problem
 
-    host = host_inputs(inp)
-    pr = oracle_problem(oracle, inp, host)
+    pr = oracle.problem_from_tensors(inp)
     rng = np.random.default_rng(0)
     S, H = inp["S"], inp["H"]
     # calibrate on a few rows, then size the sample to the budget
@@ -393,34 +413,18 @@ def run_gpu(args):
     avg_kern_s = statistics.mean(kern_ms) / 1e3
     peak, peak_kind = load_peaks()
     achieved = nbytes / avg_kern_s / 1e9
+    nbytes_all = synth.algorithmic_bytes_all_rows(inp)
+    tflops = synth.flops(inp) / avg_kern_s / 1e12
+    tpeak, tpeak_src = tensor_peak(inp["w_fmt"])
 
-    # end to end: pinned host inputs -> device, the call, output -> host
-    pin = host_copy_inputs(inp)
-    out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    dev_bufs = {k: torch.empty_like(inp[k]) for k in pin}
+    # end to end: pinned host inputs -> device, the call, output -> host, with
+    # the copies of step i+1 overlapping the call and read-back of step i
     e2e_steps = max(3, min(args.steps, 20))
-
-    def e2e_step():
-        for k in pin:
-            dev_bufs[k].copy_(pin[k], non_blocking=True)
-        m.mla_combine_uv(dev_bufs["o"], dev_bufs.get("lse"), inp["q"], inp["spr"], inp["w_v"],
-                         inp["w_fmt"], dev_bufs["gate"], out, w_scale=inp["w_scale"], stream=stream,
-                         kernel=args.kernel, tile_tokens=args.tile)
-        out_host.copy_(out, non_blocking=True)
-
-    e2e_step()
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_value = replica_rate(S, e2e_steps, ws, reduce_max(e0.elapsed_time(e1), dist, dev))
-    h2d = sum(t.numel() * t.element_size() for t in pin.values())
-    d2h = out_host.numel() * out_host.element_size()
+    e2e_ms, h2d, d2h = e2e_overlapped(m, inp, out.shape, args, stream, dev, e2e_steps, dist)
+    e2e_value = replica_rate(S, e2e_steps, ws, e2e_ms)
+    decode = None
+    if args.workload == DEFAULT_WORKLOAD and ws == 1 and not args.no_decode:
+        decode = decode_leg(m, synth, dev, stream, args.decode_launches)
 
     line = None
     if rank == 0:
@@ -435,7 +439,8 @@ def run_gpu(args):
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "mxfp4" if inp["w_fmt"] else "bf16",
             "data": "synthetic",
             "config": {"workload": f"{args.workload}: {wl.S // wl.q} requests x q={wl.q} "
                                    f"(S={S}), H={H}, {inp['spr']} splits per request, "
@@ -456,23 +461,174 @@ def run_gpu(args):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,
                          "traffic": traffic_from_profile(args.workload, kname),
-                         "algorithmic_bytes": nbytes},
-            "tensor": {"tflops": synth.flops(inp) / avg_kern_s / 1e12},
+                         "algorithmic_bytes": nbytes,
+                         "algorithmic_bytes_note": "partial rows with a finite LSE (the rows that can "
+                                                   "carry weight) + LSE + W_V + gate + out",
+                         "algorithmic_bytes_all_rows": nbytes_all,
+                         "frac_all_rows": nbytes_all / avg_kern_s / 1e9 / peak,
+                         "nominal": {"peak": NOMINAL_HBM_GBS, "unit": "GB/s", "frac": achieved / NOMINAL_HBM_GBS,
+                                     "peak_source": "nominal HBM3e 7.9 TB/s"}},
+            "tensor": {"tflops": tflops, "peak": tpeak, "frac": tflops / tpeak, "peak_source": tpeak_src},
             "kernel_ms": {"mean": statistics.mean(kern_ms), "min": min(kern_ms),
                           "max": max(kern_ms)},
             "cold_launch_us": cold_us,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps,
+                    "link_h2d_gbs": h2d * e2e_steps / (e2e_ms / 1e3) / 1e9,
+                    "copies": "double-buffered: step i+1's host->device copy (its own stream) overlaps "
+                              "step i's call and its device->host read-back (a third stream)"},
             "gpu_launches": args.steps,
             "clocks": clocks,
             "wall_s": t_wall,
         }
+        if decode is not None:
+            line["decode"] = decode
         print(json.dumps(line), flush=True)
     if dist:
         dist.barrier()
         dist.destroy_process_group()
     return line
+
+
+def e2e_overlapped(m, inp, out_shape, args, stream, dev, steps, dist):
+    """Time `steps` end-to-end calls: each step copies its inputs from pinned
+    host memory, calls the stage and reads the output back.  Two device input
+    / output sets alternate, so the host->device copy of step i+1 (on its own
+    stream) overlaps the call of step i and its read-back (a third stream).
+    Returns (ms for all steps, max over ranks; h2d bytes per step; d2h bytes
+    per step)."""
+    import torch
+
+    pin = host_copy_inputs(inp)
+    outs_host = [torch.empty(tuple(out_shape), dtype=torch.bfloat16, pin_memory=True) for _ in range(2)]
+    bufs = [{k: torch.empty_like(inp[k]) for k in pin} for _ in range(2)]
+    outs = [torch.empty(tuple(out_shape), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    cs_in, cs_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    comp_done, d2h_done = [None, None], [None, None]
+
+    def step(i):
+        b = i % 2
+        if comp_done[b] is not None:  # the call of step i-2 has read set b
+            cs_in.wait_event(comp_done[b])
+        with torch.cuda.stream(cs_in):
+            for k in pin:
+                bufs[b][k].copy_(pin[k], non_blocking=True)
+        h = torch.cuda.Event()
+        h.record(cs_in)
+        stream.wait_event(h)
+        if d2h_done[b] is not None:  # out[b] of step i-2 has been read back
+            stream.wait_event(d2h_done[b])
+        m.mla_combine_uv(bufs[b]["o"], bufs[b].get("lse"), inp["q"], inp["spr"], inp["w_v"], inp["w_fmt"],
+                         bufs[b]["gate"], outs[b], w_scale=inp["w_scale"], stream=stream, kernel=args.kernel,
+                         tile_tokens=args.tile)
+        c = torch.cuda.Event()
+        c.record(stream)
+        comp_done[b] = c
+        cs_out.wait_event(c)
+        with torch.cuda.stream(cs_out):
+            outs_host[b].copy_(outs[b], non_blocking=True)
+        d = torch.cuda.Event()
+        d.record(cs_out)
+        d2h_done[b] = d
+
+    for i in range(2):
+        step(i)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    cs_in.wait_event(e0)
+    for i in range(steps):
+        step(i)
+    for d in d2h_done:
+        stream.wait_event(d)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert m.mla_combine_uv_status(stream) == m.MLA_OK
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = outs_host[0].numel() * outs_host[0].element_size()
+    return reduce_max(e0.elapsed_time(e1), dist, dev), h2d, d2h
+
+
+def decode_leg(m, synth, dev, stream, launches):
+    """The decode-shaped workloads, each timed like the headline's small
+    cases: `launches` back-to-back calls captured in one CUDA graph over enough
+    independent input copies (W_V included) that every launch reads HBM; and,
+    in the same harness, the read-only streaming kernel reading the same byte
+    count from a rotation of the same size (0 and 1 dependent round trips
+    first) -- the fastest any single launch of that size can be -- plus the
+    floor of a chain of launches that read almost nothing."""
+    import torch
+
+    peak, peak_kind = load_peaks()
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def graph_time(fn):
+        fn(0)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        with torch.cuda.graph(g, stream=cap):
+            for k in range(launches):
+                fn(k)
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        del g
+        return e0.elapsed_time(e1) * 1e3 / launches  # us per launch
+
+    def calib_us(nbytes, rot, trips):
+        n16 = -(-nbytes // 16) * 16
+        buf = torch.randn(rot * n16 // 4, device=dev)  # finite data
+        us = graph_time(lambda k: m.mla_calib_stream_read(buf[(k % rot) * n16 // 4:], n16, trips, sink))
+        del buf
+        return us
+
+    out = {"launches_per_graph": launches, "peak": peak, "peak_source": peak_kind,
+           "nominal_peak": NOMINAL_HBM_GBS, "workloads": {}}
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        tiny = torch.zeros(1 << 10, dtype=torch.float32, device=dev)
+        out["launch_floor_us"] = graph_time(lambda k: m.mla_calib_stream_read(tiny, 64, 0, sink))
+        for name in DECODE_WORKLOADS:
+            wl = synth.WORKLOADS[name]
+            inp = synth.make(name, device=dev, seed=wl.seed)
+            nb = synth.algorithmic_bytes(inp)
+            nb_all = synth.algorithmic_bytes_all_rows(inp)
+            rot = -(-L2_DEFEAT_BYTES // nb)
+            copies = [inp] + [synth.make(name, device=dev, seed=wl.seed + 1000 * k) for k in range(1, rot)]
+            outs = [torch.empty(inp["S_out"], inp["H"] * 128, dtype=torch.bfloat16, device=dev) for _ in range(rot)]
+
+            def call(k):
+                c = copies[k % rot]
+                m.mla_combine_uv(c["o"], c["lse"], c["q"], c["spr"], c["w_v"], c["w_fmt"], c["gate"],
+                                 outs[k % rot], w_scale=c["w_scale"])
+
+            a = m.make_args(inp["o"], inp["lse"], inp["q"], inp["spr"], inp["w_v"], inp["w_fmt"], inp["gate"],
+                            outs[0], inp["w_scale"])
+            plan = m.mla_combine_uv_plan(a)
+            us = graph_time(call)
+            assert m.mla_combine_uv_status(stream) == m.MLA_OK
+            del copies, outs
+            torch.cuda.empty_cache()
+            c0 = calib_us(nb, rot, 0)
+            c1 = calib_us(nb, rot, 1)
+            gbs = nb / (us / 1e6) / 1e9
+            out["workloads"][name] = {
+                "us_per_launch": us, "algorithmic_bytes": nb, "algorithmic_bytes_all_rows": nb_all,
+                "gbs": gbs, "frac": gbs / peak, "frac_all_rows": nb_all / (us / 1e6) / 1e9 / peak,
+                "frac_nominal": gbs / NOMINAL_HBM_GBS,
+                "ceiling_us": c0, "ceiling_dep1_us": c1, "ceiling_frac": nb / (c0 / 1e6) / 1e9 / peak,
+                "of_ceiling": c0 / us, "rotation": rot,
+                "kernel": {m.MLA_KERNEL_TC: "tc", m.MLA_KERNEL_KSPLIT: "tc_ksplit_cluster4"}.get(
+                    plan["kernel"], "simt"), "tile_tokens": plan["tile_tokens"], "grid": plan["grid"]}
+    out["clocks"] = clk.summary()
+    return out
 
 
 def dcp_oracle_rate(host, budget_s: float):
@@ -481,7 +637,6 @@ def dcp_oracle_rate(host, budget_s: float):
     (tokens/s, description)."""
     import numpy as np
 
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
     import oracle
 
     import torch
@@ -683,7 +838,7 @@ def run_gpu_dcp(args):
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4" if inp["w_fmt"] else "bf16",
             "data": "synthetic",
             "config": {"workload": f"{args.workload}: decode context parallelism over {R} ranks x {H} heads "
                                    f"({R * H} global), S={S} rows ({live} live by qsl), q={q}; one step = "
@@ -726,7 +881,6 @@ def attn_oracle_rate(host, budget_s: float):
     Returns (tokens/s, description)."""
     import numpy as np
 
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
     import oracle
 
     import torch
@@ -975,7 +1129,6 @@ def oproj_oracle_rate(host, budget_s: float):
     each), scaled to the call.  Returns (tokens/s, description)."""
     import numpy as np
 
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
     import oracle
 
     import torch
@@ -1166,6 +1319,10 @@ def main():
                     help="independent input copies cycled per step (0: enough to exceed L2)")
     ap.add_argument("--graph", action=argparse.BooleanOptionalAction, default=None,
                     help="capture the timed steps in a CUDA graph (default: for workloads under L2 size)")
+    ap.add_argument("--no-decode", action="store_true",
+                    help="skip the decode-size leg of the default line")
+    ap.add_argument("--decode-launches", type=int, default=1000,
+                    help="launches per CUDA graph in the decode-size leg")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define MLA_ABI_VERSION 4
+#define MLA_ABI_VERSION 5
 
 /* W_V storage format. */
 enum {
@@ -124,6 +124,27 @@ typedef struct {
   int32_t tile_tokens;        /* tensor-core token tile (8, 16 or 32; 8 added
                                  in ABI version 4: two warps per token, each
                                  merging half of its latents); 0 = auto      */
+  int64_t wait_ns;            /* limit of the tensor-core kernel's bounded
+                                 waits, in ns; 0 = the default 0.5 s.  A wait
+                                 that runs out makes the kernel stop, drain its
+                                 own copies and MMAs (those drains keep the
+                                 default limit), free TMEM and return;
+                                 mla_combine_uv_status then reports
+                                 MLA_ERR_TIMEOUT and `out` is undefined.  The
+                                 other kernels use the default.  (Added in ABI
+                                 version 5.)                                  */
+  const int32_t *ready_flag;  /* optional device int32 (NULL: none).  The
+                                 producer's completion flag of the page's
+                                 flag handshake (the combine polls the flags
+                                 its producer raises once the partials are
+                                 written): every CTA waits, bounded by wait_ns,
+                                 until the value is non-zero before it reads
+                                 o, lse or gate.  A flag still zero when the
+                                 limit runs out ends the call with
+                                 MLA_ERR_TIMEOUT.  The producer must not be a
+                                 kernel that itself waits for this call.
+                                 Tensor-core kernel only (other kernels:
+                                 MLA_ERR_KERNEL).  (Added in ABI version 5.) */
 } mla_combine_uv_args;
 
 /* What a call would launch (host-side planning only). */
@@ -158,11 +179,15 @@ int32_t mla_combine_uv(const mla_combine_uv_args *args, void *stream);
 int32_t mla_combine_uv_plan(const mla_combine_uv_args *args, int32_t num_sms, mla_plan *plan);
 
 /*
- * mla_combine_uv_status -- synchronise `stream`, then read and clear the
- * device-side error word of the current device.  Returns MLA_OK,
- * MLA_ERR_TIMEOUT (a kernel abandoned a bounded wait; its output is
- * undefined), MLA_ERR_DATA (mla_attn_split_kv met a kv_len outside
- * [0, Lmax]) or MLA_ERR_CUDA.
+ * mla_combine_uv_status -- read and clear the device-side error word of the
+ * current device, in order on `stream`: the read and the clear are enqueued
+ * on `stream`, which is then synchronised.  The word is ONE per device: it
+ * collects the first error of any kernel of this library on any stream of
+ * the device, so a caller that runs the library on several streams should
+ * synchronise them (or the device) before asking, or it may see (and clear)
+ * another stream's error.  Returns MLA_OK, MLA_ERR_TIMEOUT (a kernel
+ * abandoned a bounded wait; its output is undefined), MLA_ERR_DATA
+ * (mla_attn_split_kv met a kv_len outside [0, Lmax]) or MLA_ERR_CUDA.
  */
 int32_t mla_combine_uv_status(void *stream);
 

@@ -38,7 +38,8 @@ MLA_ERR_KERNEL = 9
 MLA_ERR_DATA = 10
 
 EXPORTED_SYMBOLS = ("mla_combine_uv", "mla_combine_uv_plan", "mla_combine_uv_status",
-                    "mla_dcp_pack", "mla_attn_split_kv", "mla_o_proj", "mla_status_str", "mla_abi_version")
+                    "mla_dcp_pack", "mla_attn_split_kv", "mla_o_proj", "mla_status_str", "mla_abi_version",
+                    "mla_calib_stream_read")
 
 
 class MlaError(RuntimeError):
@@ -63,6 +64,7 @@ class Args(ctypes.Structure):
         ("w_fmt", ctypes.c_int32),
         ("gate", ctypes.c_void_p), ("out", ctypes.c_void_p),
         ("kernel", ctypes.c_int32), ("tile_tokens", ctypes.c_int32),
+        ("wait_ns", ctypes.c_int64), ("ready_flag", ctypes.c_void_p),
     ]
 
 
@@ -145,6 +147,9 @@ def load_library(path: str | None = None):
     L.mla_attn_split_kv.argtypes = [ctypes.POINTER(AttnArgs), ctypes.c_void_p]
     L.mla_o_proj.restype = ctypes.c_int32
     L.mla_o_proj.argtypes = [ctypes.POINTER(OprojArgs), ctypes.c_void_p]
+    L.mla_calib_stream_read.restype = ctypes.c_int32
+    L.mla_calib_stream_read.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p,
+                                        ctypes.c_void_p]
     _lib = L
     return L
 
@@ -162,7 +167,7 @@ def _ptr(t):
 
 
 def make_args(o, lse, q_per_request, splits_per_request, w_v, w_fmt, gate, out, w_scale=None,
-              kernel=MLA_KERNEL_AUTO, tile_tokens=0) -> Args:
+              kernel=MLA_KERNEL_AUTO, tile_tokens=0, wait_ns=0, ready_flag=None) -> Args:
     """Fill ``mla_combine_uv_args`` from tensors (pointers and element strides)."""
     P, S, H, _ = o.shape
     a = Args()
@@ -182,6 +187,8 @@ def make_args(o, lse, q_per_request, splits_per_request, w_v, w_fmt, gate, out, 
     a.gate = _ptr(gate)
     a.out = _ptr(out)
     a.kernel, a.tile_tokens = kernel, tile_tokens
+    a.wait_ns = wait_ns
+    a.ready_flag = _ptr(ready_flag)
     return a
 
 
@@ -204,13 +211,17 @@ def _check_tensors(o, lse, w_v, w_scale, gate, out, w_fmt):
 
 
 def mla_combine_uv(o, lse, q_per_request, splits_per_request, w_v, w_fmt, gate, out,
-                   w_scale=None, stream=None, kernel=MLA_KERNEL_AUTO, tile_tokens=0) -> None:
+                   w_scale=None, stream=None, kernel=MLA_KERNEL_AUTO, tile_tokens=0,
+                   wait_ns=0, ready_flag=None) -> None:
     """Run the stage on CUDA tensors; writes ``out`` [S_out, H*128] bf16.
 
     o [P, S, H, 512] bf16; lse [P, S, H] f32 (None allowed when P == 1);
     w_v bf16 [H, 128, 512] (w_fmt 0) or uint8 [H, 128, 256] + w_scale uint8
     [H, 128, 16] (w_fmt 1); gate [S, H*128] bf16.  Asynchronous on ``stream``
-    (default: PyTorch's current stream).
+    (default: PyTorch's current stream).  ``wait_ns`` > 0 sets the limit of
+    the tensor-core kernel's bounded waits (default 0.5 s); ``ready_flag`` (a
+    one-element int32 CUDA tensor) makes every CTA wait, within that limit,
+    until it is non-zero before reading its inputs.
     """
     import torch
 
@@ -219,7 +230,7 @@ def mla_combine_uv(o, lse, q_per_request, splits_per_request, w_v, w_fmt, gate, 
         stream = torch.cuda.current_stream(o.device)
     s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
     a = make_args(o, lse, q_per_request, splits_per_request, w_v, w_fmt, gate, out, w_scale,
-                  kernel, tile_tokens)
+                  kernel, tile_tokens, wait_ns, ready_flag)
     st = load_library().mla_combine_uv(ctypes.byref(a), ctypes.c_void_p(s))
     if st != MLA_OK:
         raise MlaError(st, "mla_combine_uv")
@@ -355,6 +366,23 @@ def mla_o_proj(x, w, out, stream=None) -> None:
         raise MlaError(st, "mla_o_proj")
 
 
+def mla_calib_stream_read(src, nbytes: int, dependent_round_trips: int, sink, stream=None) -> None:
+    """Measurement aid: one read-only streaming launch over the first ``nbytes``
+    bytes of the CUDA tensor ``src`` (``sink``: a one-element int32/uint32
+    CUDA tensor, written only for a fixed xor pattern of the data)."""
+    import torch
+
+    if nbytes > src.numel() * src.element_size():
+        raise ValueError("nbytes exceeds the tensor")
+    if stream is None:
+        stream = torch.cuda.current_stream(src.device)
+    s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    st = load_library().mla_calib_stream_read(ctypes.c_void_p(src.data_ptr()), nbytes, dependent_round_trips,
+                                              ctypes.c_void_p(sink.data_ptr()), ctypes.c_void_p(s))
+    if st != MLA_OK:
+        raise MlaError(st, "mla_calib_stream_read")
+
+
 def mla_combine_uv_plan(args: Args, num_sms: int = 0) -> dict:
     """Validate ``args`` and return the launch plan (no GPU needed when
     ``num_sms`` > 0).  Raises ``MlaError`` on a validation error."""
@@ -366,7 +394,8 @@ def mla_combine_uv_plan(args: Args, num_sms: int = 0) -> dict:
 
 
 def mla_combine_uv_status(stream=None) -> int:
-    """Synchronise ``stream`` and return (and clear) the device error status."""
+    """Read and clear the device's error word in order on ``stream`` (then
+    synchronised).  The word is one per device, shared by every stream."""
     import torch
 
     if stream is None:

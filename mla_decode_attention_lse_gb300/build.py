@@ -16,7 +16,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libmla_combine_uv.so")
-SOURCES = ["api.cu", "kernel_simt.cu", "kernel_tc.cu", "kernel_ks.cu", "kernel_pack.cu", "kernel_attn.cu", "kernel_oproj.cu"]
+SOURCES = ["api.cu", "kernel_simt.cu", "kernel_tc.cu", "kernel_ks.cu", "kernel_pack.cu", "kernel_attn.cu", "kernel_oproj.cu",
+           "kernel_calib.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -29,7 +30,8 @@ def _nvcc() -> str:
 
 def _newest_source_mtime() -> float:
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    files.append(os.path.join(ROOT, "include", "mla_combine_uv.h"))
+    inc = os.path.join(ROOT, "include")
+    files += [os.path.join(inc, f) for f in os.listdir(inc)]
     return max(os.path.getmtime(f) for f in files if os.path.isfile(f))
 
 

@@ -39,6 +39,7 @@ int32_t plan_impl(const mla_combine_uv_args *a, int32_t num_sms, mla_plan *pl, K
       a->splits_per_request < 0)
     return MLA_ERR_SHAPE;
   if ((int64_t)a->S_out * a->H * 128 >= (int64_t)1 << 40) return MLA_ERR_SHAPE;
+  if (a->wait_ns < 0) return MLA_ERR_SHAPE;
 
   // layout, chosen by P
   int layout, n_part;
@@ -95,6 +96,7 @@ int32_t plan_impl(const mla_combine_uv_args *a, int32_t num_sms, mla_plan *pl, K
   if (kernel == MLA_KERNEL_AUTO) kernel = (n_part <= mla::kTcMaxPart) ? MLA_KERNEL_TC : MLA_KERNEL_SIMT;
   if (S == 0) kernel = MLA_KERNEL_SIMT;  // nothing to merge: zero rows only
   if (kernel == MLA_KERNEL_SIMT && mla::simt_smem_bytes(n_part) > 200 * 1024) return MLA_ERR_KERNEL;
+  if (a->ready_flag && (kernel != MLA_KERNEL_TC || !aligned(a->ready_flag, 4))) return MLA_ERR_KERNEL;
 
   std::memset(pl, 0, sizeof *pl);
   pl->kernel = kernel;
@@ -191,6 +193,8 @@ int32_t plan_impl(const mla_combine_uv_args *a, int32_t num_sms, mla_plan *pl, K
     k.tiles_per_head = (kernel == MLA_KERNEL_SIMT) ? (a->S_out + 7) / 8 : (S + pl->tile_tokens - 1) / pl->tile_tokens;
     k.units = pl->units;
     k.off32 = pl->offsets32;
+    k.wait_ns = a->wait_ns > 0 ? (unsigned long long)a->wait_ns : mla::kDefaultWaitNs;
+    k.ready_flag = a->ready_flag;
   }
   return MLA_OK;
 }
@@ -455,12 +459,15 @@ int32_t mla_combine_uv_status(void *stream) {
   int *err;
   int32_t st = device_state(&dev, &sms, &err);
   if (st != MLA_OK) return st;
-  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MLA_ERR_CUDA;
+  // read and clear in order on the caller's stream (the word itself is one per
+  // device, shared by every stream)
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   int word = 0;
-  if (cudaMemcpy(&word, err, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaMemcpyAsync(&word, err, sizeof word, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MLA_ERR_CUDA;
   if (word != 0) {
-    const int zero = 0;
-    if (cudaMemcpy(err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return MLA_ERR_CUDA;
+    if (cudaMemsetAsync(err, 0, sizeof word, s) != cudaSuccess) return MLA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MLA_ERR_CUDA;
     return word == mla::kErrKvLen ? MLA_ERR_DATA : MLA_ERR_TIMEOUT;
   }
   return MLA_OK;

@@ -17,8 +17,9 @@ constexpr int kBlk = 32;   // MX block along K
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Bounded waits give up after this long and report MLA_ERR_TIMEOUT through
-// the error word; a healthy wait here lasts microseconds.
-constexpr unsigned long long kWaitNs = 500ull * 1000ull * 1000ull;
+// the error word; a healthy wait here lasts microseconds.  (The combine's
+// tensor-core kernel takes its pipeline limit from its launch parameters.)
+constexpr unsigned long long kWaitNs = kDefaultWaitNs;
 
 __device__ __forceinline__ unsigned long long globaltimer() {
   unsigned long long t;
@@ -282,6 +283,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *er
       return false;
     }
   }
+}
+
+// Global 32-bit load with acquire semantics at GPU scope (a flag another
+// kernel or CTA raises after writing the data it guards).
+__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
 // Shared-memory atomic add with acquire-release semantics at CTA scope;

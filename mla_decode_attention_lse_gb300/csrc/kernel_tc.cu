@@ -97,13 +97,13 @@ __host__ __device__ constexpr TcLayout tc_layout(int BN, int WFMT, int NW) {
   return L;
 }
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int *err, int code,
-                                              volatile int *abort_flag) {
+                                              volatile int *abort_flag, unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer() - t0 > kWaitNs) {
+    if (globaltimer() - t0 > limit_ns) {
       atomicCAS(err, 0, code);
       *abort_flag = 1;
       return false;
@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
       off[rd] = (long long)off3(t, Wrow, c.h, kV, 1, wq * 32 + v8);
       g[rd] = act[rd] ? __ldg(reinterpret_cast<const uint4 *>(p.gate + off[rd])) : make_uint4(0, 0, 0, 0);
     }
-    bool ok = wait_or_abort(bar_mma0 + 8 * bj, (uint32_t)(j / ST) & 1u, p.err, kErrWaitMma, s_abort);
+    bool ok = wait_or_abort(bar_mma0 + 8 * bj, (uint32_t)(j / ST) & 1u, p.err, kErrWaitMma, s_abort, p.wait_ns);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) return false;
     tc_fence_after();
@@ -675,7 +675,24 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
   // of o, lse and gate and every write comes after the wait
   if (nu > 0) load_wv(c_first.h);
   grid_dependency_wait();
-  if (nu > 0) {
+  if (p.ready_flag) {
+    // the producer's completion flag (optional): no input is read before it
+    // is raised; a flag still down at the wait limit ends the call
+    if (threadIdx.x == 0) {
+      const unsigned long long t0 = globaltimer();
+      while (ld_acquire_gpu(p.ready_flag) == 0) {
+        if (globaltimer() - t0 > p.wait_ns) {
+          atomicCAS(p.err, 0, kErrWaitFlag);
+          *s_abort = 1;
+          break;
+        }
+        __nanosleep(256);
+      }
+    }
+    __syncthreads();
+  }
+  // (after a flag timeout the loops below stop at once: they test the abort flag)
+  if (nu > 0 && !(p.ready_flag && *s_abort)) {
     float lse0;
     load_lse(cl, lse0);
     advance(cl);

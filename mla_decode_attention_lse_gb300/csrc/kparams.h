@@ -7,11 +7,14 @@ namespace mla {
 
 enum Layout : int { kPassthrough = 0, kCompact = 1, kRequestMajor = 2 };
 
+// Default limit of a bounded wait (ns); a healthy wait lasts microseconds.
+constexpr unsigned long long kDefaultWaitNs = 500ull * 1000ull * 1000ull;
+
 // Error codes a kernel writes into the device error word (first one wins).
 enum KernelError : int { kErrNone = 0, kErrWaitLatent = 1, kErrWaitMma = 2, kErrWaitAccEmpty = 3,
                          kErrWaitWv = 4, kErrWaitTeardown = 5,
                          kErrWaitPeer = 6, kErrWaitAttn = 7,
-                         kErrKvLen = 8 };
+                         kErrKvLen = 8, kErrWaitFlag = 9, kErrWaitTile = 10 };
 
 struct KParams {
   int S, S_out, H;
@@ -34,6 +37,8 @@ struct KParams {
   int units;         // H * tiles_per_head
   int off32;         // every element offset into o, lse, gate and out that is
                      // read or written is below 2^32 (32-bit address arithmetic)
+  unsigned long long wait_ns;  // limit of the pipeline's bounded waits (ns)
+  const int *ready_flag;       // optional: wait until non-zero before reading inputs
   int *err;          // device error word
 };
 
@@ -51,6 +56,13 @@ struct AttnParams {
   uint16_t *o;       // bf16 [spr, S, H, 512] dense
   float *lse;        // f32 [spr, S, H] dense
   int *err;          // device error word
+  // The combine fused behind the attention (mla_attn_combine_uv) only:
+  int *ws;           // workspace: [0] work queue, [1] CTAs done, [2 + k] arrivals of token tile k
+  int ntiles;        // 8-token tiles of the batch, ceil(S / 8)
+  int S_out;         // rows of out (rows S .. S_out - 1 are zeroed)
+  const uint16_t *gate;  // bf16 [S, H*128] dense
+  uint16_t *out;     // bf16 [S_out, H*128] dense
+  unsigned long long wait_ns;  // limit of the waits for a tile's partials
 };
 
 // The DCP producer side (pack into one destination rank's combine buffer).

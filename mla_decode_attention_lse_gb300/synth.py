@@ -308,6 +308,19 @@ def algorithmic_bytes(inp) -> int:
     return rows * D * 2 + lse_bytes + wv + S * H * V * 2 + S_out * H * V * 2
 
 
+def algorithmic_bytes_all_rows(inp) -> int:
+    """The same count with every selected partial row (live or dead): per
+    (t, h) the token's partials (1 KiB + a 4-byte LSE each; P == 1 reads one
+    row and no LSE), plus W_V (and its scales), the gate and the output."""
+    S, S_out, H, P, spr = (inp[k] for k in ("S", "S_out", "H", "P", "spr"))
+    n = 1 if P == 1 else spr
+    per_row = D * 2 + (0 if P == 1 else 4)
+    wv = inp["w_v"].numel() * inp["w_v"].element_size()
+    if inp["w_scale"] is not None:
+        wv += inp["w_scale"].numel()
+    return S * H * n * per_row + wv + S * H * V * 2 + S_out * H * V * 2
+
+
 def flops(inp) -> int:
     return 2 * inp["S"] * inp["H"] * V * D
 

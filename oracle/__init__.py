@@ -200,6 +200,29 @@ class Problem:
         return lat
 
 
+def host_arrays(inp):
+    """numpy copies of a workload's tensors (a dict of torch tensors as the
+    seeded generator makes them), strides kept: (o bits, lse, W_V, scales,
+    gate bits)."""
+    import torch
+
+    def bits(t):
+        return t.detach().cpu().view(torch.int16).numpy().view(np.uint16)
+
+    o = bits(inp["o"])
+    lse = None if inp["lse"] is None else inp["lse"].detach().cpu().numpy()
+    w = bits(inp["w_v"]) if inp["w_fmt"] == 0 else inp["w_v"].detach().cpu().numpy()
+    ws = None if inp["w_scale"] is None else inp["w_scale"].detach().cpu().numpy()
+    gate = bits(inp["gate"].contiguous())
+    return o, lse, w, ws, gate
+
+
+def problem_from_tensors(inp, host=None):
+    """The oracle's Problem for a workload dict (tensors copied to the host)."""
+    o, lse, w, ws, gate = host or host_arrays(inp)
+    return Problem(o, lse, inp["q"], inp["spr"], w, ws, inp["w_fmt"], gate, inp["S_out"])
+
+
 def dcp_pack(o, lse, seq_lens, qsl, q, dst):
     """stage_push for destination rank ``dst`` (the page's DCP producer side).
 

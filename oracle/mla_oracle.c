@@ -10,8 +10,10 @@
  * Source of the definition: the vLLM API page
  * "vllm.models.kimi_k3.amd.specialized_decode.mono.attention.mla_back"
  * (functions sane, combine_ranks, combine_splits, stage_combine, stage_uv,
- * wv_loads, mla_post, stage_push).  The page fixes fp32 for the merge ("LSE-weighted in
- * fp32"), so the oracle computes in fp32, single-threaded, in a fixed order:
+ * wv_loads, mla_post, stage_push).  The module docstring and combine_ranks /
+ * stage_combine state that the partials are merged with their LSE weights in
+ * single precision, so the oracle computes in fp32, single-threaded, in a
+ * fixed order:
  * partials in index order, K in ascending order, one rounding per operation
  * (this file is compiled with -ffp-contract=off so no multiply-add is fused).
  *

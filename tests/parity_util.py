@@ -25,21 +25,13 @@ def bits_to_f32(b):
 
 def host_inputs(inp):
     """numpy copies of a workload's tensors, strides kept (for the oracle)."""
-    o = inp["o"].detach().cpu()
-    o_np = o.view(torch.int16).numpy().view(np.uint16)
-    lse = None if inp["lse"] is None else inp["lse"].detach().cpu().numpy()
-    if inp["w_fmt"] == 0:
-        w = inp["w_v"].detach().cpu().view(torch.int16).numpy().view(np.uint16)
-    else:
-        w = inp["w_v"].detach().cpu().numpy()
-    ws = None if inp["w_scale"] is None else inp["w_scale"].detach().cpu().numpy()
-    gate = to_np16(inp["gate"])
-    return o_np, lse, w, ws, gate
+    import oracle
+
+    return oracle.host_arrays(inp)
 
 
 def oracle_problem(orc, inp, host=None):
-    o, lse, w, ws, gate = host or host_inputs(inp)
-    return orc.Problem(o, lse, inp["q"], inp["spr"], w, ws, inp["w_fmt"], gate, inp["S_out"])
+    return orc.problem_from_tensors(inp, host)
 
 
 def dead_rows(inp):

@@ -148,15 +148,20 @@ def test_more_than_32_partials_on_cuda_cores(lib, orc):
     assert e.value.status == m.MLA_ERR_KERNEL
 
 
-@pytest.mark.parametrize("kernel", [SIMT, TC, KS])
+@pytest.mark.parametrize("kernel,tile", [(SIMT, 16), (TC, 16), (TC, 32), (KS, 16)])
 @pytest.mark.parametrize("w_fmt", [0, 1])
-def test_all_dead_rows_and_planted_nan(lib, orc, kernel, w_fmt):
-    inp = custom(S=32, H=4, P=4, q=1, spr=4, w_fmt=w_fmt, dead_rows=10, neg_inf_frac=0.3, seed=7)
-    # plant NaN in the o rows of dead partials: they must never be read
+def test_all_dead_rows_and_planted_nan(lib, orc, kernel, tile, w_fmt):
+    # tile 32 with 4 partials is the two-batch unit whose first unit's both
+    # batches are loaded before the weights are known (MXFP4): dead rows are
+    # loaded there and must still never reach the merge
+    inp = custom(S=32 if tile == 16 else 96, H=4, P=4, q=1, spr=4, w_fmt=w_fmt, dead_rows=10,
+                 neg_inf_frac=0.3, seed=7)
+    # plant NaN and Inf in the o rows of dead partials: they must never be read
     lse, o = inp["lse"], inp["o"]
     dead = ~torch.isfinite(lse)
     o[dead] = float("nan")
-    check_full(orc, inp, kernel, 16, "planted NaN")
+    o[:, :, :, 5][dead] = float("inf")
+    check_full(orc, inp, kernel, tile, f"planted NaN, tile {tile}")
 
 
 @pytest.mark.parametrize("kernel", [SIMT, TC, KS])
