@@ -329,6 +329,74 @@ typedef struct {
  */
 int32_t mla_o_proj(const mla_o_proj_args *args, void *stream);
 
+/*
+ * The decode step's attention and its combine in ONE launch: the partial
+ * producer of mla_attn_split_kv followed, in the same persistent grid, by
+ * mla_combine_uv on its partials (compact layout, P = spr) -- the pairing the
+ * vLLM page "vllm.models.kimi_k3.amd.specialized_decode.mono.attention.
+ * mla_back" describes in its module docstring (M1c's partials, a token's
+ * request's splits merged by the combine) and in combine_splits' branch that
+ * runs with M1c in the same launch.  Each result is the same as the two calls
+ * in sequence would give: o / lse partials as mla_attn_split_kv defines them
+ * (they are written to part_o / part_lse and read back within the call), and
+ * out[t, h*128 + v] as mla_combine_uv defines it, rows S .. S_out - 1 zero.
+ *
+ * The attention's work items come from a queue shared by the CTAs; once an
+ * item's partials are written it adds one arrival to each 8-token tile its
+ * request covers.  Behind the attention items the queue holds the combine's
+ * (8-token tile, head) units; a CTA reaches one only after its own attention
+ * items, and waits (bounded by wait_ns) until the tile's items have all
+ * arrived -- items that running CTAs hold and that never wait on a combine
+ * unit.  The workspace carries the queue and the arrival counters.
+ */
+typedef struct {
+  /* the attention, as in mla_attn_split_kv_args */
+  int32_t B, q, H, spr;  /* q <= 32; spr <= 32                                 */
+  float scale;
+  const void *qv;        /* bf16 [S, H, 576], S = B * q                        */
+  int64_t q_st, q_sh;
+  const void *kv;        /* bf16 [B, Lmax, 576]                                 */
+  int64_t kv_sb, kv_sl;
+  int32_t Lmax;
+  const int32_t *kv_len; /* device int32 [B]                                    */
+  void *part_o;          /* bf16 [spr, S, H, 512] dense: the partials (caller-
+                            owned scratch, written and read in the call)      */
+  float *part_lse;       /* f32 [spr, S, H] dense                               */
+  /* the combine, as in mla_combine_uv_args with P = splits_per_request = spr */
+  const void *w_v;       /* bf16 [H, 128, 512]: W_V[h][v][k] at h*w_sh + v*w_sv
+                            + k; strides multiples of 8 elements; 16-byte
+                            aligned                                           */
+  int64_t w_sh, w_sv;
+  const uint8_t *w_scale; /* must be NULL (MXFP4 W_V: MLA_ERR_FMT)             */
+  int64_t s_sh, s_sv;
+  int32_t w_fmt;         /* MLA_W_BF16                                         */
+  const void *gate;      /* bf16 [S, H*128] dense                               */
+  void *out;             /* bf16 [S_out, H*128] dense, caller-owned            */
+  int32_t S_out;         /* >= S                                                */
+  int32_t *workspace;    /* device int32 [mla_attn_combine_uv_workspace_words(
+                            B, q)]: zero before the first call; every call
+                            leaves it zero (also after a timeout).  One call
+                            at a time per workspace.                          */
+  int64_t workspace_words;
+  int64_t wait_ns;       /* limit of the waits for a tile's partials, in ns;
+                            0 = the default 0.5 s                             */
+} mla_attn_combine_uv_args;
+
+/* Workspace words (int32) that mla_attn_combine_uv needs for B requests of q
+ * tokens: 2 + ceil(B*q / 8).  Returns -1 for B < 0 or q < 1. */
+int64_t mla_attn_combine_uv_workspace_words(int32_t B, int32_t q);
+
+/*
+ * mla_attn_combine_uv -- enqueue the fused decode step on `stream`.  Returns
+ * MLA_OK, or MLA_ERR_NULL / _SHAPE / _STRIDE / _ALIGN / _FMT before anything
+ * is launched (outputs untouched), or MLA_ERR_CUDA.  B == 0 (S = 0) only
+ * zeroes out's S_out rows (a memset on `stream`).
+ * Kernel-side failures (a kv_len outside [0, Lmax]: MLA_ERR_DATA; a wait that
+ * ran out: MLA_ERR_TIMEOUT) are reported by mla_combine_uv_status.
+ * (Added in ABI version 5.)
+ */
+int32_t mla_attn_combine_uv(const mla_attn_combine_uv_args *args, void *stream);
+
 /* A short English description of a status code (static storage). */
 const char *mla_status_str(int32_t status);
 

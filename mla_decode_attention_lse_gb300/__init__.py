@@ -39,7 +39,7 @@ MLA_ERR_DATA = 10
 
 EXPORTED_SYMBOLS = ("mla_combine_uv", "mla_combine_uv_plan", "mla_combine_uv_status",
                     "mla_dcp_pack", "mla_attn_split_kv", "mla_o_proj", "mla_status_str", "mla_abi_version",
-                    "mla_calib_stream_read")
+                    "mla_calib_stream_read", "mla_attn_combine_uv", "mla_attn_combine_uv_workspace_words")
 
 
 class MlaError(RuntimeError):
@@ -106,6 +106,25 @@ class AttnArgs(ctypes.Structure):
     ]
 
 
+class AttnCombineArgs(ctypes.Structure):
+    """Mirror of ``mla_attn_combine_uv_args``."""
+    _fields_ = [
+        ("B", ctypes.c_int32), ("q", ctypes.c_int32), ("H", ctypes.c_int32), ("spr", ctypes.c_int32),
+        ("scale", ctypes.c_float),
+        ("qv", ctypes.c_void_p), ("q_st", ctypes.c_int64), ("q_sh", ctypes.c_int64),
+        ("kv", ctypes.c_void_p), ("kv_sb", ctypes.c_int64), ("kv_sl", ctypes.c_int64),
+        ("Lmax", ctypes.c_int32),
+        ("kv_len", ctypes.c_void_p),
+        ("part_o", ctypes.c_void_p), ("part_lse", ctypes.c_void_p),
+        ("w_v", ctypes.c_void_p), ("w_sh", ctypes.c_int64), ("w_sv", ctypes.c_int64),
+        ("w_scale", ctypes.c_void_p), ("s_sh", ctypes.c_int64), ("s_sv", ctypes.c_int64),
+        ("w_fmt", ctypes.c_int32),
+        ("gate", ctypes.c_void_p), ("out", ctypes.c_void_p), ("S_out", ctypes.c_int32),
+        ("workspace", ctypes.c_void_p), ("workspace_words", ctypes.c_int64),
+        ("wait_ns", ctypes.c_int64),
+    ]
+
+
 class OprojArgs(ctypes.Structure):
     """Mirror of ``mla_o_proj_args``."""
     _fields_ = [
@@ -147,6 +166,10 @@ def load_library(path: str | None = None):
     L.mla_attn_split_kv.argtypes = [ctypes.POINTER(AttnArgs), ctypes.c_void_p]
     L.mla_o_proj.restype = ctypes.c_int32
     L.mla_o_proj.argtypes = [ctypes.POINTER(OprojArgs), ctypes.c_void_p]
+    L.mla_attn_combine_uv.restype = ctypes.c_int32
+    L.mla_attn_combine_uv.argtypes = [ctypes.POINTER(AttnCombineArgs), ctypes.c_void_p]
+    L.mla_attn_combine_uv_workspace_words.restype = ctypes.c_int64
+    L.mla_attn_combine_uv_workspace_words.argtypes = [ctypes.c_int32, ctypes.c_int32]
     L.mla_calib_stream_read.restype = ctypes.c_int32
     L.mla_calib_stream_read.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p,
                                         ctypes.c_void_p]
@@ -330,6 +353,74 @@ def mla_attn_split_kv(qv, kv, kv_len, q, spr, scale, o, lse, stream=None) -> Non
     st = load_library().mla_attn_split_kv(ctypes.byref(a), ctypes.c_void_p(s))
     if st != MLA_OK:
         raise MlaError(st, "mla_attn_split_kv")
+
+
+def mla_attn_combine_uv_workspace_words(B: int, q: int) -> int:
+    """int32 words of workspace the fused decode step needs for B requests of q tokens."""
+    return load_library().mla_attn_combine_uv_workspace_words(B, q)
+
+
+def make_attn_combine_args(qv, kv, kv_len, q, spr, scale, part_o, part_lse, w_v, gate, out, workspace,
+                           wait_ns=0) -> AttnCombineArgs:
+    """Fill ``mla_attn_combine_uv_args`` from tensors (pointers and element strides)."""
+    S, H, _ = qv.shape
+    B, Lmax, _ = kv.shape
+    a = AttnCombineArgs()
+    a.B, a.q, a.H, a.spr, a.scale = B, q, H, spr, float(scale)
+    a.qv, a.q_st, a.q_sh = _ptr(qv), qv.stride(0), qv.stride(1)
+    a.kv, a.kv_sb, a.kv_sl = _ptr(kv), kv.stride(0), kv.stride(1)
+    a.Lmax, a.kv_len = Lmax, _ptr(kv_len)
+    a.part_o, a.part_lse = _ptr(part_o), _ptr(part_lse)
+    a.w_v, a.w_sh, a.w_sv = _ptr(w_v), w_v.stride(0), w_v.stride(1)
+    a.w_fmt = MLA_W_BF16
+    a.gate, a.out, a.S_out = _ptr(gate), _ptr(out), out.shape[0]
+    a.workspace, a.workspace_words = _ptr(workspace), workspace.numel()
+    a.wait_ns = wait_ns
+    return a
+
+
+def mla_attn_combine_uv(qv, kv, kv_len, q, spr, scale, part_o, part_lse, w_v, gate, out, workspace,
+                        stream=None, wait_ns=0) -> None:
+    """The decode step in one launch: split-KV attention, then the combine of
+    its partials (bf16 W_V), on CUDA tensors.
+
+    qv [S, H, 576] bf16 (S = B * q); kv [B, Lmax, 576] bf16; kv_len [B] int32;
+    part_o [spr, S, H, 512] bf16 / part_lse [spr, S, H] f32 dense (scratch for
+    the partials); w_v bf16 [H, 128, 512]; gate [S, H*128] bf16; out
+    [S_out, H*128] bf16; workspace int32 [mla_attn_combine_uv_workspace_words(B, q)],
+    zero before the first call (every call leaves it zero).
+    """
+    import torch
+
+    S, H, dq = qv.shape
+    B, Lmax, dk = kv.shape
+    if qv.dtype != torch.bfloat16 or dq != 576 or qv.stride(2) != 1:
+        raise ValueError("qv must be bf16 [S, H, 576] with a unit-stride last dimension")
+    if kv.dtype != torch.bfloat16 or dk != 576 or kv.stride(2) != 1:
+        raise ValueError("kv must be bf16 [B, Lmax, 576] with a unit-stride last dimension")
+    if S != B * q:
+        raise ValueError("qv must hold B * q token rows")
+    if kv_len.dtype != torch.int32 or tuple(kv_len.shape) != (B,) or not kv_len.is_contiguous():
+        raise ValueError("kv_len must be a dense int32 [B] tensor")
+    if (part_o.dtype != torch.bfloat16 or tuple(part_o.shape) != (spr, S, H, 512) or not part_o.is_contiguous()
+            or part_lse.dtype != torch.float32 or tuple(part_lse.shape) != (spr, S, H)
+            or not part_lse.is_contiguous()):
+        raise ValueError("part_o / part_lse must be dense bf16 [spr, S, H, 512] / float32 [spr, S, H]")
+    if w_v.dtype != torch.bfloat16 or tuple(w_v.shape) != (H, 128, 512) or w_v.stride(2) != 1:
+        raise ValueError("w_v must be bf16 [H, 128, 512] with a unit-stride last dimension")
+    if gate.dtype != torch.bfloat16 or not gate.is_contiguous() or tuple(gate.shape) != (S, H * 128):
+        raise ValueError("gate must be a dense bf16 [S, H*128] tensor")
+    if out.dtype != torch.bfloat16 or not out.is_contiguous() or out.dim() != 2 or out.shape[1] != H * 128:
+        raise ValueError("out must be a dense bf16 [S_out, H*128] tensor")
+    if workspace.dtype != torch.int32 or not workspace.is_contiguous():
+        raise ValueError("workspace must be a dense int32 tensor")
+    if stream is None:
+        stream = torch.cuda.current_stream(qv.device)
+    s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    a = make_attn_combine_args(qv, kv, kv_len, q, spr, scale, part_o, part_lse, w_v, gate, out, workspace, wait_ns)
+    st = load_library().mla_attn_combine_uv(ctypes.byref(a), ctypes.c_void_p(s))
+    if st != MLA_OK:
+        raise MlaError(st, "mla_attn_combine_uv")
 
 
 def make_oproj_args(x, w, out) -> OprojArgs:

@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -235,6 +237,32 @@ int32_t make_kv_tmap(const mla_attn_split_kv_args *a, CUtensorMap *tm) {
   return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_STRIDE;
 }
 
+// TMA descriptor of W_V [H, 128, 512] bf16 (element strides w_sv, w_sh): boxes
+// of 64 K elements x 128 V rows x 1 head with the 128-byte swizzle -- one K
+// block of the [128 x 512] A tile of a head.
+int32_t make_wv_tmap(const void *w_v, int H, int64_t w_sh, int64_t w_sv, CUtensorMap *tm) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+      void *fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return MLA_ERR_CUDA;
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+  }
+  cuuint64_t dims[3] = {512, 128, (cuuint64_t)H};
+  cuuint64_t strides[2] = {(cuuint64_t)w_sv * 2, (cuuint64_t)(H > 1 ? w_sh : 128 * w_sv) * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(w_v), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_STRIDE;
+}
+
 // TMA descriptor of a bf16 matrix [rows, cols] (row stride in elements) as
 // a 3-D map with a unit third dimension: boxes of 64 columns x box_rows rows,
 // 128-byte swizzle; rows past the matrix read as zero.
@@ -421,6 +449,97 @@ int32_t mla_attn_split_kv(const mla_attn_split_kv_args *a, void *stream) {
   p.lse = a->lse;
   p.err = err;
   const cudaError_t e = mla::launch_attn(p, tm, sms, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int64_t mla_attn_combine_uv_workspace_words(int32_t B, int32_t q) {
+  if (B < 0 || q < 1) return -1;
+  return 2 + mla::attn_combine_tiles((int)std::min<int64_t>((int64_t)B * q, INT32_MAX));
+}
+
+int32_t mla_attn_combine_uv(const mla_attn_combine_uv_args *a, void *stream) {
+  if (!a) return MLA_ERR_NULL;
+  if (a->w_fmt != MLA_W_BF16 || a->w_scale) return MLA_ERR_FMT;  // bf16 W_V only
+  if (a->B < 0 || a->q < 1 || a->q > 32 || a->H < 1 || a->H > 65535 || a->spr < 1 || a->spr > 32 || a->Lmax < 1 ||
+      !std::isfinite(a->scale) || a->wait_ns < 0)
+    return MLA_ERR_SHAPE;
+  const int64_t S = (int64_t)a->B * a->q;
+  if (S >= ((int64_t)1 << 31) || a->S_out < S || (int64_t)a->S_out * a->H * 128 >= ((int64_t)1 << 40))
+    return MLA_ERR_SHAPE;
+  const int G = mla::attn_heads_per_cta(a->q, a->H);
+  const int groups = (a->H + G - 1) / G;
+  const int ntiles = mla::attn_combine_tiles((int)S);
+  if ((int64_t)a->B * a->spr * groups + (int64_t)ntiles * a->H >= ((int64_t)1 << 31)) return MLA_ERR_SHAPE;
+  if (a->S_out > 0 && !a->out) return MLA_ERR_NULL;
+  if (a->S_out > 0 && !aligned(a->out, 16)) return MLA_ERR_ALIGN;
+  if (a->B > 0) {
+    if (!a->qv || !a->kv || !a->kv_len || !a->part_o || !a->part_lse || !a->w_v || !a->gate || !a->workspace)
+      return MLA_ERR_NULL;
+    if (a->workspace_words < 2 + ntiles) return MLA_ERR_SHAPE;
+    if (!aligned(a->qv, 16) || !aligned(a->kv, 16) || !aligned(a->part_o, 16) || !aligned(a->w_v, 16) ||
+        !aligned(a->gate, 16))
+      return MLA_ERR_ALIGN;
+    if (!aligned(a->part_lse, 4) || !aligned(a->kv_len, 4) || !aligned(a->workspace, 4)) return MLA_ERR_ALIGN;
+    if (a->q_st < 0 || a->q_sh < 0 || a->q_st % 8 || a->q_sh % 8) return MLA_ERR_STRIDE;
+    if (a->kv_sl < 576 || a->kv_sl % 8 || a->kv_sb < 0 || a->kv_sb % 8 || (a->B > 1 && a->kv_sb == 0))
+      return MLA_ERR_STRIDE;
+    if (a->w_sv < 512 || a->w_sv % 8 || a->w_sh < 0 || a->w_sh % 8 || (a->H > 1 && a->w_sh == 0))
+      return MLA_ERR_STRIDE;
+  }
+  int dev, sms;
+  int *err;
+  int32_t st = device_state(&dev, &sms, &err);
+  if (st != MLA_OK) return st;
+  if (a->B == 0) {
+    if (a->S_out == 0) return MLA_OK;
+    return cudaMemsetAsync(a->out, 0, (size_t)a->S_out * a->H * 128 * 2, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? MLA_OK
+               : MLA_ERR_CUDA;
+  }
+  mla_attn_split_kv_args aa;
+  std::memset(&aa, 0, sizeof aa);
+  aa.B = a->B;
+  aa.q = a->q;
+  aa.H = a->H;
+  aa.spr = a->spr;
+  aa.scale = a->scale;
+  aa.qv = a->qv;
+  aa.q_st = a->q_st;
+  aa.q_sh = a->q_sh;
+  aa.kv = a->kv;
+  aa.kv_sb = a->kv_sb;
+  aa.kv_sl = a->kv_sl;
+  aa.Lmax = a->Lmax;
+  CUtensorMap tm, wm;
+  st = make_kv_tmap(&aa, &tm);
+  if (st != MLA_OK) return st;
+  st = make_wv_tmap(a->w_v, a->H, a->w_sh, a->w_sv, &wm);
+  if (st != MLA_OK) return st;
+  mla::AttnParams p;
+  std::memset(&p, 0, sizeof p);
+  p.B = a->B;
+  p.q = a->q;
+  p.H = a->H;
+  p.spr = a->spr;
+  p.G = G;
+  p.groups = groups;
+  p.Lmax = a->Lmax;
+  p.scale_log2 = a->scale * 1.4426950408889634f;
+  p.qv = static_cast<const uint16_t *>(a->qv);
+  p.q_st = a->q_st;
+  p.q_sh = a->q_sh;
+  p.kv_len = a->kv_len;
+  p.o = static_cast<uint16_t *>(a->part_o);
+  p.lse = a->part_lse;
+  p.err = err;
+  p.ws = a->workspace;
+  p.ntiles = ntiles;
+  p.S_out = a->S_out;
+  p.gate = static_cast<const uint16_t *>(a->gate);
+  p.out = static_cast<uint16_t *>(a->out);
+  p.wait_ns = a->wait_ns > 0 ? (unsigned long long)a->wait_ns : mla::kDefaultWaitNs;
+  const cudaError_t e = mla::launch_attn_combine(p, tm, wm, sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

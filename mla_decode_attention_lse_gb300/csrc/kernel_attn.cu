@@ -30,9 +30,28 @@
 // lse.  Every wait is bounded; a timeout records an error, the roles stop,
 // and the kernel waits (bounded) for its own copies and MMAs before it frees
 // TMEM and returns.
+//
+// The FUSED instance (mla_attn_combine_uv) runs the combine of the same page
+// behind the attention in the same launch, as the page's M1c + combine pair
+// does.  Its items come from a queue every CTA draws from (a workspace
+// counter): the TMA lane draws the next item when it is ready to copy its
+// tiles and hands it to the other roles through a small shared ring.  After
+// an item's o / lse are written, the softmax warps add one arrival to each
+// 8-token tile the request covers.  Behind the attention items the queue
+// holds the combine units (8-token tile, head), tile-major: a CTA that draws
+// one has finished its own attention items; it waits (bounded) until every
+// item of the tile has arrived -- those items were all drawn earlier, by CTAs
+// that are running, and none of them waits on a combine unit -- then one
+// warp per token merges the token's partials (read back from L2) with the
+// combine's LSE weights into bf16 latents in shared memory, W_V[h] arrives by
+// TMA, one thread issues the W_UV GEMM (32 kind::f16 MMAs, M = 128 V rows,
+// N = 16 with 8 tokens) into TMEM, and the same warps apply the gate and
+// store core.  The last CTA to finish zeroes the workspace again.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <cstring>
 
 #include "device_common.cuh"
 #include "kernels.h"
@@ -49,7 +68,11 @@ constexpr int kAttnThreads = (3 + kAttnSmx) * 32;  // warp 0 TMA, warp 1 MMA, so
 constexpr uint32_t kDblBytes = 2u * kAttnTile * 128u;  // 32 KiB
 constexpr uint32_t kRopeBytes = kAttnTile * 128u;      // 16 KiB
 
-template <int N>
+constexpr int kItemRing = 4;        // FUSED: items handed from the TMA lane to the other roles
+constexpr int kItemTakers = 2 + kAttnSmx;  // MMA lane, query warp, softmax warps
+constexpr int kCmbTile = 8;         // FUSED: tokens per combine unit (one merging warp each)
+
+template <int N, bool FUSED = false>
 struct AttnLayout {
   static constexpr int kRope = (N == 16) ? 2 : 1;  // rope-block slots
   static constexpr uint32_t dbl_off = 0;
@@ -62,13 +85,19 @@ struct AttnLayout {
   static constexpr uint32_t bar_off = row_off + N * 8u;
   // barriers: full/empty per double slot, full/empty per rope slot, then
   // s_full, s_free, p_full, o_full, q_full, q_free
-  static constexpr int kBars = 2 * kAttnDbl + 2 * kRope + 6;
-  static constexpr uint32_t misc_off = bar_off + kBars * 8u;  // TMEM base, abort flag
-  static constexpr uint32_t total = misc_off + 16u;
+  // FUSED adds: item full / empty per ring slot, W_V full, combine MMA done
+  static constexpr int kBars = 2 * kAttnDbl + 2 * kRope + 6 + (FUSED ? 2 * kItemRing + 2 : 0);
+  // misc: [0] TMEM base, [1] abort flag, [2 .. 2 + kItemRing) item ring,
+  // [6] the combine unit drawn last
+  static constexpr uint32_t misc_off = bar_off + kBars * 8u;
+  static constexpr uint32_t total = misc_off + 32u;
   static constexpr uint32_t tmem_cols = (5 * N <= 128) ? 128u : 256u;  // S^T (N) + O^T (4 N)
 };
-static_assert(AttnLayout<16>::total + 1024 <= 227u * 1024u, "shared memory (N = 16)");
-static_assert(AttnLayout<32>::total + 1024 <= 227u * 1024u, "shared memory (N = 32)");
+static_assert(AttnLayout<16, true>::total + 1024 <= 227u * 1024u, "shared memory (N = 16)");
+static_assert(AttnLayout<32, true>::total + 1024 <= 227u * 1024u, "shared memory (N = 32)");
+// FUSED: W_V[h] (128 KiB) reuses the first four double-block slots, the
+// latent tile [16 x 512] bf16 (16 KiB) the first rope slot
+static_assert(4 * kDblBytes == 128u * 1024u && kRopeBytes >= 16u * 1024u, "combine tiles");
 
 // Bounded wait on an mbarrier phase, shared abort flag (as the combine kernels).
 __device__ __forceinline__ bool attn_wait(uint32_t bar, uint32_t parity, int *err, volatile int *abort_flag) {
@@ -85,12 +114,227 @@ __device__ __forceinline__ bool attn_wait(uint32_t bar, uint32_t parity, int *er
   }
 }
 
+// Wait (bounded) until the global counter reaches `target` (acquire).
+__device__ __forceinline__ bool wait_count(const int *cnt, int target, unsigned long long limit_ns) {
+  if (ld_acquire_gpu(cnt) >= target) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    __nanosleep(128);
+    if (ld_acquire_gpu(cnt) >= target) return true;
+    if (globaltimer() - t0 > limit_ns) return false;
+  }
+}
+
+__device__ __forceinline__ uint4 ld_cg_v4(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float ld_cg_f32(const float *p) {
+  float v;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+
+// The combine units of the fused launch (see the file comment), run by every
+// thread of the CTA once its role has finished the attention items.  Shared
+// memory: W_V[h] in the first four double-block slots (8 K blocks of [128 x
+// 128 B], 128-byte swizzle, as TMA writes them), the unit's latents in the
+// first rope slot (8 K blocks of [16 x 128 B]); TMEM columns 0..15 hold the
+// accumulator D[v, token].
+template <int N>
+__device__ __forceinline__ void combine_phase(const AttnParams &p, const CUtensorMap &wv_map, uint32_t sbase,
+                                              uint8_t *gbase, uint32_t tmem, uint32_t *misc, volatile int *s_abort,
+                                              uint32_t wv_full, uint32_t cmb_mma, int nitems) {
+  using L = AttnLayout<N, true>;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = p.B * p.q, H = p.H, n = p.spr;
+  const int nunits = p.ntiles * H;
+  const int Wrow = H * kV;
+  const uint32_t sA = sbase + L::dbl_off;
+  const uint32_t sB = sbase + L::rope_off;
+  uint8_t *gB = gbase + L::rope_off;
+  const float kNegInf = __int_as_float(0xFF800000);
+  constexpr unsigned kFull = 0xffffffffu;
+
+  tc_fence_before();
+  __syncthreads();  // every role is done with its attention items (copies landed, MMAs complete)
+  tc_fence_after();
+  int cur_h = -1, units = 0;
+  int wv_issued = 0;   // thread 0: W_V loads issued
+  int mma_issued = 0;  // MMA lane: units whose MMAs it committed
+  int wv_seen = 0;     // every thread: W_V loads so far
+  uint32_t unit = misc[6];
+  while (!*s_abort && unit != 0xFFFFFFFFu && (int)unit - nitems < nunits) {
+    const int u = (int)unit - nitems;
+    const int tile = u / H, h = u - tile * H;
+    const bool new_h = h != cur_h;
+    if (threadIdx.x == 0) {
+      // every (request, split, head group) item of the requests the tile covers
+      const int t_lo = tile * kCmbTile, t_hi = min(t_lo + kCmbTile, S) - 1;
+      const int target = (t_hi / p.q - t_lo / p.q + 1) * p.spr * p.groups;
+      if (!wait_count(p.ws + 2 + tile, target, p.wait_ns)) {
+        atomicCAS(p.err, 0, kErrWaitTile);
+        *s_abort = 1;
+      } else if (new_h) {
+        mbar_arrive_expect_tx(wv_full, 4u * kDblBytes);
+#pragma unroll 1
+        for (int kb = 0; kb < 8; ++kb) tma_load_3d(sA + (uint32_t)kb * 16384u, &wv_map, 64 * kb, 0, h, wv_full);
+        ++wv_issued;
+      }
+    }
+    __syncthreads();
+    if (*s_abort) break;
+    if (new_h) {
+      cur_h = h;
+      ++wv_seen;
+    }
+    const bool merger = warp >= 2 && warp < 2 + kAttnSmx;
+    if (merger) {
+      // token t: the LSE weights of its spr partials (one per lane), then its
+      // rows in partial order, fp32, one rounding per operation (the rule of
+      // the combine kernels), rounded to bf16 into row mw of the tile
+      const int mw = warp - 2, t = tile * kCmbTile + mw;
+      const bool valid = t < S;
+      float lv = kNegInf;
+      if (valid && lane < n) lv = ld_cg_f32(p.lse + ((long long)lane * S + t) * H + h);
+      const float l = sane(lv);
+      float m = l;
+#pragma unroll
+      for (int s = 1; s < 32; s <<= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, s));
+      if (m == kNegInf) m = 0.0f;
+      const float e = (lane < n) ? ex2_approx(__fmul_rn(__fsub_rn(l, m), kLog2e)) : 0.0f;
+      float Z = 0.0f;
+      for (int j = 0; j < n; ++j) Z = __fadd_rn(Z, __shfl_sync(kFull, e, j));
+      const float inv = (Z == 0.0f) ? 0.0f : rcp_approx(Z);
+      const float wg = (e == 0.0f) ? 0.0f : __fmul_rn(e, inv);
+      uint64_t acc[8];
+#pragma unroll
+      for (int x = 0; x < 8; ++x) acc[x] = 0ull;
+      const long long pstride = (long long)S * H * kD;
+      const uint16_t *row0 = p.o + ((long long)t * H + h) * kD;
+      for (int j0 = 0; j0 < n; j0 += 8) {
+        uint4 buf[8][2];
+        float w[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          w[jj] = __shfl_sync(kFull, wg, (j0 + jj) & 31);  // 0 for partials past n
+          if (w[jj] != 0.0f && valid) {
+            const uint16_t *r = row0 + (long long)(j0 + jj) * pstride;
+            buf[jj][0] = ld_cg_v4(r + 8 * lane);
+            buf[jj][1] = ld_cg_v4(r + 256 + 8 * lane);
+          } else {
+            buf[jj][0] = buf[jj][1] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          if (w[jj] == 0.0f) continue;
+          const uint64_t w2 = f2_pack(w[jj], w[jj]);
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const uint32_t uu[4] = {buf[jj][c].x, buf[jj][c].y, buf[jj][c].z, buf[jj][c].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[c * 4 + q] = f2_add(acc[c * 4 + q], f2_mul(w2, f2_pack(bf16_lo(uu[q]), bf16_hi(uu[q]))));
+          }
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float lo, hi;
+          f2_unpack(acc[c * 4 + q], lo, hi);
+          pk[q] = pack_bf16(lo, hi);
+        }
+        const uint4 x = valid ? make_uint4(pk[0], pk[1], pk[2], pk[3]) : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4 *>(gB + sw128_offset(mw, lane + 32 * c, 16)) = x;
+      }
+      fence_proxy_async_smem();
+    }
+    __syncthreads();
+    if (warp == 1 && lane == 0) {
+      // D[v, token] = sum_k W_V[h][v][k] lat[token][k]: M = 128, N = 16, K = 512
+      const bool ok = !new_h || attn_wait(wv_full, (uint32_t)(wv_seen - 1) & 1u, p.err, s_abort);
+      if (ok) {
+        tc_fence_after();
+        const uint32_t dA = (uint32_t)smem_desc_sw128(sA), dB = (uint32_t)smem_desc_sw128(sB);
+        constexpr uint32_t kIdesc = idesc_bf16(128, 16);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const uint32_t kb = (uint32_t)k >> 2, kk = (uint32_t)k & 3u;
+          tc_mma_f16(tmem, desc_sw128_at(dA, kb * 16384u + kk * 32u), desc_sw128_at(dB, kb * 2048u + kk * 32u), kIdesc,
+                     k > 0 ? 1u : 0u);
+        }
+        tc_commit(cmb_mma);
+        ++mma_issued;
+      }
+    }
+    if (merger) {
+      // epilogue: this warp's TMEM lane quadrant (32 V rows) x 4 tokens
+      const int qd = warp & 3, hh = (warp - 2) >> 2;
+      bool ok = attn_wait(cmb_mma, (uint32_t)units & 1u, p.err, s_abort);
+      ok = __all_sync(kFull, ok);
+      if (ok) {
+        tc_fence_after();
+        uint32_t r[4];
+        tmem_ld_x4(tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(hh * 4), r);
+        tc_wait_ld();
+        tc_fence_before();
+        const int v = qd * 32 + lane;
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const int t = tile * kCmbTile + hh * 4 + x;
+          if (t < S) {
+            const long long off = (long long)t * Wrow + h * kV + v;
+            const float a = round_bf16(__uint_as_float(r[x]));
+            const float g = __uint_as_float((uint32_t)__ldg(p.gate + off) << 16);
+            const __nv_bfloat16 y = __float2bfloat16_rn(a * g);  // bf16(acc) * gate, exact in fp32, one rounding
+            p.out[off] = *reinterpret_cast<const uint16_t *>(&y);
+          }
+        }
+      }
+    }
+    ++units;
+    __syncthreads();
+    if (threadIdx.x == 0) misc[6] = (uint32_t)atomicAdd(p.ws, 1);
+    __syncthreads();
+    unit = misc[6];
+  }
+  // after an abort: this CTA's weight copies and MMAs land before it exits
+  if (threadIdx.x == 0 && wv_issued > 0) mbar_wait(wv_full, (uint32_t)(wv_issued - 1) & 1u, p.err, kErrWaitTeardown);
+  if (warp == 1 && lane == 0 && mma_issued > 0)
+    mbar_wait(cmb_mma, (uint32_t)(mma_issued - 1) & 1u, p.err, kErrWaitTeardown);
+  // rows S .. S_out - 1 of core are zero (this CTA's slice of them)
+  const long long n16 = (long long)(p.S_out - S) * Wrow / 8;
+  if (n16 > 0) {
+    const long long zb = (long long)blockIdx.x * n16 / gridDim.x;
+    const long long ze = (long long)(blockIdx.x + 1) * n16 / gridDim.x;
+    uint4 *dst = reinterpret_cast<uint4 *>(p.out + (long long)S * Wrow);
+    for (long long k = zb + threadIdx.x; k < ze; k += blockDim.x) dst[k] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // the last CTA to finish leaves the workspace zeroed for the next call
+    __threadfence();
+    if (atomicAdd(p.ws + 1, 1) == (int)gridDim.x - 1) {
+      __threadfence();
+      for (int k = 0; k < p.ntiles; ++k) p.ws[2 + k] = 0;
+      p.ws[0] = 0;
+      p.ws[1] = 0;
+      __threadfence();
+    }
+  }
+}
+
 }  // namespace
 
-template <int N>
+template <int N, bool FUSED>
 __global__ void __launch_bounds__(kAttnThreads, 1)
-    attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap kv_map) {
-  using L = AttnLayout<N>;
+    attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap kv_map,
+                const __grid_constant__ CUtensorMap wv_map) {
+  using L = AttnLayout<N, FUSED>;
   constexpr int NR = L::kRope;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -112,6 +356,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t o_full = s_full + 24u;  // a tile's O^T MMAs are complete
   const uint32_t q_full = s_full + 32u;  // an item's query rows are in shared memory
   const uint32_t q_free = s_full + 40u;  // the item's last S^T MMAs are done: Q may be replaced
+  // FUSED: item ring slots (full: published by the TMA lane; empty: every
+  // taker has read it), W_V of a combine unit in shared memory, its MMAs done
+  auto item_full = [&](int s) { return s_full + 48u + 8u * (uint32_t)s; };
+  auto item_empty = [&](int s) { return s_full + 48u + 8u * (uint32_t)(kItemRing + s); };
+  const uint32_t wv_full = s_full + 48u + 8u * (uint32_t)(2 * kItemRing);
+  const uint32_t cmb_mma = wv_full + 8u;
+  volatile uint32_t *ring = misc + 2;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -129,7 +380,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     mbar_init(o_full, 1u);
     mbar_init(q_full, 1u);
     mbar_init(q_free, 1u);
+    if constexpr (FUSED) {
+      for (int s = 0; s < kItemRing; ++s) {
+        mbar_init(item_full(s), 1u);
+        mbar_init(item_empty(s), (uint32_t)kItemTakers);
+      }
+      mbar_init(wv_full, 1u);
+      mbar_init(cmb_mma, 1u);
+    }
     misc[1] = 0u;
+    misc[6] = 0xFFFFFFFFu;
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -168,7 +428,38 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     return I;
   };
   // the query rows, the lengths and the cache come from earlier kernels
+  // (and, FUSED, the workspace's last user)
   grid_dependency_wait();
+
+  // The k-th item of this CTA: a fixed stride over the grid, or (FUSED) the
+  // queue: the TMA lane draws it and publishes it in ring slot k % kItemRing,
+  // the other roles read it there and release the slot.  An index >= nitems
+  // ends the attention items.
+  auto draw = [&](int k, bool &ok) -> int {  // TMA lane
+    if constexpr (!FUSED) {
+      return blockIdx.x + k * gridDim.x;
+    } else {
+      const int s = k % kItemRing;
+      if (k >= kItemRing) ok = attn_wait(item_empty(s), (uint32_t)(k / kItemRing - 1) & 1u, p.err, s_abort);
+      if (!ok) return nitems;
+      const int it = atomicAdd(p.ws, 1);
+      ring[s] = (uint32_t)it;
+      mbar_arrive(item_full(s));
+      return it;
+    }
+  };
+  auto take = [&](int k, bool &ok) -> int {  // the other roles
+    if constexpr (!FUSED) {
+      return blockIdx.x + k * gridDim.x;
+    } else {
+      const int s = k % kItemRing;
+      ok = ok && attn_wait(item_full(s), (uint32_t)(k / kItemRing) & 1u, p.err, s_abort);
+      return ok ? (int)ring[s] : nitems;
+    }
+  };
+  auto release = [&](int k) {  // once per taker
+    if constexpr (FUSED) mbar_arrive(item_empty(k % kItemRing));
+  };
 
   if (warp == 0) {
     // ---- TMA producer: per tile four double blocks, then the rope block ----
@@ -176,7 +467,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       bool ok = true;
       int T = 0;                        // tiles started
       int issued_db = 0, issued_r = 0;  // double blocks / rope blocks whose copies were issued
-      for (int it = blockIdx.x; it < nitems && ok; it += gridDim.x) {
+      for (int k = 0; ok; ++k) {
+        const int it = draw(k, ok);
+        if (!ok) break;
+        if (it >= nitems) {
+          if constexpr (FUSED) misc[6] = (uint32_t)it;  // this CTA's first combine unit
+          break;
+        }
         const Item I = item_of(it);
         for (int t = 0; t < I.ntiles && ok; ++t, ++T) {
           const int y = I.j0 + t * kAttnTile;
@@ -217,7 +514,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       int last_s = -1, last_o = -1, last_q = -1;  // last committed S^T / O^T tile, Q release
       bool ok = true;
       int T = 0, kq = 0;  // tiles, non-empty items
-      for (int it = blockIdx.x; it < nitems && ok; it += gridDim.x) {
+      for (int k = 0; ok; ++k) {
+        const int it = take(k, ok);
+        if (!ok) break;
+        release(k);
+        if (it >= nitems) break;
         const Item I = item_of(it);
         if (I.ntiles == 0) continue;
         ok = attn_wait(q_full, (uint32_t)kq & 1u, p.err, s_abort);
@@ -286,7 +587,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     bool ok = true;
     int kq = 0;
     const int qG = p.q * p.G;
-    for (int it = blockIdx.x; it < nitems && ok; it += gridDim.x) {
+    for (int k = 0; ok; ++k) {
+      const int it = take(k, ok);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      if (lane == 0) release(k);
+      if (it >= nitems) break;
       const Item I = item_of(it);
       if (I.ntiles == 0) continue;
       if (kq > 0) ok = attn_wait(q_free, (uint32_t)(kq - 1) & 1u, p.err, s_abort);
@@ -330,9 +636,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // the named barrier), so that no warp waits at a barrier another left.
     bool ok = true;
     int T = 0;  // tiles
-    for (int it = blockIdx.x; it < nitems && ok; it += gridDim.x) {
+    // FUSED: one arrival per 8-token tile the item's request covers, once
+    // every softmax warp has written the item's o / lse
+    auto arrive_tiles = [&](const Item &I) {
+      if constexpr (FUSED) {
+        named_barrier(1, kSmxThreads);
+        if (ts == 0) {
+          __threadfence();
+          for (int k = (I.b * p.q) / kCmbTile; k <= (I.b * p.q + p.q - 1) / kCmbTile; ++k) atomicAdd(p.ws + 2 + k, 1);
+        }
+      }
+    };
+    for (int k = 0; ok; ++k) {
+      bool got = true;
+      const int it = take(k, got);
+      __syncwarp();
+      if (lane == 0 && got) release(k);
+      // (also: the previous item's readers of lim_s / orow_s are done)
+      ok = named_barrier_and(1, kSmxThreads, got);
+      if (!ok || it >= nitems) break;
       const Item I = item_of(it);
-      named_barrier(1, kSmxThreads);  // the previous item's readers of lim_s / orow_s are done
       // per query row: the positions of this split it sees (counted from j0)
       // and its o / lse row (-1: a padded row)
       if (ts < N) {
@@ -356,6 +679,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
             for (int c = 0; c < 4; ++c) p.o[row * kD + 128 * c + pos] = 0;
         }
+        arrive_tiles(I);
         continue;
       }
       int lim[NC];
@@ -517,10 +841,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
       }
       tc_fence_before();
+      arrive_tiles(I);
     }
     // the next kernel on the stream may start its prologue
     grid_launch_dependents();
   }
+  if constexpr (FUSED) combine_phase<N>(p, wv_map, sbase, gbase, tmem, misc, s_abort, wv_full, cmb_mma, nitems);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -534,11 +860,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 int attn_heads_per_cta(int q, int H) { return q * H <= 32 ? H : (32 / q > 0 ? 32 / q : 1); }
 int attn_rows(int q, int H) { return ((q * attn_heads_per_cta(q, H) + 15) / 16) * 16; }
 size_t attn_smem_bytes(int rows) { return 1024 + (rows <= 16 ? AttnLayout<16>::total : AttnLayout<32>::total); }
+int attn_combine_tiles(int S) { return (S + kCmbTile - 1) / kCmbTile; }
 
-template <int N>
-static cudaError_t launch_attn_n(const AttnParams &p, const CUtensorMap &map, unsigned grid, cudaStream_t stream) {
-  const size_t smem = 1024 + AttnLayout<N>::total;
-  cudaError_t e = cudaFuncSetAttribute(attn_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+template <int N, bool FUSED>
+static cudaError_t launch_attn_n(const AttnParams &p, const CUtensorMap &map, const CUtensorMap &wv_map,
+                                 unsigned grid, cudaStream_t stream) {
+  const size_t smem = 1024 + AttnLayout<N, FUSED>::total;
+  cudaError_t e = cudaFuncSetAttribute(attn_kernel<N, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
@@ -550,7 +878,7 @@ static cudaError_t launch_attn_n(const AttnParams &p, const CUtensorMap &map, un
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, attn_kernel<N>, p, map);
+  e = cudaLaunchKernelEx(&cfg, attn_kernel<N, FUSED>, p, map, wv_map);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -563,7 +891,23 @@ cudaError_t launch_attn(const AttnParams &p, const CUtensorMap &map, int num_sms
   const unsigned grid = (unsigned)(items < num_sms ? items : num_sms);
   const int rows = ((p.q * p.G + 15) / 16) * 16;  // the host keeps q G <= 32
   if (rows > 32) return cudaErrorInvalidValue;
-  return rows <= 16 ? launch_attn_n<16>(p, map, grid, stream) : launch_attn_n<32>(p, map, grid, stream);
+  CUtensorMap none;
+  std::memset(&none, 0, sizeof none);
+  return rows <= 16 ? launch_attn_n<16, false>(p, map, none, grid, stream)
+                    : launch_attn_n<32, false>(p, map, none, grid, stream);
+}
+
+// The fused attention + combine: one CTA per SM over the attention items and
+// then the combine units (ntiles * H), all drawn from the workspace queue.
+cudaError_t launch_attn_combine(const AttnParams &p, const CUtensorMap &map, const CUtensorMap &wv_map, int num_sms,
+                                cudaStream_t stream) {
+  const long long work = (long long)p.B * p.spr * p.groups + (long long)p.ntiles * p.H;
+  if (work <= 0 || work >= (1LL << 31) || num_sms < 1 || !p.ws) return cudaErrorInvalidValue;
+  const unsigned grid = (unsigned)(work < num_sms ? work : num_sms);
+  const int rows = ((p.q * p.G + 15) / 16) * 16;
+  if (rows > 32 || p.spr > 32) return cudaErrorInvalidValue;
+  return rows <= 16 ? launch_attn_n<16, true>(p, map, wv_map, grid, stream)
+                    : launch_attn_n<32, true>(p, map, wv_map, grid, stream);
 }
 
 }  // namespace mla

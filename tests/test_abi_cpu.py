@@ -169,6 +169,63 @@ def test_attn_validation_errors(lib):
     assert st(attn_args(B=0, qv=None, kv=None)) == m.MLA_OK  # nothing to do, nothing read
 
 
+def test_attn_combine_args_struct_layout_matches_header(lib, tmp_path):
+    fields = [f for f, _ in m.AttnCombineArgs._fields_]
+    prog = ["#include <stdio.h>", "#include <stddef.h>", '#include "mla_combine_uv.h"',
+            "int main(void) {", 'printf("%zu\\n", sizeof(mla_attn_combine_uv_args));']
+    prog += [f'printf("%zu\\n", offsetof(mla_attn_combine_uv_args, {f}));' for f in fields]
+    prog += ["return 0; }"]
+    src = tmp_path / "probe_fused.c"
+    src.write_text("\n".join(prog))
+    exe = tmp_path / "probe_fused"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                           check=True).stdout.split()]
+    assert vals[0] == ctypes.sizeof(m.AttnCombineArgs)
+    for f, off in zip(fields, vals[1:]):
+        assert getattr(m.AttnCombineArgs, f).offset == off, f
+
+
+def fused_args(B=4, q=1, H=12, spr=16, Lmax=256, **kw):
+    a = m.AttnCombineArgs()
+    a.B, a.q, a.H, a.spr, a.scale = B, q, H, spr, 0.07
+    a.qv, a.q_st, a.q_sh = ALIGNED, H * 576, 576
+    a.kv, a.kv_sb, a.kv_sl = ALIGNED * 2, Lmax * 576, 576
+    a.Lmax, a.kv_len = Lmax, ALIGNED * 3
+    a.part_o, a.part_lse = ALIGNED * 4, ALIGNED * 5
+    a.w_v, a.w_sh, a.w_sv = ALIGNED * 6, 128 * 512, 512
+    a.w_fmt = 0
+    a.gate, a.out, a.S_out = ALIGNED * 7, ALIGNED * 8, B * q
+    a.workspace, a.workspace_words = ALIGNED * 9, 2 + (B * q + 7) // 8
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_attn_combine_validation_errors(lib):
+    fn = lib.mla_attn_combine_uv
+    st = lambda a: fn(ctypes.byref(a), None)  # noqa: E731  (errors return before any CUDA call)
+    assert fn(None, None) == m.MLA_ERR_NULL
+    assert st(fused_args(w_fmt=1)) == m.MLA_ERR_FMT           # bf16 W_V only
+    assert st(fused_args(w_scale=ALIGNED)) == m.MLA_ERR_FMT
+    assert st(fused_args(B=-1)) == m.MLA_ERR_SHAPE
+    assert st(fused_args(q=33)) == m.MLA_ERR_SHAPE
+    assert st(fused_args(spr=33)) == m.MLA_ERR_SHAPE           # one lane per partial in the merge
+    assert st(fused_args(spr=0)) == m.MLA_ERR_SHAPE
+    assert st(fused_args(S_out=3)) == m.MLA_ERR_SHAPE          # S_out < S
+    assert st(fused_args(wait_ns=-1)) == m.MLA_ERR_SHAPE
+    assert st(fused_args(workspace_words=2)) == m.MLA_ERR_SHAPE
+    assert st(fused_args(workspace=None)) == m.MLA_ERR_NULL
+    assert st(fused_args(part_o=None)) == m.MLA_ERR_NULL
+    assert st(fused_args(out=ALIGNED + 8)) == m.MLA_ERR_ALIGN
+    assert st(fused_args(workspace=ALIGNED + 2)) == m.MLA_ERR_ALIGN
+    assert st(fused_args(w_sv=500)) == m.MLA_ERR_STRIDE
+    assert st(fused_args(kv_sl=568)) == m.MLA_ERR_STRIDE
+    for B, q in ((0, 1), (1, 1), (8, 1), (9, 1), (64, 1), (3, 3), (1024, 4)):
+        assert lib.mla_attn_combine_uv_workspace_words(B, q) == 2 + (B * q + 7) // 8
+    assert lib.mla_attn_combine_uv_workspace_words(-1, 1) == -1
+
+
 def test_oproj_args_struct_layout_matches_header(lib, tmp_path):
     fields = [f for f, _ in m.OprojArgs._fields_]
     prog = ["#include <stdio.h>", "#include <stddef.h>", '#include "mla_combine_uv.h"',
