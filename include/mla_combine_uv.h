@@ -74,8 +74,11 @@ enum {
   MLA_ERR_TIMEOUT = 8, /* a kernel gave up a bounded wait (reported by
                           mla_combine_uv_status)                              */
   MLA_ERR_KERNEL = 9,  /* the requested kernel cannot run this problem        */
-  MLA_ERR_DATA = 10    /* a kernel met invalid device data: a kv_len outside
+  MLA_ERR_DATA = 10,   /* a kernel met invalid device data: a kv_len outside
                           [0, Lmax] (reported by mla_combine_uv_status)       */
+  MLA_ERR_SCRATCH = 11 /* mla_attn_combine_uv_noalloc: the problem needs more
+                          scratch than the library's fixed device buffer holds
+                          (nothing launched)                                  */
 };
 
 /* Kernel selection. */
@@ -396,6 +399,35 @@ int64_t mla_attn_combine_uv_workspace_words(int32_t B, int32_t q);
  * (Added in ABI version 5.)
  */
 int32_t mla_attn_combine_uv(const mla_attn_combine_uv_args *args, void *stream);
+
+/*
+ * mla_attn_combine_uv_noalloc -- the same decode step as mla_attn_combine_uv,
+ * for callers that cannot allocate device memory when they run it (a serving
+ * engine that hands nearly all free device memory to its KV cache at start-up
+ * and may not allocate afterwards; a decode loop that cannot afford the
+ * device-wide synchronisation cudaMalloc can cause).  The pages have no
+ * counterpart to this call: it exists for those callers only.
+ *
+ * The caller passes the inputs and `out` as for mla_attn_combine_uv; the
+ * fields part_o, part_lse, workspace and workspace_words are not read.  The
+ * step's scratch (the partials and the work-queue / arrival counters) lives
+ * in one fixed 16 MiB device array inside the library, which every device
+ * that loads the library holds until the process exits; the call allocates
+ * nothing and calls no allocating routine.  Limits: 16 KiB of counters
+ * (B*q <= 32752 tokens) and spr * B*q * H * (1024 + 4) bytes of partials
+ * (LSE rounded up to 256 bytes) within the remaining 16 MiB - 16 KiB; a
+ * bigger problem returns MLA_ERR_SCRATCH before anything is launched (the
+ * decode step of 64 requests x 12 heads x 16 splits needs 12.6 MB).
+ *
+ * The array is shared by every call on a device, and keeps the last call's
+ * contents: calls whose work overlaps on the GPU race on it (undefined
+ * results), so run them one after another.  The first call on a device does
+ * the set-up -- it looks the array's address up and clears its counters (a
+ * memset on `stream`, ahead of the kernel) -- so make that first call before
+ * any stream capture.  Every call leaves the counters zero.  Returns as
+ * mla_attn_combine_uv does, plus MLA_ERR_SCRATCH.
+ */
+int32_t mla_attn_combine_uv_noalloc(const mla_attn_combine_uv_args *args, void *stream);
 
 /* A short English description of a status code (static storage). */
 const char *mla_status_str(int32_t status);

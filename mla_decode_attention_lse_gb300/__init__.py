@@ -36,10 +36,12 @@ MLA_ERR_CUDA = 7
 MLA_ERR_TIMEOUT = 8
 MLA_ERR_KERNEL = 9
 MLA_ERR_DATA = 10
+MLA_ERR_SCRATCH = 11
 
 EXPORTED_SYMBOLS = ("mla_combine_uv", "mla_combine_uv_plan", "mla_combine_uv_status",
                     "mla_dcp_pack", "mla_attn_split_kv", "mla_o_proj", "mla_status_str", "mla_abi_version",
-                    "mla_calib_stream_read", "mla_attn_combine_uv", "mla_attn_combine_uv_workspace_words")
+                    "mla_calib_stream_read", "mla_attn_combine_uv", "mla_attn_combine_uv_workspace_words",
+                    "mla_attn_combine_uv_noalloc")
 
 
 class MlaError(RuntimeError):
@@ -170,6 +172,8 @@ def load_library(path: str | None = None):
     L.mla_attn_combine_uv.argtypes = [ctypes.POINTER(AttnCombineArgs), ctypes.c_void_p]
     L.mla_attn_combine_uv_workspace_words.restype = ctypes.c_int64
     L.mla_attn_combine_uv_workspace_words.argtypes = [ctypes.c_int32, ctypes.c_int32]
+    L.mla_attn_combine_uv_noalloc.restype = ctypes.c_int32
+    L.mla_attn_combine_uv_noalloc.argtypes = [ctypes.POINTER(AttnCombineArgs), ctypes.c_void_p]
     L.mla_calib_stream_read.restype = ctypes.c_int32
     L.mla_calib_stream_read.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p,
                                         ctypes.c_void_p]
@@ -421,6 +425,32 @@ def mla_attn_combine_uv(qv, kv, kv_len, q, spr, scale, part_o, part_lse, w_v, ga
     st = load_library().mla_attn_combine_uv(ctypes.byref(a), ctypes.c_void_p(s))
     if st != MLA_OK:
         raise MlaError(st, "mla_attn_combine_uv")
+
+
+def mla_attn_combine_uv_noalloc(qv, kv, kv_len, q, spr, scale, w_v, gate, out, stream=None, wait_ns=0) -> None:
+    """The fused decode step for callers that cannot allocate device memory
+    when they run it: the same inputs and output as ``mla_attn_combine_uv``,
+    the scratch (partials and counters) in the library's fixed 16 MiB device
+    buffer.  Calls that overlap on the GPU race on that buffer."""
+    import torch
+
+    S, H, _ = qv.shape
+    if stream is None:
+        stream = torch.cuda.current_stream(qv.device)
+    s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    B, Lmax, _ = kv.shape
+    a = AttnCombineArgs()
+    a.B, a.q, a.H, a.spr, a.scale = B, q, H, spr, float(scale)
+    a.qv, a.q_st, a.q_sh = _ptr(qv), qv.stride(0), qv.stride(1)
+    a.kv, a.kv_sb, a.kv_sl = _ptr(kv), kv.stride(0), kv.stride(1)
+    a.Lmax, a.kv_len = Lmax, _ptr(kv_len)
+    a.w_v, a.w_sh, a.w_sv = _ptr(w_v), w_v.stride(0), w_v.stride(1)
+    a.w_fmt = MLA_W_BF16
+    a.gate, a.out, a.S_out = _ptr(gate), _ptr(out), out.shape[0]
+    a.wait_ns = wait_ns
+    st = load_library().mla_attn_combine_uv_noalloc(ctypes.byref(a), ctypes.c_void_p(s))
+    if st != MLA_OK:
+        raise MlaError(st, "mla_attn_combine_uv_noalloc")
 
 
 def make_oproj_args(x, w, out) -> OprojArgs:

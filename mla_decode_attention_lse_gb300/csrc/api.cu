@@ -328,6 +328,7 @@ const char *mla_status_str(int32_t s) {
     case MLA_ERR_TIMEOUT: return "a kernel abandoned a bounded wait";
     case MLA_ERR_KERNEL: return "the requested kernel cannot run this problem";
     case MLA_ERR_DATA: return "a kernel met invalid device data (a kv_len outside [0, Lmax])";
+    case MLA_ERR_SCRATCH: return "the problem needs more scratch than the library's fixed device buffer holds";
     default: return "unknown status";
   }
 }

@@ -44,7 +44,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_abi_version_and_status_strings(lib):
     assert m.mla_abi_version() == 5
-    for s in range(0, 11):
+    for s in range(0, 12):
         assert m.mla_status_str(s) and m.mla_status_str(s) != "unknown status"
     assert m.mla_status_str(99) == "unknown status"
 
