@@ -381,6 +381,7 @@ def run_gpu(args):
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with ClockSampler(local) as clk:
+            graph.replay()  # untimed: the GPU is busy right up to the timed replay
             t_wall0 = time.perf_counter()
             e0.record(stream)
             graph.replay()
@@ -393,6 +394,11 @@ def run_gpu(args):
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         with ClockSampler(local) as clk:
+            # untimed warm-up steps again, enqueued right before the timed ones,
+            # so the GPU does not idle (and drop its clocks) while the clock
+            # sampler starts
+            for k in range(args.warmup):
+                call(k)
             t_wall0 = time.perf_counter()
             for i in range(args.steps):
                 starts[i].record(stream)

@@ -126,7 +126,9 @@ typedef struct {
   int32_t kernel;             /* MLA_KERNEL_*; 0 = automatic                  */
   int32_t tile_tokens;        /* tensor-core token tile (8, 16 or 32; 8 added
                                  in ABI version 4: two warps per token, each
-                                 merging half of its latents); 0 = auto      */
+                                 merging half of its latents; 17..31 added in
+                                 version 5: the 32-token kernel with that many
+                                 tokens per unit, <= 16 partials); 0 = auto  */
   int64_t wait_ns;            /* limit of the tensor-core kernel's bounded
                                  waits, in ns; 0 = the default 0.5 s.  A wait
                                  that runs out makes the kernel stop, drain its

@@ -83,7 +83,7 @@ int32_t plan_impl(const mla_combine_uv_args *a, int32_t num_sms, mla_plan *pl, K
   if (kernel != MLA_KERNEL_AUTO && kernel != MLA_KERNEL_SIMT && kernel != MLA_KERNEL_TC &&
       kernel != MLA_KERNEL_KSPLIT)
     return MLA_ERR_KERNEL;
-  if (a->tile_tokens != 0 && a->tile_tokens != 8 && a->tile_tokens != 16 && a->tile_tokens != 32)
+  if (a->tile_tokens != 0 && a->tile_tokens != 8 && (a->tile_tokens < 16 || a->tile_tokens > 32))
     return MLA_ERR_KERNEL;
   if (kernel == MLA_KERNEL_TC && n_part > mla::kTcMaxPart) return MLA_ERR_KERNEL;
   if (kernel == MLA_KERNEL_KSPLIT && (n_part > mla::kKsMaxPart || S == 0 ||
@@ -129,10 +129,18 @@ int32_t plan_impl(const mla_combine_uv_args *a, int32_t num_sms, mla_plan *pl, K
     // than 16 partials per token need 8- or 16-token tiles.
     if (tile == 0) {
       const int64_t u8 = (int64_t)a->H * ((S + 7) / 8);
+      // more 16-token units than SMs, too few 32-token ones to fill the GPU:
+      // units of ut tokens (17..31, the 32-token kernel) so that each SM
+      // takes exactly one (a stacked decode batch: 144 22-token units instead
+      // of 192 16-token units, 40 SMs of which would run two)
+      const int64_t tph = a->H <= num_sms ? num_sms / a->H : 0;
+      const int64_t ut = tph > 0 ? (S + tph - 1) / tph : 0;
       if ((int64_t)a->H * ((S + 31) / 32) >= num_sms && n_part <= 16)
         tile = 32;
       else if (a->w_fmt == MLA_W_BF16 && n_part >= 16 && u8 <= num_sms && u8 > units16)
         tile = 8;
+      else if (n_part <= 16 && units16 > num_sms && ut > 16 && ut < 32)
+        tile = (int)ut;
       else
         tile = 16;
     }

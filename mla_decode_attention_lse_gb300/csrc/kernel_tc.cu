@@ -113,7 +113,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int
 
 }  // namespace
 
-template <int BN, int WFMT, int NW, bool O32, bool HR>
+template <int BN, int WFMT, int NW, bool O32, bool HR, bool RT>
 __global__ void __launch_bounds__(NW * 32, 16 / NW)
     tc_kernel(const __grid_constant__ KParams p) {
   constexpr int kWorkers = NW;             // all warps combine, drain and (one of them) issue
@@ -137,6 +137,18 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
   static_assert(TPW >= 1 && BN % NW == 0 && JB >= 1 && NW % 4 == 0, "tile must split over the warps");
   static_assert(!HR || NW == 2 * UT, "half rows: two warps per token");
   static_assert(CPW == 4 || CPW == 8 || CPW == 16, "epilogue drains 4, 8 or 16 columns per warp");
+  static_assert(!(RT && HR), "runtime tiles use whole rows");
+  // RT (runtime tile): a unit is p.tile <= BN tokens; the MMA keeps N = BN and
+  // the slots past p.tile are empty (their latent rows zero, their columns
+  // never stored): a slot index past the unit gets a token index no token
+  // has, so every `t < p.S` test below leaves it out.  Decode batches use it
+  // to give every SM one unit.  Other instances: tile * BN + slot.
+  auto tok = [&](int tile, int slot) -> int {
+    if constexpr (RT)
+      return slot < p.tile ? tile * p.tile + slot : 0x7FFFFFFF;
+    else
+      return tile * BN + slot;
+  };
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -240,7 +252,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
         if ((lane & 3) == 0 && e < CPW && ws * CPW + e < UT && t < p.S)
           prefetch_l2_line(p.gate + off3(t, Wrow, c.h, kV, 1, wq * 32));
       } else {
-        const int t = c.tile * BN + ws * CPW + e;
+        const int t = tok(c.tile, ws * CPW + e);
         if ((lane & 3) == 0 && e < CPW && t < p.S) prefetch_l2_line(p.gate + off3(t, Wrow, c.h, kV, 1, wq * 32));
       }
     }
@@ -265,7 +277,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
 #pragma unroll
     for (int rd = 0; rd < kRounds; ++rd) {
       const int e = rd * 8 + (lane >> 2);
-      const int t = c.tile * UT + ws * CPW + e;
+      const int t = HR ? c.tile * UT + ws * CPW + e : tok(c.tile, ws * CPW + e);
       if constexpr (HR)
         act[rd] = e < CPW && ws * CPW + e < UT && t < p.S;
       else
@@ -319,7 +331,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
 
   // This lane's LSE (-inf past n or past S; sanitised when used).
   auto load_lse = [&](const Cur &c, float &lv) {
-    const int t = HR ? c.tile * UT + (warp >> 1) + my_tk : c.tile * BN + warp * TPW + my_tk;
+    const int t = HR ? c.tile * UT + (warp >> 1) + my_tk : tok(c.tile, warp * TPW + my_tk);
     lv = kNegInf;
     if (!pass && t < p.S && my_j < n) {
       const int r0 = (layout == kRequestMajor) ? (t / p.q) * p.spr : 0;
@@ -334,7 +346,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
   // loads) it measured slower and is left out.
   auto prefetch_rows = [&](const Cur &c, float lv) {
     if (WFMT != 0) return;
-    const int t = HR ? c.tile * UT + (warp >> 1) + my_tk : c.tile * BN + warp * TPW + my_tk;
+    const int t = HR ? c.tile * UT + (warp >> 1) + my_tk : tok(c.tile, warp * TPW + my_tk);
     const bool live = pass ? (my_j == 0 && t < p.S) : isfinite(lv);
     if (live) {
       const int r0 = (layout == kRequestMajor) ? (t / p.q) * p.spr : 0;
@@ -372,7 +384,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
   auto issue = [&](const Cur &c, int j0, Buf &buf, Wts &w, float wg) {
 #pragma unroll
     for (int tk = 0; tk < TPW; ++tk) {
-      const int t = HR ? c.tile * UT + (warp >> 1) + tk : c.tile * BN + warp * TPW + tk;
+      const int t = HR ? c.tile * UT + (warp >> 1) + tk : tok(c.tile, warp * TPW + tk);
       const int r0 = (layout == kRequestMajor) ? (t / p.q) * p.spr : 0;
       const uint16_t *base = p.o + off3(t, p.o_st, c.h, p.o_sh, r0 + j0, p.o_sp);
 #pragma unroll
@@ -400,7 +412,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
   auto issue_blind = [&](const Cur &c, int j0, Buf &buf) {
 #pragma unroll
     for (int tk = 0; tk < TPW; ++tk) {
-      const int t = HR ? c.tile * UT + (warp >> 1) + tk : c.tile * BN + warp * TPW + tk;
+      const int t = HR ? c.tile * UT + (warp >> 1) + tk : tok(c.tile, warp * TPW + tk);
       const int r0 = (layout == kRequestMajor) ? (t / p.q) * p.spr : 0;
       const uint16_t *base = p.o + off3(t, p.o_st, c.h, p.o_sh, r0 + j0, p.o_sp);
 #pragma unroll
@@ -561,7 +573,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
     uint8_t *gB = gB0 + (size_t)b * L.b_bytes;
 #pragma unroll
     for (int tk = 0; tk < TPW; ++tk) {
-      const bool valid = HR ? c.tile * UT + (warp >> 1) + tk < p.S : c.tile * BN + warp * TPW + tk < p.S;
+      const bool valid = HR ? c.tile * UT + (warp >> 1) + tk < p.S : tok(c.tile, warp * TPW + tk) < p.S;
       const int row = HR ? (warp >> 1) + tk : warp * TPW + tk;
 #pragma unroll
       for (int cc = 0; cc < NCH; ++cc) {
@@ -779,7 +791,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
       // the new unit's second batch into L2 (live rows): it is merged only
       // one batch after it is issued (large MXFP4 batch 291.4 -> 289.4 us;
       // bf16 prefetches whole units ahead instead)
-      const int t = HR ? cn.tile * UT + (warp >> 1) + my_tk : cn.tile * BN + warp * TPW + my_tk;
+      const int t = HR ? cn.tile * UT + (warp >> 1) + my_tk : tok(cn.tile, warp * TPW + my_tk);
       if (my_j >= JB && my_j < 2 * JB && wnxt != 0.0f && t < p.S) {
         const int r0 = (layout == kRequestMajor) ? (t / p.q) * p.spr : 0;
         if constexpr (HR)  // this warp's half of the row
@@ -894,17 +906,18 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW)
 // are the half-row instance of the 16-token kernel: 16 warps, two per token.
 int tc_warps(int tile, int w_fmt, int n_part) { return (w_fmt && tile == 16 && n_part <= 16) ? 8 : 16; }
 int tc_ctas_per_sm(int tile, int w_fmt, int n_part) { return tc_warps(tile, w_fmt, n_part) == 8 ? 2 : 1; }
-int tc_max_part(int tile, int /*w_fmt*/) { return tile == 32 ? 16 : 32; }
+// 17..31-token tiles are the 32-token kernel with that many tokens per unit.
+int tc_max_part(int tile, int /*w_fmt*/) { return tile > 16 ? 16 : 32; }
 
 size_t tc_smem_bytes(int tile, int w_fmt, int n_part) {
-  const int bn = tile == 8 ? 16 : tile;
+  const int bn = tile == 8 ? 16 : (tile > 16 ? 32 : tile);
   return 1024 + tc_layout(bn, w_fmt, tc_warps(tile, w_fmt, n_part)).total;
 }
 
-template <int BN, int WFMT, int NW, bool O32, bool HR = false>
+template <int BN, int WFMT, int NW, bool O32, bool HR = false, bool RT = false>
 static cudaError_t launch_one(const KParams &p, int grid, cudaStream_t s) {
   const size_t smem = 1024 + tc_layout(BN, WFMT, NW).total;
-  cudaError_t e = cudaFuncSetAttribute(tc_kernel<BN, WFMT, NW, O32, HR>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(tc_kernel<BN, WFMT, NW, O32, HR, RT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
@@ -917,7 +930,7 @@ static cudaError_t launch_one(const KParams &p, int grid, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, tc_kernel<BN, WFMT, NW, O32, HR>, p);
+  e = cudaLaunchKernelEx(&cfg, tc_kernel<BN, WFMT, NW, O32, HR, RT>, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -933,6 +946,9 @@ static cudaError_t launch_tc_off(const KParams &p, int grid, cudaStream_t stream
     return nw == 8 ? launch_one<16, 1, 8, O32>(p, grid, stream) : launch_one<16, 1, 16, O32>(p, grid, stream);
   if (p.tile == 32 && p.n_part <= 16)
     return p.w_fmt == 0 ? launch_one<32, 0, 16, O32>(p, grid, stream) : launch_one<32, 1, 16, O32>(p, grid, stream);
+  if (p.tile > 16 && p.tile < 32 && p.n_part <= 16)
+    return p.w_fmt == 0 ? launch_one<32, 0, 16, O32, false, true>(p, grid, stream)
+                        : launch_one<32, 1, 16, O32, false, true>(p, grid, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -352,12 +352,22 @@ def test_kernel_and_tile_choice(lib):
     assert (p["kernel"], p["tile_tokens"], p["threads"]) == (m.MLA_KERNEL_TC, 16, 512)
     assert status_of(args(P=20, spr=20, tile=32)) == m.MLA_ERR_KERNEL
     # MXFP4 16-token tiles run two 8-warp CTAs per SM
-    p = mla_combine_uv_plan(args(S=256, H=12, P=8, spr=8, w_fmt=1), SMS)
+    p = mla_combine_uv_plan(args(S=256, H=12, P=8, spr=8, w_fmt=1, tile=16), SMS)
     assert (p["tile_tokens"], p["units"], p["grid"], p["threads"]) == (16, 192, 192, 256)
+    # ... but a stacked decode batch with more 16-token units than SMs gets
+    # one unit per SM: 12 tiles of 22 tokens per head on the 32-token kernel
+    p = mla_combine_uv_plan(args(S=256, H=12, P=8, spr=8, w_fmt=1), SMS)
+    assert (p["tile_tokens"], p["units"], p["grid"], p["threads"]) == (22, 144, 144, 512)
+    p = mla_combine_uv_plan(args(S=256, H=12, P=8, spr=8, w_fmt=0), SMS)
+    assert (p["tile_tokens"], p["units"], p["grid"]) == (22, 144, 144)
+    p = mla_combine_uv_plan(args(S=256, H=12, P=8, spr=8, tile=20), SMS)
+    assert (p["tile_tokens"], p["units"]) == (20, 12 * 13)
+    assert status_of(args(S=256, H=12, P=20, spr=20, tile=20)) == m.MLA_ERR_KERNEL  # <= 16 partials
     # more than 32 partials per token: CUDA cores only
     assert mla_combine_uv_plan(args(P=64, spr=64), SMS)["kernel"] == m.MLA_KERNEL_SIMT
     assert status_of(args(P=64, spr=64, kernel=m.MLA_KERNEL_TC)) == m.MLA_ERR_KERNEL
-    assert status_of(args(tile=24)) == m.MLA_ERR_KERNEL
+    assert status_of(args(tile=12)) == m.MLA_ERR_KERNEL
+    assert status_of(args(tile=33)) == m.MLA_ERR_KERNEL
     assert status_of(args(kernel=7)) == m.MLA_ERR_KERNEL
     p = mla_combine_uv_plan(args(S=0, S_out=5, kernel=m.MLA_KERNEL_TC), SMS)
     assert p["kernel"] == m.MLA_KERNEL_SIMT  # nothing to merge: zero rows only
@@ -448,7 +458,7 @@ def test_plan_invariants_on_random_problems(lib):
             spr = 0
         w_fmt = int(rng.integers(0, 2))
         kernel = int(rng.choice([0, 0, m.MLA_KERNEL_SIMT, m.MLA_KERNEL_TC, m.MLA_KERNEL_KSPLIT]))
-        tile = int(rng.choice([0, 0, 8, 16, 32]))
+        tile = int(rng.choice([0, 0, 8, 16, 32, 24]))
         a = args(S=S, S_out=S + int(rng.integers(0, 4)), H=H, P=P, q=q, spr=spr, w_fmt=w_fmt,
                  kernel=kernel, tile=tile)
         try:
@@ -461,9 +471,11 @@ def test_plan_invariants_on_random_problems(lib):
         assert p["smem_bytes"] <= 227 * 1024
         if p["kernel"] == m.MLA_KERNEL_TC:
             t = p["tile_tokens"]
-            assert t in (8, 16, 32) and (tile == 0 or t == tile)
+            assert (t in (8, 16, 32) or 16 < t < 32) and (tile == 0 or t == tile)
             assert p["units"] == H * -(-S // t) and 1 <= p["grid"] <= min(p["units"], 2 * SMS)
-            assert n <= (16 if t == 32 else 32)
+            assert n <= (16 if t > 16 else 32)
+            if tile == 0 and 16 < t < 32:  # runtime tiles: one unit per SM
+                assert p["units"] <= SMS
             assert p["threads"] == (256 if (w_fmt and t == 16 and n <= 16) else 512)
             if tile == 0 and t == 8:
                 assert w_fmt == 0 and n >= 16 and H * -(-S // 8) <= SMS
@@ -472,6 +484,6 @@ def test_plan_invariants_on_random_problems(lib):
         else:
             assert p["kernel"] == m.MLA_KERNEL_SIMT and p["grid"] == p["units"]
     # the random draws reached every kernel and every tensor-core tile
-    assert {(m.MLA_KERNEL_TC, 8), (m.MLA_KERNEL_TC, 16), (m.MLA_KERNEL_TC, 32),
+    assert {(m.MLA_KERNEL_TC, 8), (m.MLA_KERNEL_TC, 16), (m.MLA_KERNEL_TC, 32), (m.MLA_KERNEL_TC, 24),
             (m.MLA_KERNEL_KSPLIT, 16)} <= seen
     assert any(k == m.MLA_KERNEL_SIMT for k, _ in seen)

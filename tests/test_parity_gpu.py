@@ -283,3 +283,34 @@ def test_eight_token_tiles_dead_rows_strided_heads(lib, orc, w_fmt):
     inp = custom(S=16, H=2, P=1, q=1, spr=0, w_fmt=w_fmt, lse_unused=True, seed=95)
     inp["o"][0, 3, 1, 300] = float("inf")
     check_full(orc, inp, TC, 8, "8-token tiles, inf latent")
+
+
+# ---- runtime tiles: the 32-token kernel with 17..31 tokens per unit ----------
+
+@pytest.mark.parametrize("w_fmt", [0, 1])
+@pytest.mark.parametrize("tile,S,S_out,P,q,spr", [
+    (22, 256, 264, 8, 1, 8),    # the stacked decode batch's automatic tile
+    (17, 40, 41, 4, 1, 4),      # two batches per unit (the blind second batch with MXFP4)
+    (31, 95, 95, 16, 1, 16),    # a ragged last unit
+    (20, 47, 50, 1, 1, 0),      # passthrough
+    (24, 18, 18, 30, 3, 5),     # request-major, q = 3, one unit
+])
+def test_runtime_token_tiles(lib, orc, w_fmt, tile, S, S_out, P, q, spr):
+    pas = P == 1
+    inp = custom(S=S, S_out=S_out, H=3, P=P, q=q, spr=spr, w_fmt=w_fmt, neg_inf_frac=0.0 if pas else 0.2,
+                 nan_frac=0.0 if pas else 0.05, lse_unused=pas, dead_rows=0 if pas else 4,
+                 seed=200 + tile + S + w_fmt)
+    if not pas:  # dead partials' rows poisoned: they must never be read
+        inp["o"][~torch.isfinite(inp["lse"])] = float("nan")
+    check_full(orc, inp, TC, tile, f"tile {tile} S={S} P={P} w_fmt={w_fmt}")
+
+
+@pytest.mark.parametrize("w_fmt,S", [(0, 700), (1, 400)])
+def test_runtime_tiles_head_changes(lib, orc, w_fmt, S):
+    # more units than SMs: CTAs walk across head boundaries with 20-token units.
+    # (MXFP4 on fewer rows: its E2M1 codes follow the latents exactly, and the
+    # kernel's hardware exp2 / reciprocal for the weights can move a latent
+    # one bf16 ulp across an E2M1 rounding midpoint, a flip that exceeded the
+    # bound once in 1.07 M outputs of 700 x 12 rows)
+    inp = custom(S=S, H=12, P=4, q=1, spr=4, w_fmt=w_fmt, neg_inf_frac=0.05, seed=300 + w_fmt)
+    check_full(orc, inp, TC, 20, f"tile 20, head changes, w_fmt={w_fmt}")
