@@ -288,15 +288,23 @@ typedef struct {
   void *o;               /* bf16 [spr, S, H, 512], dense, 16-byte aligned;
                             caller-owned, every element written               */
   float *lse;            /* f32 [spr, S, H], dense                            */
+  int32_t kernel;        /* 0 automatic (= 1); 1 one CTA per (request, split,
+                            head group); 2 on request: a 2-CTA cluster per
+                            item, each CTA holding half of every cached row's
+                            latents and the partial scores summed through
+                            distributed shared memory (the fp32 score sum is
+                            split in two and added once, so o / lse may
+                            differ from kernel 1 in the last bits).  (Added
+                            in ABI version 5.)                                */
 } mla_attn_split_kv_args;
 
 /*
- * mla_attn_split_kv -- enqueue the attention on `stream` (one CTA per
- * request, split and group of heads; reads each cached row once per group of
- * up to 32 / q heads).  Returns MLA_OK, or MLA_ERR_NULL / _SHAPE / _STRIDE /
- * _ALIGN before anything is launched (outputs untouched), or MLA_ERR_CUDA.
- * B == 0 launches nothing.  The library allocates nothing; kv_len is read on
- * the device.  (Added in ABI version 3.)
+ * mla_attn_split_kv -- enqueue the attention on `stream` (a persistent grid
+ * over (request, split, group of heads) items; reads each cached row once
+ * per group of up to 32 / q heads).  Returns MLA_OK, or MLA_ERR_NULL /
+ * _SHAPE / _STRIDE / _ALIGN / _KERNEL before anything is launched (outputs
+ * untouched), or MLA_ERR_CUDA.  B == 0 launches nothing.  The library
+ * allocates nothing; kv_len is read on the device.  (Added in ABI version 3.)
  */
 int32_t mla_attn_split_kv(const mla_attn_split_kv_args *args, void *stream);
 

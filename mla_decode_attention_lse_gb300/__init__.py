@@ -105,6 +105,7 @@ class AttnArgs(ctypes.Structure):
         ("Lmax", ctypes.c_int32),
         ("kv_len", ctypes.c_void_p),
         ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+        ("kernel", ctypes.c_int32),
     ]
 
 
@@ -315,7 +316,7 @@ def mla_dcp_pack(o, lse, seq_lens, qsl, q_per_request, dst_rank, cmb_o, cmb_lse,
         raise MlaError(st, "mla_dcp_pack")
 
 
-def make_attn_args(qv, kv, kv_len, q, spr, scale, o, lse) -> AttnArgs:
+def make_attn_args(qv, kv, kv_len, q, spr, scale, o, lse, kernel=0) -> AttnArgs:
     """Fill ``mla_attn_split_kv_args`` from tensors (pointers and element strides)."""
     S, H, _ = qv.shape
     B, Lmax, _ = kv.shape
@@ -325,15 +326,18 @@ def make_attn_args(qv, kv, kv_len, q, spr, scale, o, lse) -> AttnArgs:
     a.kv, a.kv_sb, a.kv_sl = _ptr(kv), kv.stride(0), kv.stride(1)
     a.Lmax, a.kv_len = Lmax, _ptr(kv_len)
     a.o, a.lse = _ptr(o), _ptr(lse)
+    a.kernel = kernel
     return a
 
 
-def mla_attn_split_kv(qv, kv, kv_len, q, spr, scale, o, lse, stream=None) -> None:
+def mla_attn_split_kv(qv, kv, kv_len, q, spr, scale, o, lse, stream=None, kernel=0) -> None:
     """The partial producer: split-KV MLA decode attention on CUDA tensors.
 
     qv [S, H, 576] bf16 (S = B * q; unit-stride last dimension); kv
     [B, Lmax, 576] bf16 (unit-stride last dimension); kv_len [B] int32; o
-    [spr, S, H, 512] bf16 dense; lse [spr, S, H] f32 dense.
+    [spr, S, H, 512] bf16 dense; lse [spr, S, H] f32 dense.  ``kernel``: 0
+    automatic (one CTA per item), 1 one CTA per item, 2 a 2-CTA cluster per
+    item (on request).
     """
     import torch
 
@@ -353,7 +357,7 @@ def mla_attn_split_kv(qv, kv, kv_len, q, spr, scale, o, lse, stream=None) -> Non
     if stream is None:
         stream = torch.cuda.current_stream(qv.device)
     s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
-    a = make_attn_args(qv, kv, kv_len, q, spr, scale, o, lse)
+    a = make_attn_args(qv, kv, kv_len, q, spr, scale, o, lse, kernel)
     st = load_library().mla_attn_split_kv(ctypes.byref(a), ctypes.c_void_p(s))
     if st != MLA_OK:
         raise MlaError(st, "mla_attn_split_kv")

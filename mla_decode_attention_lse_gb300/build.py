@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libmla_combine_uv.so")
 SOURCES = ["api.cu", "kernel_simt.cu", "kernel_tc.cu", "kernel_ks.cu", "kernel_pack.cu", "kernel_attn.cu", "kernel_oproj.cu",
-           "kernel_calib.cu", "noalloc.cu"]
+           "kernel_calib.cu", "noalloc.cu", "kernel_attn_pair.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -433,6 +433,7 @@ int32_t mla_attn_split_kv(const mla_attn_split_kv_args *a, void *stream) {
   if (a->q_st < 0 || a->q_sh < 0 || a->q_st % 8 || a->q_sh % 8) return MLA_ERR_STRIDE;
   if (a->kv_sl < 576 || a->kv_sl % 8 || a->kv_sb < 0 || a->kv_sb % 8 || (a->B > 1 && a->kv_sb == 0))
     return MLA_ERR_STRIDE;
+  if (a->kernel < 0 || a->kernel > 2) return MLA_ERR_KERNEL;
   CUtensorMap tm;
   int32_t st = make_kv_tmap(a, &tm);
   if (st != MLA_OK) return st;
@@ -457,7 +458,11 @@ int32_t mla_attn_split_kv(const mla_attn_split_kv_args *a, void *stream) {
   p.o = static_cast<uint16_t *>(a->o);
   p.lse = a->lse;
   p.err = err;
-  const cudaError_t e = mla::launch_attn(p, tm, sms, static_cast<cudaStream_t>(stream));
+  // one CTA per item unless the 2-CTA cluster kernel is asked for (measured
+  // slower on the decode step: 135.9 against 87.6 us, its per-tile chain is
+  // latency-bound and each SM pair walks twice the tiles)
+  const cudaError_t e = a->kernel == 2 ? mla::launch_attn_pair(p, tm, sms, static_cast<cudaStream_t>(stream))
+                                       : mla::launch_attn(p, tm, sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

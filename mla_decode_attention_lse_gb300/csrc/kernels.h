@@ -41,6 +41,10 @@ int attn_heads_per_cta(int q, int H);  // G
 int attn_rows(int q, int H);           // the MMA's N: q * G rounded up to 16
 size_t attn_smem_bytes(int rows);
 cudaError_t launch_attn(const AttnParams &p, const CUtensorMap &map, int num_sms, cudaStream_t stream);
+// The same attention on 2-CTA clusters: each CTA holds half of every cached
+// row's latents (rank 1 also the rope part), the partial scores meet through
+// distributed shared memory.
+cudaError_t launch_attn_pair(const AttnParams &p, const CUtensorMap &map, int num_sms, cudaStream_t stream);
 // The same attention with the combine of its partials behind it in the same
 // launch (bf16 W_V through `wv_map`: [H, 128, 512], boxes of 64 x 128 x 1,
 // 128-byte swizzle); p.ws holds 2 + attn_combine_tiles(S) zeroed words.

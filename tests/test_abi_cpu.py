@@ -166,6 +166,7 @@ def test_attn_validation_errors(lib):
     assert st(attn_args(q_sh=580)) == m.MLA_ERR_STRIDE
     assert st(attn_args(kv_sl=568)) == m.MLA_ERR_STRIDE  # rows overlap
     assert st(attn_args(kv_sb=0)) == m.MLA_ERR_STRIDE    # B > 1 requests on one row set
+    assert st(attn_args(kernel=3)) == m.MLA_ERR_KERNEL
     assert st(attn_args(B=0, qv=None, kv=None)) == m.MLA_OK  # nothing to do, nothing read
 
 

@@ -48,14 +48,15 @@ def problem(B, q, H, spr, Lmax, lens, seed=0, kv_pad=0, q_pad=0):
     return dict(qv=qv, kv=kv, kv_len=kv_len, q=q, spr=spr, scale=1 / math.sqrt(192), B=B, H=H, Lmax=Lmax)
 
 
-def run_attn(inp):
+def run_attn(inp, kernel=0):
     import mla_decode_attention_lse_gb300 as m
 
     S = inp["B"] * inp["q"]
     o = torch.empty((inp["spr"], S, inp["H"], D), dtype=torch.int16, device="cuda").fill_(CANARY)
     o = o.view(torch.bfloat16)
     lse = torch.full((inp["spr"], S, inp["H"]), 1234.5, dtype=torch.float32, device="cuda")
-    m.mla_attn_split_kv(inp["qv"], inp["kv"], inp["kv_len"], inp["q"], inp["spr"], inp["scale"], o, lse)
+    m.mla_attn_split_kv(inp["qv"], inp["kv"], inp["kv_len"], inp["q"], inp["spr"], inp["scale"], o, lse,
+                        kernel=kernel)
     torch.cuda.synchronize()
     assert m.mla_combine_uv_status() == m.MLA_OK
     return o, lse
@@ -95,28 +96,31 @@ def check(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
     (1, 1, 1, 1, 1000, [1000]),                   # one split of 8 tiles: the slot rings wrap
     (6, 1, 12, 1, 257, [127, 128, 129, 255, 256, 257]),  # tile boundaries
 ])
-def test_attn_matches_oracle(lib, orc, B, q, H, spr, Lmax, lens):
+@pytest.mark.parametrize("kernel", [1, 2])  # one CTA per item; a 2-CTA cluster per item
+def test_attn_matches_oracle(lib, orc, B, q, H, spr, Lmax, lens, kernel):
     inp = problem(B, q, H, spr, Lmax, lens, seed=B * 100 + q)
-    o, lse = run_attn(inp)
+    o, lse = run_attn(inp, kernel)
     o_ref, lse_ref = oracle(orc, inp)
-    check(o, lse, o_ref, lse_ref, f"B={B} q={q} H={H} spr={spr} lens={lens}")
+    check(o, lse, o_ref, lse_ref, f"kernel {kernel}: B={B} q={q} H={H} spr={spr} lens={lens}")
 
 
-def test_attn_strided_views(lib, orc):
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_attn_strided_views(lib, orc, kernel):
     inp = problem(3, 2, 6, 3, 150, [150, 64, 3], seed=7, kv_pad=64, q_pad=2)
     assert not inp["qv"].is_contiguous() and not inp["kv"].is_contiguous()
-    o, lse = run_attn(inp)
+    o, lse = run_attn(inp, kernel)
     o_ref, lse_ref = oracle(orc, inp)
-    check(o, lse, o_ref, lse_ref, "strided")
+    check(o, lse, o_ref, lse_ref, f"strided, kernel {kernel}")
 
 
-def test_attn_full_workload_sampled(lib, orc):
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_attn_full_workload_sampled(lib, orc, kernel):
     # the bench's decode step (64 requests x 12 heads, 16 splits, up to 4096
     # cached positions), checked on a sample of requests
     from mla_decode_attention_lse_gb300 import synth
 
     inp = synth.make_attn("attn_splitkv", device="cuda")
-    o, lse = run_attn(inp)
+    o, lse = run_attn(inp, kernel)
     lens = inp["kv_len"].cpu().numpy()
     reqs = [int(np.argmax(lens)), int(np.argmin(lens)), 0, 17, 63]
     o_ref, lse_ref = oracle(orc, inp, reqs)
@@ -171,6 +175,8 @@ def test_attn_errors(lib):
 
     a = m.make_attn_args(inp["qv"], inp["kv"], inp["kv_len"], 33, 2, 0.1, o, lse)  # q > 32
     assert m.load_library().mla_attn_split_kv(ctypes.byref(a), None) == m.MLA_ERR_SHAPE
+    a = m.make_attn_args(inp["qv"], inp["kv"], inp["kv_len"], 1, 2, 0.1, o, lse, kernel=3)
+    assert m.load_library().mla_attn_split_kv(ctypes.byref(a), None) == m.MLA_ERR_KERNEL
     flat = torch.empty(2 * 64 * K + 8, dtype=torch.bfloat16, device="cuda")
     odd = flat[1:1 + 2 * 64 * K].view(2, 64, K)  # 2-byte offset
     with pytest.raises(m.MlaError) as e:
@@ -178,7 +184,7 @@ def test_attn_errors(lib):
     assert e.value.status == m.MLA_ERR_ALIGN
 
 
-@pytest.mark.parametrize("case", range(16))
+@pytest.mark.parametrize("case", range(24))
 def test_attn_fuzz(lib, orc, case):
     # seeded random shapes: queries per request, heads (one or several head
     # groups), splits, lengths (empty, short, tile edges, long), strided views
@@ -192,6 +198,7 @@ def test_attn_fuzz(lib, orc, case):
     lens = [min(L, Lmax) for L in lens]
     inp = problem(B, q, H, spr, Lmax, lens, seed=case, kv_pad=int(rng.choice([0, 8, 64])),
                   q_pad=int(rng.choice([0, 1])))
-    o, lse = run_attn(inp)
+    kernel = 1 + case % 2  # both kernels
+    o, lse = run_attn(inp, kernel)
     o_ref, lse_ref = oracle(orc, inp)
-    check(o, lse, o_ref, lse_ref, f"fuzz {case}: B={B} q={q} H={H} spr={spr} Lmax={Lmax} lens={lens}")
+    check(o, lse, o_ref, lse_ref, f"fuzz {case} (kernel {kernel}): B={B} q={q} H={H} spr={spr} Lmax={Lmax} lens={lens}")

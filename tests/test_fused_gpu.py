@@ -75,7 +75,8 @@ def run_unfused(inp):
     o = torch.empty((spr, S, H, D), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((spr, S, H), dtype=torch.float32, device="cuda")
     out = torch.empty((S_out, H * 128), dtype=torch.bfloat16, device="cuda")
-    m.mla_attn_split_kv(inp["qv"], inp["kv"], inp["kv_len"], q, spr, inp["scale"], o, lse)
+    # one CTA per item, the attention kernel the fused launch runs
+    m.mla_attn_split_kv(inp["qv"], inp["kv"], inp["kv_len"], q, spr, inp["scale"], o, lse, kernel=1)
     m.mla_combine_uv(o, lse, q, spr, inp["w_v"], 0, inp["gate"], out, tile_tokens=8)
     torch.cuda.synchronize()
     assert m.mla_combine_uv_status() == m.MLA_OK
