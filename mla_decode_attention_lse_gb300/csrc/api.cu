@@ -97,14 +97,22 @@ int32_t plan_impl(const mla_combine_uv_args *a, int32_t num_sms, mla_plan *pl, K
   // kernel runs on request only
   if (kernel == MLA_KERNEL_AUTO) kernel = (n_part <= mla::kTcMaxPart) ? MLA_KERNEL_TC : MLA_KERNEL_SIMT;
   if (S == 0) kernel = MLA_KERNEL_SIMT;  // nothing to merge: zero rows only
-  if (kernel == MLA_KERNEL_SIMT && mla::simt_smem_bytes(n_part) > 200 * 1024) return MLA_ERR_KERNEL;
+  const bool simt_small = mla::simt_small_fits(S, n_part);
+  if (kernel == MLA_KERNEL_SIMT && !simt_small && mla::simt_smem_bytes(n_part) > 200 * 1024) return MLA_ERR_KERNEL;
   if (a->ready_flag && (kernel != MLA_KERNEL_TC || !aligned(a->ready_flag, 4))) return MLA_ERR_KERNEL;
 
   std::memset(pl, 0, sizeof *pl);
   pl->kernel = kernel;
   pl->layout = layout;
   pl->n_part = n_part;
-  if (kernel == MLA_KERNEL_SIMT) {
+  if (kernel == MLA_KERNEL_SIMT && simt_small) {
+    // small batches: one CTA per (head, 16 V rows), every token of the batch
+    pl->tile_tokens = S;
+    pl->units = mla::simt_small_grid(a->H);
+    pl->grid = pl->units;
+    pl->threads = 256;
+    pl->smem_bytes = (int32_t)mla::simt_small_smem_bytes();
+  } else if (kernel == MLA_KERNEL_SIMT) {
     pl->tile_tokens = 8;
     pl->units = a->H * ((a->S_out + 7) / 8);
     pl->grid = pl->units;
@@ -366,7 +374,7 @@ int32_t mla_combine_uv(const mla_combine_uv_args *args, void *stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (pl.kernel == MLA_KERNEL_SIMT) {
-    e = mla::launch_simt(kp, s);
+    e = mla::simt_small_fits(kp.S, kp.n_part) ? mla::launch_simt_small(kp, s) : mla::launch_simt(kp, s);
   } else if (pl.kernel == MLA_KERNEL_KSPLIT) {
     e = mla::launch_ks(kp, s);
   } else {

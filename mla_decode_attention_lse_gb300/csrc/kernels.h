@@ -11,6 +11,12 @@ namespace mla {
 // CUDA-core kernel: any number of partials per token.
 size_t simt_smem_bytes(int n_part);
 cudaError_t launch_simt(const KParams &p, cudaStream_t stream);
+// CUDA-core kernel for small batches (1 <= S <= 16, n_part <= 32): one CTA
+// per (head, 16 V rows).
+bool simt_small_fits(int S, int n_part);
+size_t simt_small_smem_bytes();
+int simt_small_grid(int H);
+cudaError_t launch_simt_small(const KParams &p, cudaStream_t stream);
 
 // Fused tcgen05 kernel: tile = 8, 16 or 32 tokens, n_part <= 32 (16 for 32-token tiles).
 constexpr int kTcMaxPart = 32;

@@ -151,6 +151,9 @@ def make(wl: Workload | str, device="cpu", seed: int | None = None, w_fmt: int |
     S, H, P = wl.S, wl.H, wl.P
 
     request_major = P > 1 and P != wl.spr
+    if request_major and (S % wl.q != 0 or P != (S // wl.q) * wl.spr):
+        # the layouts of mla_combine_uv: P == 1, P == spr, or P == (S / q) * spr
+        raise ValueError(f"P={P} is none of the layouts for S={S}, q={wl.q}, spr={wl.spr}")
     if request_major:
         # only token t's request's splits are ever read; everything else NaN
         o = torch.full((P, S, H, D), float("nan"), device=device, dtype=torch.bfloat16)

@@ -314,3 +314,29 @@ def test_runtime_tiles_head_changes(lib, orc, w_fmt, S):
     # bound once in 1.07 M outputs of 700 x 12 rows)
     inp = custom(S=S, H=12, P=4, q=1, spr=4, w_fmt=w_fmt, neg_inf_frac=0.05, seed=300 + w_fmt)
     check_full(orc, inp, TC, 20, f"tile 20, head changes, w_fmt={w_fmt}")
+
+
+# ---- CUDA cores for small batches: one CTA per (head, 16 V rows) ------------
+
+@pytest.mark.parametrize("w_fmt", [0, 1])
+@pytest.mark.parametrize("S,S_out,H,P,q,spr", [
+    (1, 1, 2, 3, 1, 3),       # one token
+    (3, 5, 12, 1, 1, 0),      # passthrough, padded rows
+    (8, 8, 12, 16, 1, 16),    # a split-KV decode batch of 8 tokens
+    (16, 20, 4, 32, 1, 32),   # 16 tokens (the layout's limit), 32 partials
+    (12, 12, 3, 24, 2, 4),    # request-major, q = 2
+])
+def test_small_batch_cuda_cores(lib, orc, w_fmt, S, S_out, H, P, q, spr):
+    import mla_decode_attention_lse_gb300 as m
+
+    pas = P == 1
+    inp = custom(S=S, S_out=S_out, H=H, P=P, q=q, spr=spr, w_fmt=w_fmt, neg_inf_frac=0.0 if pas else 0.2,
+                 nan_frac=0.0 if pas else 0.05, lse_unused=pas, dead_rows=0 if pas else min(2, S),
+                 seed=400 + S + P + w_fmt)
+    if not pas:  # dead partials' rows poisoned: they must never be read
+        inp["o"][~torch.isfinite(inp["lse"])] = float("nan")
+    a = m.make_args(inp["o"], inp["lse"], inp["q"], inp["spr"], inp["w_v"], w_fmt, inp["gate"],
+                    torch.empty(S_out, H * 128, dtype=torch.bfloat16, device="cuda"), inp["w_scale"], kernel=SIMT)
+    plan = m.mla_combine_uv_plan(a)
+    assert (plan["grid"], plan["tile_tokens"]) == (H * 8, S)  # the small-batch layout
+    check_full(orc, inp, SIMT, 0, f"small-batch CUDA cores S={S} P={P} w_fmt={w_fmt}")
