@@ -170,17 +170,20 @@ __device__ __forceinline__ void combine_phase(const AttnParams &p, const CUtenso
     const int tile = u / H, h = u - tile * H;
     const bool new_h = h != cur_h;
     if (threadIdx.x == 0) {
+      // W_V[h] first (a weight: it does not wait for the attention), so its
+      // copy overlaps the wait for the tile's partials
+      if (new_h) {
+        mbar_arrive_expect_tx(wv_full, 4u * kDblBytes);
+#pragma unroll 1
+        for (int kb = 0; kb < 8; ++kb) tma_load_3d(sA + (uint32_t)kb * 16384u, &wv_map, 64 * kb, 0, h, wv_full);
+        ++wv_issued;
+      }
       // every (request, split, head group) item of the requests the tile covers
       const int t_lo = tile * kCmbTile, t_hi = min(t_lo + kCmbTile, S) - 1;
       const int target = (t_hi / p.q - t_lo / p.q + 1) * p.spr * p.groups;
       if (!wait_count(p.ws + 2 + tile, target, p.wait_ns)) {
         atomicCAS(p.err, 0, kErrWaitTile);
         *s_abort = 1;
-      } else if (new_h) {
-        mbar_arrive_expect_tx(wv_full, 4u * kDblBytes);
-#pragma unroll 1
-        for (int kb = 0; kb < 8; ++kb) tma_load_3d(sA + (uint32_t)kb * 16384u, &wv_map, 64 * kb, 0, h, wv_full);
-        ++wv_issued;
       }
     }
     __syncthreads();
