@@ -601,15 +601,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (kq > 0) ok = attn_wait(q_free, (uint32_t)(kq - 1) & 1u, p.err, s_abort);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      for (int e = lane; e < N * (kAttnK / 8); e += 32) {
-        const int m = e / (kAttnK / 8), ch = e - m * (kAttnK / 8);
-        const int i = m / p.G, h = I.g * p.G + (m - i * p.G);
-        const uint32_t dst = sbase + L::q_off + (uint32_t)((ch >> 3) * (N * 128) + m * 128 + (((ch & 7) ^ (m & 7)) << 4));
-        if (m < qG && h < p.H)
-          cp_async_16(dst, reinterpret_cast<const uint4 *>(p.qv + (long long)(I.b * p.q + i) * p.q_st +
-                                                           (long long)h * p.q_sh) + ch);
-        else
-          *reinterpret_cast<uint4 *>(gbase + (dst - sbase)) = make_uint4(0u, 0u, 0u, 0u);
+      // row by row (token i, head g G + hh of the row kept incrementally: no
+      // division per chunk), a lane per 16-byte chunk
+      int i = 0, hh = 0;
+      for (int m = 0; m < N; ++m) {
+        const int h = I.g * p.G + hh;
+        const bool live = m < qG && h < p.H;
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.qv + (long long)(I.b * p.q + i) * p.q_st +
+                                                           (long long)h * p.q_sh);
+        for (int ch = lane; ch < kAttnK / 8; ch += 32) {
+          const uint32_t dst = sbase + L::q_off + (uint32_t)((ch >> 3) * (N * 128) + m * 128 + (((ch & 7) ^ (m & 7)) << 4));
+          if (live)
+            cp_async_16(dst, src + ch);
+          else
+            *reinterpret_cast<uint4 *>(gbase + (dst - sbase)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (++hh == p.G) {
+          hh = 0;
+          ++i;
+        }
       }
       cp_async_commit();
       cp_async_wait<0>();
