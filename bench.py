@@ -41,6 +41,7 @@ L2_DEFEAT_BYTES = 256 << 20  # working set per rotation, about twice the 129 MB 
 # are the denominators of `frac`)
 NOMINAL_HBM_GBS = 7900.0            # HBM3e, nominal
 NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25  # dense tensor-core rates, nominal
+OPROJ_N_OUT = 7168  # o_proj outputs of the decode step (the hidden size; K = 12 heads x 128)
 
 
 def nominal_hbm(achieved_gbs: float) -> dict:
@@ -986,16 +987,30 @@ def run_gpu_attn(args):
     B, q, H, spr = wl.B, wl.q, wl.H, wl.spr
     S = B * q
 
-    def with_bufs(c):
+    n_out = OPROJ_N_OUT
+
+    def with_bufs(c, seed=0):
         c["o"] = torch.empty(spr, S, H, 512, dtype=torch.bfloat16, device=dev)
         c["lse"] = torch.empty(spr, S, H, dtype=torch.float32, device=dev)
         c["out"] = torch.empty(S, H * 128, dtype=torch.bfloat16, device=dev)
         c["ws"] = torch.zeros(m.mla_attn_combine_uv_workspace_words(B, q), dtype=torch.int32, device=dev)
+        # the o_proj shard's weight (another layer's weight per copy) and output
+        g = torch.Generator(device=dev)
+        g.manual_seed(7919 + seed)
+        c["w_o"] = (torch.randn((n_out, H * 128), generator=g, device=dev) / (H * 128) ** 0.5).to(torch.bfloat16)
+        c["y"] = torch.empty(S, n_out, dtype=torch.bfloat16, device=dev)
         return c
 
     def fused(c, stream=None):  # the same step in one launch
         m.mla_attn_combine_uv(c["qv"], c["kv"], c["kv_len"], q, spr, c["scale"], c["o"], c["lse"], c["w_v"],
                               c["gate"], c["out"], c["ws"], stream=stream)
+
+    def fused_op(c, stream=None):  # the same step and the o_proj shard, in one launch
+        m.mla_attn_combine_uv(c["qv"], c["kv"], c["kv_len"], q, spr, c["scale"], c["o"], c["lse"], c["w_v"],
+                              c["gate"], c["out"], c["ws"], stream=stream, w_o=c["w_o"], y=c["y"])
+
+    def oproj(c, stream=None):
+        m.mla_o_proj(c["out"], c["w_o"], c["y"], stream=stream)
 
     def attn(c, stream=None):
         m.mla_attn_split_kv(c["qv"], c["kv"], c["kv_len"], q, spr, c["scale"], c["o"], c["lse"], stream=stream)
@@ -1012,7 +1027,7 @@ def run_gpu_attn(args):
                 gate=inp["gate"], S=S, S_out=S, H=H, P=spr)
     comb_b = synth.algorithmic_bytes(cinp)
     rotate = args.rotate or max(1, -(-L2_DEFEAT_BYTES // (attn_b + comb_b)))
-    copies = [inp] + [with_bufs(synth.make_attn(wl, device=dev, seed=seed0 + 1000 * k)) for k in range(1, rotate)]
+    copies = [inp] + [with_bufs(synth.make_attn(wl, device=dev, seed=seed0 + 1000 * k), k) for k in range(1, rotate)]
     a = m.make_args(inp["o"], inp["lse"], q, spr, inp["w_v"], 0, inp["gate"], inp["out"], None,
                     kernel=args.kernel, tile_tokens=args.tile)
     plan = m.mla_combine_uv_plan(a)
@@ -1045,9 +1060,13 @@ def run_gpu_attn(args):
 
     for k in range(max(3, args.warmup)):
         fused(copies[k % rotate])
+        fused_op(copies[k % rotate])
+        oproj(copies[k % rotate])
     torch.cuda.synchronize()
     assert m.mla_combine_uv_status(stream) == m.MLA_OK
     g_step = graph_of(fused)
+    g_step_op = graph_of(fused_op)
+    g_step_then_op = graph_of(lambda c: (fused(c), oproj(c)))
     g_two = graph_of(lambda c: (attn(c), combine(c)))
     g_attn = graph_of(attn)
     g_comb = graph_of(combine)
@@ -1062,6 +1081,8 @@ def run_gpu_attn(args):
     two_ms = timed(g_two) / args.steps
     attn_ms = timed(g_attn) / args.steps
     comb_ms = timed(g_comb) / args.steps
+    step_op_ms = timed(g_step_op) / args.steps
+    step_then_op_ms = timed(g_step_then_op) / args.steps
     cold_us = cold_launch_us(lambda: fused(copies[0]), stream, dev)
     assert m.mla_combine_uv_status(stream) == m.MLA_OK
     total_ms = reduce_max(total_ms, dist, dev)
@@ -1130,6 +1151,11 @@ def run_gpu_attn(args):
                        "timing": "CUDA graphs of the timed steps (the fused step; for comparison the two-launch "
                                  "step, the attention alone, the combine alone), per-step time = replay / steps"},
             "two_launch_step_us": two_ms * 1e3,
+            "with_oproj": {"n_out": n_out, "one_launch_us": step_op_ms * 1e3,
+                           "step_then_oproj_us": step_then_op_ms * 1e3,
+                           "note": "the decode step followed by this rank's o_proj shard (W_o [n_out, H*128]): "
+                                   "in the same launch (mla_attn_combine_uv with w_o), and as the fused step "
+                                   "followed by mla_o_proj on the stream"},
             "achieved_gbs": achieved,
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,

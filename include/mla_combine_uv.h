@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define MLA_ABI_VERSION 5
+#define MLA_ABI_VERSION 6
 
 /* W_V storage format. */
 enum {
@@ -360,7 +360,12 @@ int32_t mla_o_proj(const mla_o_proj_args *args, void *stream);
  * (8-token tile, head) units; a CTA reaches one only after its own attention
  * items, and waits (bounded by wait_ns) until the tile's items have all
  * arrived -- items that running CTAs hold and that never wait on a combine
- * unit.  The workspace carries the queue and the arrival counters.
+ * unit.  With n_out > 0 the queue then holds o_proj units (64 outputs x 64
+ * tokens): a CTA reaches one only after its combine units; it copies its
+ * weight rows at once and waits (bounded by wait_ns) until every combine unit
+ * has stored its core rows -- units held by running CTAs that never wait on
+ * an o_proj unit.  The workspace carries the queue, the arrival counters and
+ * the count of stored combine units.
  */
 typedef struct {
   /* the attention, as in mla_attn_split_kv_args */
@@ -391,12 +396,26 @@ typedef struct {
                             leaves it zero (also after a timeout).  One call
                             at a time per workspace.                          */
   int64_t workspace_words;
-  int64_t wait_ns;       /* limit of the waits for a tile's partials, in ns;
-                            0 = the default 0.5 s                             */
+  int64_t wait_ns;       /* limit of the waits for a tile's partials (and of
+                            o_proj's wait for the core rows), in ns; 0 = the
+                            default 0.5 s                                     */
+  /* o_proj in the same launch (ABI version 6; n_out == 0: none).  The page's
+     stage ends at "o_proj's input"; with n_out > 0 the same grid then computes
+     this rank's o_proj shard on the core rows it just wrote, exactly as
+     mla_o_proj defines it: y[t][j] = bf16(sum_k out[t][k] w_o[j][k]) over
+     k < H*128 (fp32 accumulation, one rounding), t < S.  The tensor-parallel
+     all-reduce of the shards is the caller's.                                */
+  const void *w_o;       /* bf16 [n_out, H*128]: w_o[j][k] at j*w_o_sj + k;
+                            16-byte aligned                                   */
+  int64_t w_o_sj;        /* >= H*128, multiple of 8 elements                  */
+  int32_t n_out;         /* 0, or a multiple of 64                            */
+  void *y;               /* bf16 [S, y_st], caller-owned                      */
+  int64_t y_st;          /* >= n_out                                          */
 } mla_attn_combine_uv_args;
 
 /* Workspace words (int32) that mla_attn_combine_uv needs for B requests of q
- * tokens: 2 + ceil(B*q / 8).  Returns -1 for B < 0 or q < 1. */
+ * tokens: 3 + ceil(B*q / 8) (ABI version 6; version 5 needed 2 + ...).
+ * Returns -1 for B < 0 or q < 1. */
 int64_t mla_attn_combine_uv_workspace_words(int32_t B, int32_t q);
 
 /*
@@ -424,7 +443,7 @@ int32_t mla_attn_combine_uv(const mla_attn_combine_uv_args *args, void *stream);
  * in one fixed 16 MiB device array inside the library, which every device
  * that loads the library holds until the process exits; the call allocates
  * nothing and calls no allocating routine.  Limits: 16 KiB of counters
- * (B*q <= 32752 tokens) and spr * B*q * H * (1024 + 4) bytes of partials
+ * (B*q <= 32744 tokens) and spr * B*q * H * (1024 + 4) bytes of partials
  * (LSE rounded up to 256 bytes) within the remaining 16 MiB - 16 KiB; a
  * bigger problem returns MLA_ERR_SCRATCH before anything is launched (the
  * decode step of 64 requests x 12 heads x 16 splits needs 12.6 MB).

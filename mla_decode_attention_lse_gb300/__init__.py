@@ -125,6 +125,8 @@ class AttnCombineArgs(ctypes.Structure):
         ("gate", ctypes.c_void_p), ("out", ctypes.c_void_p), ("S_out", ctypes.c_int32),
         ("workspace", ctypes.c_void_p), ("workspace_words", ctypes.c_int64),
         ("wait_ns", ctypes.c_int64),
+        ("w_o", ctypes.c_void_p), ("w_o_sj", ctypes.c_int64), ("n_out", ctypes.c_int32),
+        ("y", ctypes.c_void_p), ("y_st", ctypes.c_int64),
     ]
 
 
@@ -369,7 +371,7 @@ def mla_attn_combine_uv_workspace_words(B: int, q: int) -> int:
 
 
 def make_attn_combine_args(qv, kv, kv_len, q, spr, scale, part_o, part_lse, w_v, gate, out, workspace,
-                           wait_ns=0) -> AttnCombineArgs:
+                           wait_ns=0, w_o=None, y=None) -> AttnCombineArgs:
     """Fill ``mla_attn_combine_uv_args`` from tensors (pointers and element strides)."""
     S, H, _ = qv.shape
     B, Lmax, _ = kv.shape
@@ -384,13 +386,31 @@ def make_attn_combine_args(qv, kv, kv_len, q, spr, scale, part_o, part_lse, w_v,
     a.gate, a.out, a.S_out = _ptr(gate), _ptr(out), out.shape[0]
     a.workspace, a.workspace_words = _ptr(workspace), workspace.numel()
     a.wait_ns = wait_ns
+    if w_o is not None:
+        a.w_o, a.w_o_sj, a.n_out = _ptr(w_o), w_o.stride(0), w_o.shape[0]
+        a.y, a.y_st = _ptr(y), y.stride(0)
     return a
 
 
+def _check_oproj(w_o, y, S, H):
+    import torch
+
+    if (w_o is None) != (y is None):
+        raise ValueError("w_o and y go together")
+    if w_o is None:
+        return
+    if w_o.dtype != torch.bfloat16 or w_o.dim() != 2 or w_o.shape[1] != H * 128 or w_o.stride(1) != 1:
+        raise ValueError("w_o must be bf16 [n_out, H*128] with a unit-stride last dimension")
+    if y.dtype != torch.bfloat16 or y.dim() != 2 or tuple(y.shape) != (S, w_o.shape[0]) or y.stride(1) != 1:
+        raise ValueError("y must be bf16 [S, n_out] with a unit-stride last dimension")
+
+
 def mla_attn_combine_uv(qv, kv, kv_len, q, spr, scale, part_o, part_lse, w_v, gate, out, workspace,
-                        stream=None, wait_ns=0) -> None:
+                        stream=None, wait_ns=0, w_o=None, y=None) -> None:
     """The decode step in one launch: split-KV attention, then the combine of
-    its partials (bf16 W_V), on CUDA tensors.
+    its partials (bf16 W_V), on CUDA tensors; with ``w_o`` (bf16 [n_out,
+    H*128], n_out a multiple of 64) and ``y`` (bf16 [S, n_out]) also the
+    o_proj shard y = out[:S] w_o^T, in the same launch.
 
     qv [S, H, 576] bf16 (S = B * q); kv [B, Lmax, 576] bf16; kv_len [B] int32;
     part_o [spr, S, H, 512] bf16 / part_lse [spr, S, H] f32 dense (scratch for
@@ -425,7 +445,9 @@ def mla_attn_combine_uv(qv, kv, kv_len, q, spr, scale, part_o, part_lse, w_v, ga
     if stream is None:
         stream = torch.cuda.current_stream(qv.device)
     s = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
-    a = make_attn_combine_args(qv, kv, kv_len, q, spr, scale, part_o, part_lse, w_v, gate, out, workspace, wait_ns)
+    _check_oproj(w_o, y, S, H)
+    a = make_attn_combine_args(qv, kv, kv_len, q, spr, scale, part_o, part_lse, w_v, gate, out, workspace, wait_ns,
+                               w_o, y)
     st = load_library().mla_attn_combine_uv(ctypes.byref(a), ctypes.c_void_p(s))
     if st != MLA_OK:
         raise MlaError(st, "mla_attn_combine_uv")

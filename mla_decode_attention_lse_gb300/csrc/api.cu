@@ -476,7 +476,7 @@ int32_t mla_attn_split_kv(const mla_attn_split_kv_args *a, void *stream) {
 
 int64_t mla_attn_combine_uv_workspace_words(int32_t B, int32_t q) {
   if (B < 0 || q < 1) return -1;
-  return 2 + mla::attn_combine_tiles((int)std::min<int64_t>((int64_t)B * q, INT32_MAX));
+  return 3 + mla::attn_combine_tiles((int)std::min<int64_t>((int64_t)B * q, INT32_MAX));
 }
 
 int32_t mla_attn_combine_uv(const mla_attn_combine_uv_args *a, void *stream) {
@@ -491,13 +491,22 @@ int32_t mla_attn_combine_uv(const mla_attn_combine_uv_args *a, void *stream) {
   const int G = mla::attn_heads_per_cta(a->q, a->H);
   const int groups = (a->H + G - 1) / G;
   const int ntiles = mla::attn_combine_tiles((int)S);
-  if ((int64_t)a->B * a->spr * groups + (int64_t)ntiles * a->H >= ((int64_t)1 << 31)) return MLA_ERR_SHAPE;
+  // o_proj in the same launch: n_out outputs (a multiple of 64) of K = H*128 inputs
+  const int64_t K = (int64_t)a->H * 128;
+  const int64_t op_units = a->n_out > 0 ? (int64_t)(a->n_out / 64) * ((S + 63) / 64) : 0;
+  if (a->n_out < 0 || a->n_out % 64 || (int64_t)a->n_out * K >= ((int64_t)1 << 40)) return MLA_ERR_SHAPE;
+  if ((int64_t)a->B * a->spr * groups + (int64_t)ntiles * a->H + op_units >= ((int64_t)1 << 31)) return MLA_ERR_SHAPE;
   if (a->S_out > 0 && !a->out) return MLA_ERR_NULL;
   if (a->S_out > 0 && !aligned(a->out, 16)) return MLA_ERR_ALIGN;
   if (a->B > 0) {
     if (!a->qv || !a->kv || !a->kv_len || !a->part_o || !a->part_lse || !a->w_v || !a->gate || !a->workspace)
       return MLA_ERR_NULL;
-    if (a->workspace_words < 2 + ntiles) return MLA_ERR_SHAPE;
+    if (a->workspace_words < 3 + ntiles) return MLA_ERR_SHAPE;
+    if (a->n_out > 0) {
+      if (!a->w_o || !a->y) return MLA_ERR_NULL;
+      if (!aligned(a->w_o, 16) || !aligned(a->y, 2)) return MLA_ERR_ALIGN;
+      if (a->w_o_sj < K || a->w_o_sj % 8 || a->y_st < a->n_out) return MLA_ERR_STRIDE;
+    }
     if (!aligned(a->qv, 16) || !aligned(a->kv, 16) || !aligned(a->part_o, 16) || !aligned(a->w_v, 16) ||
         !aligned(a->gate, 16))
       return MLA_ERR_ALIGN;
@@ -533,11 +542,19 @@ int32_t mla_attn_combine_uv(const mla_attn_combine_uv_args *a, void *stream) {
   aa.kv_sb = a->kv_sb;
   aa.kv_sl = a->kv_sl;
   aa.Lmax = a->Lmax;
-  CUtensorMap tm, wm;
+  CUtensorMap tm, wm, om, xm;
   st = make_kv_tmap(&aa, &tm);
   if (st != MLA_OK) return st;
   st = make_wv_tmap(a->w_v, a->H, a->w_sh, a->w_sv, &wm);
   if (st != MLA_OK) return st;
+  std::memset(&om, 0, sizeof om);
+  std::memset(&xm, 0, sizeof xm);
+  if (a->n_out > 0) {
+    st = make_rows_tmap(a->w_o, a->n_out, K, a->w_o_sj, 64, &om);  // W_o [n_out, K]
+    if (st != MLA_OK) return st;
+    st = make_rows_tmap(a->out, S, K, K, 64, &xm);  // core rows 0 .. S - 1 (later rows read as zero)
+    if (st != MLA_OK) return st;
+  }
   mla::AttnParams p;
   std::memset(&p, 0, sizeof p);
   p.B = a->B;
@@ -561,7 +578,11 @@ int32_t mla_attn_combine_uv(const mla_attn_combine_uv_args *a, void *stream) {
   p.gate = static_cast<const uint16_t *>(a->gate);
   p.out = static_cast<uint16_t *>(a->out);
   p.wait_ns = a->wait_ns > 0 ? (unsigned long long)a->wait_ns : mla::kDefaultWaitNs;
-  const cudaError_t e = mla::launch_attn_combine(p, tm, wm, sms, static_cast<cudaStream_t>(stream));
+  p.n_out = a->n_out;
+  p.op_units = (int)op_units;
+  p.y = static_cast<uint16_t *>(a->y);
+  p.y_st = a->y_st;
+  const cudaError_t e = mla::launch_attn_combine(p, tm, wm, om, xm, sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

@@ -71,6 +71,8 @@ constexpr uint32_t kRopeBytes = kAttnTile * 128u;      // 16 KiB
 constexpr int kItemRing = 4;        // FUSED: items handed from the TMA lane to the other roles
 constexpr int kItemTakers = 2 + kAttnSmx;  // MMA lane, query warp, softmax warps
 constexpr int kCmbTile = 8;         // FUSED: tokens per combine unit (one merging warp each)
+constexpr int kOpStages = 10;       // FUSED o_proj: stages of a weight box and a core box (16 KiB each)
+constexpr uint32_t kOpBox = 64u * 128u;  // 64 rows x 64 bf16, 128-byte swizzle
 
 template <int N, bool FUSED = false>
 struct AttnLayout {
@@ -85,8 +87,9 @@ struct AttnLayout {
   static constexpr uint32_t bar_off = row_off + N * 8u;
   // barriers: full/empty per double slot, full/empty per rope slot, then
   // s_full, s_free, p_full, o_full, q_full, q_free
-  // FUSED adds: item full / empty per ring slot, W_V full, combine MMA done
-  static constexpr int kBars = 2 * kAttnDbl + 2 * kRope + 6 + (FUSED ? 2 * kItemRing + 2 : 0);
+  // FUSED adds: item full / empty per ring slot, W_V full, combine MMA done,
+  // then the o_proj stages' full / empty and its accumulator's full
+  static constexpr int kBars = 2 * kAttnDbl + 2 * kRope + 6 + (FUSED ? 2 * kItemRing + 2 + 2 * kOpStages + 1 : 0);
   // misc: [0] TMEM base, [1] abort flag, [2 .. 2 + kItemRing) item ring,
   // [6] the combine unit drawn last
   static constexpr uint32_t misc_off = bar_off + kBars * 8u;
@@ -98,6 +101,8 @@ static_assert(AttnLayout<32, true>::total + 1024 <= 227u * 1024u, "shared memory
 // FUSED: W_V[h] (128 KiB) reuses the first four double-block slots, the
 // latent tile [16 x 512] bf16 (16 KiB) the first rope slot
 static_assert(4 * kDblBytes == 128u * 1024u && kRopeBytes >= 16u * 1024u, "combine tiles");
+// FUSED o_proj: its stage ring reuses the latent double-block slots
+static_assert(kOpStages * 2u * kOpBox <= kAttnDbl * kDblBytes, "o_proj stages");
 
 // Bounded wait on an mbarrier phase, shared abort flag (as the combine kernels).
 __device__ __forceinline__ bool attn_wait(uint32_t bar, uint32_t parity, int *err, volatile int *abort_flag) {
@@ -301,7 +306,13 @@ __device__ __forceinline__ void combine_phase(const AttnParams &p, const CUtenso
     }
     ++units;
     __syncthreads();
-    if (threadIdx.x == 0) misc[6] = (uint32_t)atomicAdd(p.ws, 1);
+    if (threadIdx.x == 0) {
+      if (p.n_out > 0) {  // this unit's core rows are stored (read by the o_proj units)
+        __threadfence();
+        atomicAdd(p.ws + 2 + p.ntiles, 1);
+      }
+      misc[6] = (uint32_t)atomicAdd(p.ws, 1);
+    }
     __syncthreads();
     unit = misc[6];
   }
@@ -317,13 +328,148 @@ __device__ __forceinline__ void combine_phase(const AttnParams &p, const CUtenso
     uint4 *dst = reinterpret_cast<uint4 *>(p.out + (long long)S * Wrow);
     for (long long k = zb + threadIdx.x; k < ze; k += blockDim.x) dst[k] = make_uint4(0u, 0u, 0u, 0u);
   }
+}
+
+// The o_proj units of the fused launch (n_out > 0), run by every thread of
+// the CTA after its combine units: unit u covers outputs 64 (u % MT) .. + 63
+// and tokens 64 (u / MT) .. + 63 of y[t][j] = sum_k core[t][k] W_o[j][k]
+// (the page's stage ends at "o_proj's input"; this is the shard of o_proj
+// that follows it).  Per 64-wide K block a stage holds the weight box and the
+// core box (TMA, 128-byte swizzle); one thread issues four kind::f16 MMAs of
+// M = 64, N = 64, K = 16 into TMEM columns 0..63 (D row i in lane 32 (i / 16)
+// + i % 16), and warps 2..5 store the bf16 rounding of the accumulator.  The
+// weight boxes of a CTA's first stages go out at once (a weight no kernel
+// writes); its first core copy waits (bounded) until every combine unit has
+// stored -- units drawn before any o_proj unit by CTAs that are running and
+// never wait on an o_proj unit -- then orders those stores before its TMA
+// reads with a proxy fence.
+template <int N>
+__device__ __forceinline__ void oproj_phase(const AttnParams &p, const CUtensorMap &wo_map, const CUtensorMap &x_map,
+                                            uint32_t sbase, uint32_t tmem, uint32_t *misc, volatile int *s_abort,
+                                            uint32_t obar) {
+  using L = AttnLayout<N, true>;
+  constexpr unsigned kFull = 0xffffffffu;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = p.B * p.q, K = p.H * kV, KB = K / 64, MT = p.n_out / 64;
+  const int base = p.B * p.spr * p.groups + p.ntiles * p.H;  // queue index of o_proj unit 0
+  auto full = [&](int s) { return obar + 8u * (uint32_t)s; };
+  auto empty = [&](int s) { return obar + 8u * (uint32_t)(kOpStages + s); };
+  const uint32_t acc_full = obar + 8u * (uint32_t)(2 * kOpStages);
+  auto sA = [&](int s) { return sbase + L::dbl_off + (uint32_t)s * 2u * kOpBox; };
+  auto sB = [&](int s) { return sbase + L::dbl_off + (uint32_t)s * 2u * kOpBox + kOpBox; };
+
+  tc_fence_before();
+  __syncthreads();  // the combine units of this CTA are done (their copies landed, MMAs complete)
+  tc_fence_after();
+  int g = 0;           // stages issued (thread 0) / consumed (MMA lane) over this CTA's units
+  int issued = 0;      // thread 0: stages whose copies went out
+  int nu = 0;          // units done
+  bool ready = false;  // thread 0: every combine unit has stored
+  int last_mma = -1;   // MMA lane: the last unit whose MMAs it committed
+  uint32_t unit = misc[6];
+  while (!*s_abort && unit != 0xFFFFFFFFu && (int)unit >= base && (int)unit - base < p.op_units) {
+    const int u = (int)unit - base, mt = u % MT, nt = u / MT;
+    if (threadIdx.x == 0) {
+      bool ok = true;
+      int pre = 0;
+      if (!ready) {  // the CTA's first unit (g == 0): weight boxes first, then the wait
+        pre = KB < kOpStages ? KB : kOpStages;
+        for (int kb = 0; kb < pre; ++kb) {
+          mbar_arrive_expect_tx(full(kb), 2u * kOpBox);
+          tma_load_3d(sA(kb), &wo_map, 64 * kb, mt * 64, 0, full(kb));
+        }
+        if (!wait_count(p.ws + 2 + p.ntiles, p.ntiles * p.H, p.wait_ns)) {
+          atomicCAS(p.err, 0, kErrWaitTile);
+          *s_abort = 1;
+          ok = false;
+        }
+        fence_proxy_async_global();
+        ready = true;
+        // their core boxes (after a failed wait too, so that every stage
+        // whose weight went out completes and the teardown can wait for it)
+        for (int kb = 0; kb < pre; ++kb) tma_load_3d(sB(kb), &x_map, 64 * kb, nt * 64, 0, full(kb));
+        g = pre;
+        issued = pre;
+      }
+      for (int kb = pre; kb < KB && ok; ++kb, ++g) {
+        const int s = g % kOpStages;
+        if (g >= kOpStages) ok = attn_wait(empty(s), (uint32_t)(g / kOpStages - 1) & 1u, p.err, s_abort);
+        if (!ok) break;
+        mbar_arrive_expect_tx(full(s), 2u * kOpBox);
+        tma_load_3d(sA(s), &wo_map, 64 * kb, mt * 64, 0, full(s));
+        tma_load_3d(sB(s), &x_map, 64 * kb, nt * 64, 0, full(s));
+        issued = g + 1;
+      }
+    } else if (warp == 1 && lane == 0) {
+      constexpr uint32_t kId = idesc_bf16(64, 64);
+      bool ok = true;
+      for (int kb = 0; kb < KB && ok; ++kb, ++g) {
+        const int s = g % kOpStages;
+        ok = attn_wait(full(s), (uint32_t)(g / kOpStages) & 1u, p.err, s_abort);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t dA = (uint32_t)smem_desc_sw128(sA(s)), dB = (uint32_t)smem_desc_sw128(sB(s));
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4)
+          tc_mma_f16(tmem, desc_sw128_at(dA, (uint32_t)k4 * 32u), desc_sw128_at(dB, (uint32_t)k4 * 32u), kId,
+                     (kb | k4) ? 1u : 0u);
+        tc_commit(empty(s));
+      }
+      if (ok) {
+        tc_commit(acc_full);
+        last_mma = nu;
+      }
+    } else if (warp >= 2 && warp < 6) {
+      // quadrant warp % 4: rows 16 qd .. 16 qd + 15 of the M = 64 accumulator in lanes 0..15
+      const int qd = warp & 3;
+      bool ok = attn_wait(acc_full, (uint32_t)nu & 1u, p.err, s_abort);
+      ok = __all_sync(kFull, ok);
+      if (ok) {
+        tc_fence_after();
+        const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);
+        const int j = mt * 64 + qd * 16 + (lane & 15);
+#pragma unroll 1
+        for (int c = 0; c < 64; c += 16) {
+          uint32_t r[16];
+          tmem_ld_x16(trow + (uint32_t)c, r);
+          tc_wait_ld();
+          if (lane < 16) {
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+              const int t = nt * 64 + c + x;
+              if (t < S) {
+                const __nv_bfloat16 hv = __float2bfloat16_rn(__uint_as_float(r[x]));
+                p.y[(long long)t * p.y_st + j] = *reinterpret_cast<const uint16_t *>(&hv);
+              }
+            }
+          }
+        }
+      }
+    }
+    ++nu;
+    tc_fence_before();
+    __syncthreads();  // the accumulator is drained before the next unit's MMAs overwrite it
+    tc_fence_after();
+    if (threadIdx.x == 0) misc[6] = (uint32_t)atomicAdd(p.ws, 1);
+    __syncthreads();
+    unit = misc[6];
+  }
+  // after an abort: this CTA's copies land and its committed MMAs complete
+  if (threadIdx.x == 0)
+    for (int q = issued - kOpStages < 0 ? 0 : issued - kOpStages; q < issued; ++q)
+      mbar_wait(full(q % kOpStages), (uint32_t)(q / kOpStages) & 1u, p.err, kErrWaitTeardown);
+  if (warp == 1 && lane == 0 && last_mma >= 0) mbar_wait(acc_full, (uint32_t)last_mma & 1u, p.err, kErrWaitTeardown);
+}
+
+// The last CTA of the fused launch to finish leaves the workspace zeroed for
+// the next call.
+__device__ __forceinline__ void finish_workspace(const AttnParams &p) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    // the last CTA to finish leaves the workspace zeroed for the next call
     __threadfence();
     if (atomicAdd(p.ws + 1, 1) == (int)gridDim.x - 1) {
       __threadfence();
-      for (int k = 0; k < p.ntiles; ++k) p.ws[2 + k] = 0;
+      for (int k = 0; k <= p.ntiles; ++k) p.ws[2 + k] = 0;
       p.ws[0] = 0;
       p.ws[1] = 0;
       __threadfence();
@@ -336,7 +482,8 @@ __device__ __forceinline__ void combine_phase(const AttnParams &p, const CUtenso
 template <int N, bool FUSED>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap kv_map,
-                const __grid_constant__ CUtensorMap wv_map) {
+                const __grid_constant__ CUtensorMap wv_map, const __grid_constant__ CUtensorMap wo_map,
+                const __grid_constant__ CUtensorMap x_map) {
   using L = AttnLayout<N, FUSED>;
   constexpr int NR = L::kRope;
   extern __shared__ uint8_t smem_raw[];
@@ -365,6 +512,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   auto item_empty = [&](int s) { return s_full + 48u + 8u * (uint32_t)(kItemRing + s); };
   const uint32_t wv_full = s_full + 48u + 8u * (uint32_t)(2 * kItemRing);
   const uint32_t cmb_mma = wv_full + 8u;
+  const uint32_t op_bar = cmb_mma + 8u;  // FUSED o_proj: full / empty per stage, accumulator full
   volatile uint32_t *ring = misc + 2;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -390,6 +538,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       mbar_init(wv_full, 1u);
       mbar_init(cmb_mma, 1u);
+      for (int s = 0; s < 2 * kOpStages + 1; ++s) mbar_init(op_bar + 8u * (uint32_t)s, 1u);
     }
     misc[1] = 0u;
     misc[6] = 0xFFFFFFFFu;
@@ -859,7 +1008,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // the next kernel on the stream may start its prologue
     grid_launch_dependents();
   }
-  if constexpr (FUSED) combine_phase<N>(p, wv_map, sbase, gbase, tmem, misc, s_abort, wv_full, cmb_mma, nitems);
+  if constexpr (FUSED) {
+    combine_phase<N>(p, wv_map, sbase, gbase, tmem, misc, s_abort, wv_full, cmb_mma, nitems);
+    if (p.n_out > 0) oproj_phase<N>(p, wo_map, x_map, sbase, tmem, misc, s_abort, op_bar);
+    finish_workspace(p);
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -877,7 +1030,8 @@ int attn_combine_tiles(int S) { return (S + kCmbTile - 1) / kCmbTile; }
 
 template <int N, bool FUSED>
 static cudaError_t launch_attn_n(const AttnParams &p, const CUtensorMap &map, const CUtensorMap &wv_map,
-                                 unsigned grid, cudaStream_t stream) {
+                                 const CUtensorMap &wo_map, const CUtensorMap &x_map, unsigned grid,
+                                 cudaStream_t stream) {
   const size_t smem = 1024 + AttnLayout<N, FUSED>::total;
   cudaError_t e = cudaFuncSetAttribute(attn_kernel<N, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -891,7 +1045,7 @@ static cudaError_t launch_attn_n(const AttnParams &p, const CUtensorMap &map, co
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, attn_kernel<N, FUSED>, p, map, wv_map);
+  e = cudaLaunchKernelEx(&cfg, attn_kernel<N, FUSED>, p, map, wv_map, wo_map, x_map);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -906,21 +1060,24 @@ cudaError_t launch_attn(const AttnParams &p, const CUtensorMap &map, int num_sms
   if (rows > 32) return cudaErrorInvalidValue;
   CUtensorMap none;
   std::memset(&none, 0, sizeof none);
-  return rows <= 16 ? launch_attn_n<16, false>(p, map, none, grid, stream)
-                    : launch_attn_n<32, false>(p, map, none, grid, stream);
+  return rows <= 16 ? launch_attn_n<16, false>(p, map, none, none, none, grid, stream)
+                    : launch_attn_n<32, false>(p, map, none, none, none, grid, stream);
 }
 
-// The fused attention + combine: one CTA per SM over the attention items and
-// then the combine units (ntiles * H), all drawn from the workspace queue.
-cudaError_t launch_attn_combine(const AttnParams &p, const CUtensorMap &map, const CUtensorMap &wv_map, int num_sms,
-                                cudaStream_t stream) {
-  const long long work = (long long)p.B * p.spr * p.groups + (long long)p.ntiles * p.H;
+// The fused attention + combine (+ o_proj): one CTA per SM over the attention
+// items, then the combine units (ntiles * H), then the o_proj units, all
+// drawn from the workspace queue.
+cudaError_t launch_attn_combine(const AttnParams &p, const CUtensorMap &map, const CUtensorMap &wv_map,
+                                const CUtensorMap &wo_map, const CUtensorMap &x_map, int num_sms, cudaStream_t stream) {
+  const long long work =
+      (long long)p.B * p.spr * p.groups + (long long)p.ntiles * p.H + (p.n_out > 0 ? (long long)p.op_units : 0);
   if (work <= 0 || work >= (1LL << 31) || num_sms < 1 || !p.ws) return cudaErrorInvalidValue;
+  if (p.n_out > 0 && (p.n_out % 64 || (p.H * kV) % 64 || !p.y)) return cudaErrorInvalidValue;
   const unsigned grid = (unsigned)(work < num_sms ? work : num_sms);
   const int rows = ((p.q * p.G + 15) / 16) * 16;
   if (rows > 32 || p.spr > 32) return cudaErrorInvalidValue;
-  return rows <= 16 ? launch_attn_n<16, true>(p, map, wv_map, grid, stream)
-                    : launch_attn_n<32, true>(p, map, wv_map, grid, stream);
+  return rows <= 16 ? launch_attn_n<16, true>(p, map, wv_map, wo_map, x_map, grid, stream)
+                    : launch_attn_n<32, true>(p, map, wv_map, wo_map, x_map, grid, stream);
 }
 
 }  // namespace mla

@@ -53,9 +53,12 @@ cudaError_t launch_attn(const AttnParams &p, const CUtensorMap &map, int num_sms
 cudaError_t launch_attn_pair(const AttnParams &p, const CUtensorMap &map, int num_sms, cudaStream_t stream);
 // The same attention with the combine of its partials behind it in the same
 // launch (bf16 W_V through `wv_map`: [H, 128, 512], boxes of 64 x 128 x 1,
-// 128-byte swizzle); p.ws holds 2 + attn_combine_tiles(S) zeroed words.
+// 128-byte swizzle) and, when p.n_out > 0, the o_proj shard on its core rows
+// (`wo_map`: W_o [n_out, H*128], `x_map`: core [S, H*128], both boxes of 64
+// columns x 64 rows, 128-byte swizzle); p.ws holds 3 + attn_combine_tiles(S)
+// zeroed words.
 int attn_combine_tiles(int S);
-cudaError_t launch_attn_combine(const AttnParams &p, const CUtensorMap &map, const CUtensorMap &wv_map, int num_sms,
-                                cudaStream_t stream);
+cudaError_t launch_attn_combine(const AttnParams &p, const CUtensorMap &map, const CUtensorMap &wv_map,
+                                const CUtensorMap &wo_map, const CUtensorMap &x_map, int num_sms, cudaStream_t stream);
 
 }  // namespace mla

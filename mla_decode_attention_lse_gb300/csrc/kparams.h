@@ -57,12 +57,19 @@ struct AttnParams {
   float *lse;        // f32 [spr, S, H] dense
   int *err;          // device error word
   // The combine fused behind the attention (mla_attn_combine_uv) only:
-  int *ws;           // workspace: [0] work queue, [1] CTAs done, [2 + k] arrivals of token tile k
+  int *ws;           // workspace: [0] work queue, [1] CTAs done, [2 + k] arrivals of token tile k,
+                     // [2 + ntiles] combine units stored
   int ntiles;        // 8-token tiles of the batch, ceil(S / 8)
   int S_out;         // rows of out (rows S .. S_out - 1 are zeroed)
   const uint16_t *gate;  // bf16 [S, H*128] dense
   uint16_t *out;     // bf16 [S_out, H*128] dense
   unsigned long long wait_ns;  // limit of the waits for a tile's partials
+  // o_proj in the same launch (n_out > 0): y[t][j] = sum_k out[t][k] w_o[j][k]
+  // over k < H*128, units of 64 outputs x 64 tokens behind the combine units
+  int n_out;         // outputs, a multiple of 64 (0: no o_proj)
+  int op_units;      // (n_out / 64) * ceil(S / 64)
+  uint16_t *y;       // bf16 [S, y_st]
+  long long y_st;
 };
 
 // The DCP producer side (pack into one destination rank's combine buffer).

@@ -30,7 +30,7 @@ namespace {
 
 // 16 MiB: the counter region first, then the partials' LSE and latents.
 constexpr int64_t kScratchBytes = 16ll << 20;
-constexpr int64_t kCounterWords = 4096;  // 16 KiB: 2 + ceil(B q / 8) words at most
+constexpr int64_t kCounterWords = 4096;  // 16 KiB: 3 + ceil(B q / 8) words at most
 constexpr int64_t kCounterBytes = kCounterWords * 4;
 
 static __device__ __align__(256) unsigned char g_step_scratch[kScratchBytes];
@@ -68,7 +68,7 @@ extern "C" int32_t mla_attn_combine_uv_noalloc(const mla_attn_combine_uv_args *a
   // what this call's scratch needs, against what the array holds (the token
   // count is bounded first, so nothing below overflows)
   const int64_t S = (int64_t)a.B * a.q;
-  if (2 + (S + 7) / 8 > kCounterWords) return MLA_ERR_SCRATCH;
+  if (3 + (S + 7) / 8 > kCounterWords) return MLA_ERR_SCRATCH;
   const int64_t rows = (int64_t)a.spr * S * a.H;
   const int64_t lse_bytes = round_up(rows * 4, 256);
   const int64_t o_bytes = rows * 512 * 2;

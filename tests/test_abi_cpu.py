@@ -43,7 +43,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert m.mla_abi_version() == 5
+    assert m.mla_abi_version() == 6
     for s in range(0, 12):
         assert m.mla_status_str(s) and m.mla_status_str(s) != "unknown status"
     assert m.mla_status_str(99) == "unknown status"
@@ -197,7 +197,7 @@ def fused_args(B=4, q=1, H=12, spr=16, Lmax=256, **kw):
     a.w_v, a.w_sh, a.w_sv = ALIGNED * 6, 128 * 512, 512
     a.w_fmt = 0
     a.gate, a.out, a.S_out = ALIGNED * 7, ALIGNED * 8, B * q
-    a.workspace, a.workspace_words = ALIGNED * 9, 2 + (B * q + 7) // 8
+    a.workspace, a.workspace_words = ALIGNED * 9, 3 + (B * q + 7) // 8
     for k, v in kw.items():
         setattr(a, k, v)
     return a
@@ -216,6 +216,18 @@ def test_attn_combine_validation_errors(lib):
     assert st(fused_args(S_out=3)) == m.MLA_ERR_SHAPE          # S_out < S
     assert st(fused_args(wait_ns=-1)) == m.MLA_ERR_SHAPE
     assert st(fused_args(workspace_words=2)) == m.MLA_ERR_SHAPE
+    assert st(fused_args(workspace_words=2 + 1)) == m.MLA_ERR_SHAPE  # 3 + ceil(4 / 8) = 4 words needed
+    # o_proj in the same launch
+    op = dict(w_o=ALIGNED * 10, w_o_sj=12 * 128, n_out=128, y=ALIGNED * 11, y_st=128)
+    assert st(fused_args(**{**op, "n_out": 96})) == m.MLA_ERR_SHAPE   # not a multiple of 64
+    assert st(fused_args(**{**op, "n_out": -64})) == m.MLA_ERR_SHAPE
+    assert st(fused_args(**{**op, "w_o": None})) == m.MLA_ERR_NULL
+    assert st(fused_args(**{**op, "y": None})) == m.MLA_ERR_NULL
+    assert st(fused_args(**{**op, "w_o": ALIGNED + 8})) == m.MLA_ERR_ALIGN
+    assert st(fused_args(**{**op, "y": ALIGNED + 1})) == m.MLA_ERR_ALIGN
+    assert st(fused_args(**{**op, "w_o_sj": 12 * 128 - 8})) == m.MLA_ERR_STRIDE  # shorter than H*128
+    assert st(fused_args(**{**op, "w_o_sj": 12 * 128 + 4})) == m.MLA_ERR_STRIDE  # not a multiple of 8
+    assert st(fused_args(**{**op, "y_st": 64})) == m.MLA_ERR_STRIDE
     assert st(fused_args(workspace=None)) == m.MLA_ERR_NULL
     assert st(fused_args(part_o=None)) == m.MLA_ERR_NULL
     assert st(fused_args(out=ALIGNED + 8)) == m.MLA_ERR_ALIGN
@@ -223,7 +235,7 @@ def test_attn_combine_validation_errors(lib):
     assert st(fused_args(w_sv=500)) == m.MLA_ERR_STRIDE
     assert st(fused_args(kv_sl=568)) == m.MLA_ERR_STRIDE
     for B, q in ((0, 1), (1, 1), (8, 1), (9, 1), (64, 1), (3, 3), (1024, 4)):
-        assert lib.mla_attn_combine_uv_workspace_words(B, q) == 2 + (B * q + 7) // 8
+        assert lib.mla_attn_combine_uv_workspace_words(B, q) == 3 + (B * q + 7) // 8
     assert lib.mla_attn_combine_uv_workspace_words(-1, 1) == -1
 
 

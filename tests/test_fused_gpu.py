@@ -178,3 +178,112 @@ def test_fused_empty_batch_and_errors(lib):
     with pytest.raises(m.MlaError) as e:
         run_fused(inp, small)
     assert e.value.status == m.MLA_ERR_SHAPE
+
+
+def run_fused_oproj(inp, n_out, seed=5, ws=None):
+    """The decode step with the o_proj shard in the same launch; returns (y,
+    core, canary columns of y)."""
+    import mla_decode_attention_lse_gb300 as m
+
+    B, q, H, spr, S, S_out = (inp[k] for k in ("B", "q", "H", "spr", "S", "S_out"))
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    w_o = (torch.randn((n_out, H * 128), generator=g, device="cuda") / math.sqrt(H * 128)).to(torch.bfloat16)
+    part_o = torch.empty((spr, S, H, D), dtype=torch.bfloat16, device="cuda")
+    part_lse = torch.empty((spr, S, H), dtype=torch.float32, device="cuda")
+    out = torch.empty((S_out, H * 128), dtype=torch.bfloat16, device="cuda")
+    ybuf = torch.full((S, n_out + 8), CANARY, dtype=torch.int16, device="cuda")
+    y = ybuf[:, :n_out].view(torch.bfloat16)
+    if ws is None:
+        ws = torch.zeros(m.mla_attn_combine_uv_workspace_words(B, q), dtype=torch.int32, device="cuda")
+    m.mla_attn_combine_uv(inp["qv"], inp["kv"], inp["kv_len"], q, spr, inp["scale"], part_o, part_lse, inp["w_v"],
+                          inp["gate"], out, ws, w_o=w_o, y=y)
+    torch.cuda.synchronize()
+    assert m.mla_combine_uv_status() == m.MLA_OK
+    assert int(ws.abs().sum()) == 0, "workspace not left zero"
+    full = ybuf.cpu().numpy().view(np.uint16)
+    return full[:, :n_out], full[:, n_out:], out, w_o
+
+
+OPROJ_CASES = [
+    (3, 1, 12, 4, 300, [300, 129, 5], 128),           # S = 3, K = 1536
+    (4, 2, 3, 3, 260, [128, 256, 1, 0], 64),          # q = 2, a token that sees nothing, K = 384
+    (40, 2, 2, 3, 200, [200 - 4 * i for i in range(40)], 192),  # S = 80: two 64-token tiles
+]
+
+
+@pytest.mark.parametrize("B,q,H,spr,Lmax,lens,n_out", OPROJ_CASES)
+def test_fused_with_oproj(lib, orc, B, q, H, spr, Lmax, lens, n_out):
+    """o_proj in the same launch: y bit for bit as mla_o_proj on the launch's
+    own core rows, and against the oracle chain (attention -> combine ->
+    o_proj) at the stage's tolerance; the core rows as without o_proj."""
+    import mla_decode_attention_lse_gb300 as m
+
+    inp = problem(B, q, H, spr, Lmax, lens, seed=B * 3 + n_out)
+    y, canary, core, w_o = run_fused_oproj(inp, n_out)
+    assert np.all(canary == CANARY), "wrote past n_out"
+    S = inp["S"]
+    # core as the launch without o_proj gives it
+    got, _, _, _ = run_fused(inp, extra_rows=0)
+    assert np.array_equal(to_np16(core), got), "core differs from the launch without o_proj"
+    # y as mla_o_proj on the same core rows
+    y2 = torch.empty((S, n_out), dtype=torch.bfloat16, device="cuda")
+    m.mla_o_proj(core[:S].contiguous(), w_o, y2)
+    torch.cuda.synchronize()
+    assert np.array_equal(y, to_np16(y2)), "y differs from mla_o_proj on the same core"
+    # against the oracle chain
+    ref_core, _ = oracle_chain(orc, inp)
+    ref = orc.o_proj(ref_core, to_np16(w_o))
+    g32 = (y.astype(np.uint32) << 16).view(np.float32)
+    r32 = (ref.astype(np.uint32) << 16).view(np.float32) if ref.dtype == np.uint16 else ref
+    assert np.all(np.isfinite(g32))
+    d = np.abs(g32 - r32)
+    bad = d > 1e-2 + 1e-2 * np.abs(r32)
+    assert not bad.any(), f"o_proj in the launch: {bad.sum()} out of tolerance, max {d.max()}"
+
+
+def test_fused_with_oproj_decode_step(lib, orc):
+    """The bench's decode step (64 requests x 12 heads, 16 splits) with the
+    7168-output o_proj shard in the same launch: bit for bit as the launch
+    without it followed by mla_o_proj; two calls in a row agree."""
+    import mla_decode_attention_lse_gb300 as m
+    from mla_decode_attention_lse_gb300 import synth
+
+    a = synth.make_attn("attn_splitkv", device="cuda")
+    inp = dict(qv=a["qv"], kv=a["kv"], kv_len=a["kv_len"], q=a["q"], spr=a["spr"], scale=a["scale"], B=a["B"],
+               H=a["H"], Lmax=a["kv"].shape[1], w_v=a["w_v"], gate=a["gate"], S=a["B"] * a["q"],
+               S_out=a["B"] * a["q"])
+    ws = torch.zeros(m.mla_attn_combine_uv_workspace_words(inp["B"], inp["q"]), dtype=torch.int32, device="cuda")
+    y, canary, core, w_o = run_fused_oproj(inp, 7168, ws=ws)
+    y_again, _, _, _ = run_fused_oproj(inp, 7168, ws=ws)
+    assert np.array_equal(y, y_again), "two calls differ"
+    assert np.all(canary == CANARY)
+    got, _, _, _ = run_fused(inp, ws)
+    assert np.array_equal(to_np16(core), got)
+    y2 = torch.empty((inp["S"], 7168), dtype=torch.bfloat16, device="cuda")
+    m.mla_o_proj(core.contiguous(), w_o, y2)
+    torch.cuda.synchronize()
+    assert np.array_equal(y, to_np16(y2))
+
+
+def test_fused_oproj_argument_errors(lib):
+    import mla_decode_attention_lse_gb300 as m
+
+    inp = problem(2, 1, 2, 2, 64, [64, 10], seed=3)
+    S, H = inp["S"], inp["H"]
+    part_o = torch.empty((2, S, H, D), dtype=torch.bfloat16, device="cuda")
+    part_lse = torch.empty((2, S, H), dtype=torch.float32, device="cuda")
+    out = torch.empty((S, H * 128), dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(m.mla_attn_combine_uv_workspace_words(2, 1), dtype=torch.int32, device="cuda")
+    w_o = torch.zeros((96, H * 128), dtype=torch.bfloat16, device="cuda")  # 96 outputs: not a multiple of 64
+    y = torch.zeros((S, 96), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(m.MlaError) as e:
+        m.mla_attn_combine_uv(inp["qv"], inp["kv"], inp["kv_len"], 1, 2, inp["scale"], part_o, part_lse, inp["w_v"],
+                              inp["gate"], out, ws, w_o=w_o, y=y)
+    assert e.value.status == m.MLA_ERR_SHAPE
+    # a workspace of the previous size (2 + tiles words) is refused
+    small = torch.zeros(m.mla_attn_combine_uv_workspace_words(2, 1) - 1, dtype=torch.int32, device="cuda")
+    with pytest.raises(m.MlaError) as e:
+        m.mla_attn_combine_uv(inp["qv"], inp["kv"], inp["kv_len"], 1, 2, inp["scale"], part_o, part_lse, inp["w_v"],
+                              inp["gate"], out, small)
+    assert e.value.status == m.MLA_ERR_SHAPE
