@@ -537,7 +537,7 @@ __global__ void __launch_bounds__(kPrThreads, 1)
       for (int x = 0; x < NC; ++x) {
         const int m = c0 + x;
         const float l = (rd[m] + rd[N + m]) + (rd[2 * N + m] + rd[3 * N + m]);
-        inv[x] = l > 0.0f ? __frcp_rn(l) : 0.0f;
+        inv[x] = l > 0.0f ? rcp_approx(l) : 0.0f;
         if (rank == 0 && qd == 0 && lane == x && orow_s[m] >= 0)
           p.lse[orow_s[m]] = l > 0.0f ? (m_ref[x] + lg2_approx(l)) * kLn2 : kNegInf;
       }
