@@ -869,34 +869,54 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(s_free);
         }
-        // scores in log2 units, masked; the tile's column max over 128 positions
+        // scores in log2 units, masked
         const int jr = t * kAttnTile + pos;
         float sc[NC];
-        float *rd = red + (T & 1) * 4 * N;
+        bool up = false;  // a score of this thread exceeds its column's reference by more than the slack
 #pragma unroll
         for (int x = 0; x < NC; ++x) {
           sc[x] = (jr < lim[x]) ? __uint_as_float(sr[x]) * p.scale_log2 : kNegInf;
-          float mx = sc[x];
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-          if (lane == x) rd[qd * N + c0 + x] = mx;
+          up |= sc[x] > m_ref[x] + kSlack;
         }
-        ok = named_barrier_and(1, kSmxThreads, got);
-        if (!ok) break;
+        // After an item's first tile a column's reference rarely moves: one
+        // barrier vote (every wait succeeded, no score above its reference +
+        // slack) lets the warps take P = exp2(s - reference) at once -- the same
+        // values the exchange below gives when no column moves
+        const bool fast = t > 0 && named_barrier_and(1, kSmxThreads, got && !up);
         float alpha[NC];
         bool moved = false;
+        if (fast) {
 #pragma unroll
-        for (int x = 0; x < NC; ++x) {
-          const int m = c0 + x;
-          const float tmax = fmaxf(fmaxf(rd[m], rd[N + m]), fmaxf(rd[2 * N + m], rd[3 * N + m]));
-          const float mn = (tmax > m_ref[x] + kSlack) ? tmax : m_ref[x];
-          alpha[x] = (mn == m_ref[x]) ? 1.0f : ex2_approx(m_ref[x] - mn);  // 0 when m_ref was -inf
-          moved |= (alpha[x] != 1.0f) && (m_ref[x] != kNegInf);
-          m_ref[x] = mn;
-          sc[x] = (sc[x] == kNegInf) ? 0.0f : ex2_approx(sc[x] - mn);  // P
-          l_part[x] = __fmaf_rn(l_part[x], alpha[x], sc[x]);
+          for (int x = 0; x < NC; ++x) {
+            alpha[x] = 1.0f;
+            sc[x] = (sc[x] == kNegInf) ? 0.0f : ex2_approx(sc[x] - m_ref[x]);  // P
+            l_part[x] = __fmaf_rn(l_part[x], 1.0f, sc[x]);
+          }
+        } else {
+          // the tile's column max over 128 positions, exchanged through shared memory
+          float *rd = red + (T & 1) * 4 * N;
+#pragma unroll
+          for (int x = 0; x < NC; ++x) {
+            float mx = sc[x];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            if (lane == x) rd[qd * N + c0 + x] = mx;
+          }
+          ok = named_barrier_and(1, kSmxThreads, got);
+          if (!ok) break;
+#pragma unroll
+          for (int x = 0; x < NC; ++x) {
+            const int m = c0 + x;
+            const float tmax = fmaxf(fmaxf(rd[m], rd[N + m]), fmaxf(rd[2 * N + m], rd[3 * N + m]));
+            const float mn = (tmax > m_ref[x] + kSlack) ? tmax : m_ref[x];
+            alpha[x] = (mn == m_ref[x]) ? 1.0f : ex2_approx(m_ref[x] - mn);  // 0 when m_ref was -inf
+            moved |= (alpha[x] != 1.0f) && (m_ref[x] != kNegInf);
+            m_ref[x] = mn;
+            sc[x] = (sc[x] == kNegInf) ? 0.0f : ex2_approx(sc[x] - mn);  // P
+            l_part[x] = __fmaf_rn(l_part[x], alpha[x], sc[x]);
+          }
+          moved = __any_sync(0xffffffffu, moved);
         }
-        moved = __any_sync(0xffffffffu, moved);
         // the previous tile's O^T MMAs are done before P and O are touched (a
         // failed wait is shared at the next barrier)
         if (T > 0) {
