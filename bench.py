@@ -81,7 +81,7 @@ def tensor_peak(w_fmt: int):
 # (device helpers, parameter structs, launch declarations) count for every one
 KERNEL_FILES = {"tc": "kernel_tc.cu", "tc_ksplit_cluster4": "kernel_ks.cu", "simt": "kernel_simt.cu",
                 "dcp_pack": "kernel_pack.cu", "attn_split_kv": "kernel_attn.cu",
-                "attn_combine_uv_fused": "kernel_attn.cu",
+                "attn_combine_uv_fused": "kernel_attn.cu", "attn_combine_uv_oproj_fused": "kernel_attn.cu",
                 "o_proj": ("kernel_oproj.cu", "kernel_oproj.h")}
 SHARED_SOURCES = ("device_common.cuh", "kernels.h", "kparams.h")
 
