@@ -226,10 +226,11 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_
 EncodeTiledFn g_encode = nullptr;
 
 // TMA descriptor of the cache tensor [B, Lmax, 576] bf16: boxes of 64
-// elements x 128 positions x 1 request with the 128-byte swizzle (the
-// layout the tensor-core descriptors of the attention kernel read);
-// positions past Lmax read as zero.
-int32_t make_kv_tmap(const mla_attn_split_kv_args *a, CUtensorMap *tm) {
+// elements x box_rows positions (a tile of the attention kernel: 64 or 128)
+// x 1 request with the 128-byte swizzle (the layout the tensor-core
+// descriptors of the attention kernels read); positions past Lmax read as
+// zero.
+int32_t make_kv_tmap(const mla_attn_split_kv_args *a, int box_rows, CUtensorMap *tm) {
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_encode) {
@@ -245,7 +246,7 @@ int32_t make_kv_tmap(const mla_attn_split_kv_args *a, CUtensorMap *tm) {
   cuuint64_t dims[3] = {576, (cuuint64_t)a->Lmax, (cuuint64_t)a->B};
   cuuint64_t strides[2] = {(cuuint64_t)a->kv_sl * 2, (cuuint64_t)a->kv_sb * 2};
   if (a->B == 1) strides[1] = (cuuint64_t)a->Lmax * (cuuint64_t)a->kv_sl * 2;  // unused dimension
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a->kv), dims, strides, box,
                               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -443,7 +444,8 @@ int32_t mla_attn_split_kv(const mla_attn_split_kv_args *a, void *stream) {
     return MLA_ERR_STRIDE;
   if (a->kernel < 0 || a->kernel > 2) return MLA_ERR_KERNEL;
   CUtensorMap tm;
-  int32_t st = make_kv_tmap(a, &tm);
+  const int rows = ((a->q * G + 15) / 16) * 16;
+  int32_t st = make_kv_tmap(a, a->kernel == 2 ? 128 : mla::attn_tile_positions(rows, false), &tm);
   if (st != MLA_OK) return st;
   int dev, sms;
   int *err;
@@ -543,7 +545,7 @@ int32_t mla_attn_combine_uv(const mla_attn_combine_uv_args *a, void *stream) {
   aa.kv_sl = a->kv_sl;
   aa.Lmax = a->Lmax;
   CUtensorMap tm, wm, om, xm;
-  st = make_kv_tmap(&aa, &tm);
+  st = make_kv_tmap(&aa, mla::attn_tile_positions(((a->q * G + 15) / 16) * 16, true), &tm);
   if (st != MLA_OK) return st;
   st = make_wv_tmap(a->w_v, a->H, a->w_sh, a->w_sv, &wm);
   if (st != MLA_OK) return st;

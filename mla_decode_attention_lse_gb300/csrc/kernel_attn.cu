@@ -61,12 +61,9 @@ namespace mla {
 namespace {
 
 constexpr int kAttnK = kD + 64;     // query / cached row width (576)
-constexpr int kAttnTile = 128;      // positions per tile (MMA M of S^T)
-constexpr int kAttnDbl = 5;         // double-block slots (a tile needs 4)
 constexpr int kAttnSmx = 8;         // softmax warps: two per TMEM lane quadrant, half the query rows each
 constexpr int kAttnThreads = (3 + kAttnSmx) * 32;  // warp 0 TMA, warp 1 MMA, softmax warps, one query warp
-constexpr uint32_t kDblBytes = 2u * kAttnTile * 128u;  // 32 KiB
-constexpr uint32_t kRopeBytes = kAttnTile * 128u;      // 16 KiB
+constexpr uint32_t kWvBytes = 128u * 1024u;  // FUSED: W_V[h], [128 x 512] bf16
 
 constexpr int kItemRing = 4;        // FUSED: items handed from the TMA lane to the other roles
 constexpr int kItemTakers = 2 + kAttnSmx;  // MMA lane, query warp, softmax warps
@@ -74,14 +71,26 @@ constexpr int kCmbTile = 8;         // FUSED: tokens per combine unit (one mergi
 constexpr int kOpStages = 10;       // FUSED o_proj: stages of a weight box and a core box (16 KiB each)
 constexpr uint32_t kOpBox = 64u * 128u;  // 64 rows x 64 bf16, 128-byte swizzle
 
+// Two tilings.  The attention alone with up to 16 query rows (N = 16) runs
+// two CTAs per SM, each with 64-position tiles (a tile's S^T is an M = 64 MMA,
+// D row i in TMEM lane 32 (i / 16) + i % 16) and one tile's four latent
+// double blocks plus two rope slots: one CTA's copies land while the other
+// computes.  The fused launch (which keeps W_V[h] in shared memory for its
+// combine units) and N = 32 run one CTA per SM with 128-position tiles and a
+// ring of five double blocks.
 template <int N, bool FUSED = false>
 struct AttnLayout {
-  static constexpr int kRope = (N == 16) ? 2 : 1;  // rope-block slots
+  static constexpr int kCtas = (N == 16 && !FUSED) ? 2 : 1;   // CTAs per SM
+  static constexpr int kTile = kCtas == 2 ? 64 : 128;          // positions per tile (MMA M of S^T)
+  static constexpr uint32_t kDblBytes = 2u * kTile * 128u;     // latents 128 c .. 128 c + 127 of a tile
+  static constexpr uint32_t kRopeBytes = kTile * 128u;         // the tile's rope block
+  static constexpr int kDbl = kCtas == 2 ? 4 : 5;              // double-block slots (a tile needs 4)
+  static constexpr int kRope = kCtas == 2 ? 2 : (N == 16) ? 2 : 1;  // rope-block slots
   static constexpr uint32_t dbl_off = 0;
-  static constexpr uint32_t rope_off = dbl_off + kAttnDbl * kDblBytes;
+  static constexpr uint32_t rope_off = dbl_off + kDbl * kDblBytes;
   static constexpr uint32_t q_off = rope_off + kRope * kRopeBytes;  // 9 K blocks of [N x 128 B]
-  static constexpr uint32_t p_off = q_off + 9u * N * 128u;          // 2 K blocks of [N x 128 B]
-  static constexpr uint32_t red_off = p_off + 2u * N * 128u;        // float [2][4][N] (by tile parity)
+  static constexpr uint32_t p_off = q_off + 9u * N * 128u;          // kTile / 64 K blocks of [N x 128 B]
+  static constexpr uint32_t red_off = p_off + (kTile / 64) * N * 128u;  // float [2][4][N] (by tile parity)
   static constexpr uint32_t lim_off = red_off + 2u * 4u * N * 4u;   // int [N]
   static constexpr uint32_t row_off = (lim_off + N * 4u + 7u) & ~7u;  // long long [N]: o / lse row of a query row
   static constexpr uint32_t bar_off = row_off + N * 8u;
@@ -89,7 +98,7 @@ struct AttnLayout {
   // s_full, s_free, p_full, o_full, q_full, q_free
   // FUSED adds: item full / empty per ring slot, W_V full, combine MMA done,
   // then the o_proj stages' full / empty and its accumulator's full
-  static constexpr int kBars = 2 * kAttnDbl + 2 * kRope + 6 + (FUSED ? 2 * kItemRing + 2 + 2 * kOpStages + 1 : 0);
+  static constexpr int kBars = 2 * kDbl + 2 * kRope + 6 + (FUSED ? 2 * kItemRing + 2 + 2 * kOpStages + 1 : 0);
   // misc: [0] TMEM base, [1] abort flag, [2 .. 2 + kItemRing) item ring,
   // [6] the combine unit drawn last
   static constexpr uint32_t misc_off = bar_off + kBars * 8u;
@@ -100,9 +109,13 @@ static_assert(AttnLayout<16, true>::total + 1024 <= 227u * 1024u, "shared memory
 static_assert(AttnLayout<32, true>::total + 1024 <= 227u * 1024u, "shared memory (N = 32)");
 // FUSED: W_V[h] (128 KiB) reuses the first four double-block slots, the
 // latent tile [16 x 512] bf16 (16 KiB) the first rope slot
-static_assert(4 * kDblBytes == 128u * 1024u && kRopeBytes >= 16u * 1024u, "combine tiles");
+static_assert(AttnLayout<16, false>::total + 1024 <= 113u * 1024u, "shared memory (two CTAs per SM)");
+static_assert(AttnLayout<16, true>::kTile == 128 && AttnLayout<32, true>::kTile == 128 &&
+                  4 * AttnLayout<16, true>::kDblBytes == kWvBytes && AttnLayout<16, true>::kRopeBytes >= 16u * 1024u &&
+                  AttnLayout<32, true>::kRopeBytes >= 16u * 1024u,
+              "combine tiles");
 // FUSED o_proj: its stage ring reuses the latent double-block slots
-static_assert(kOpStages * 2u * kOpBox <= kAttnDbl * kDblBytes, "o_proj stages");
+static_assert(kOpStages * 2u * kOpBox <= 5 * AttnLayout<16, true>::kDblBytes, "o_proj stages");
 
 // Bounded wait on an mbarrier phase, shared abort flag (as the combine kernels).
 __device__ __forceinline__ bool attn_wait(uint32_t bar, uint32_t parity, int *err, volatile int *abort_flag) {
@@ -178,7 +191,7 @@ __device__ __forceinline__ void combine_phase(const AttnParams &p, const CUtenso
       // W_V[h] first (a weight: it does not wait for the attention), so its
       // copy overlaps the wait for the tile's partials
       if (new_h) {
-        mbar_arrive_expect_tx(wv_full, 4u * kDblBytes);
+        mbar_arrive_expect_tx(wv_full, kWvBytes);
 #pragma unroll 1
         for (int kb = 0; kb < 8; ++kb) tma_load_3d(sA + (uint32_t)kb * 16384u, &wv_map, 64 * kb, 0, h, wv_full);
         ++wv_issued;
@@ -480,12 +493,15 @@ __device__ __forceinline__ void finish_workspace(const AttnParams &p) {
 }  // namespace
 
 template <int N, bool FUSED>
-__global__ void __launch_bounds__(kAttnThreads, 1)
+__global__ void __launch_bounds__(kAttnThreads, AttnLayout<N, FUSED>::kCtas)
     attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap kv_map,
                 const __grid_constant__ CUtensorMap wv_map, const __grid_constant__ CUtensorMap wo_map,
                 const __grid_constant__ CUtensorMap x_map) {
   using L = AttnLayout<N, FUSED>;
   constexpr int NR = L::kRope;
+  constexpr int kAttnDbl = L::kDbl;
+  constexpr int kAttnTile = L::kTile;
+  constexpr uint32_t kDblBytes = L::kDblBytes, kRopeBytes = L::kRopeBytes;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;  // swizzle atoms: 1024-byte aligned
@@ -658,7 +674,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   } else if (warp == 1) {
     // ---- MMA issuer ----
     if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_bf16(128, N);
+      constexpr uint32_t kIdS = idesc_bf16(kAttnTile, N);  // M = the tile's positions
       constexpr uint32_t kIdO = idesc_bf16(128, N) | (1u << 15);  // A = V^T, MN-major
       const uint32_t tS = tmem, tO = tmem + (uint32_t)N;
       const uint32_t dQ = (uint32_t)smem_desc_sw128(sbase + L::q_off);
@@ -717,7 +733,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           for (int c = 0; c < 4; ++c) {
             const uint32_t vbase = sbase + L::dbl_off + (uint32_t)((4 * T + c) % kAttnDbl) * kDblBytes;
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks)  // 16 positions per step
+            for (int ks = 0; ks < kAttnTile / 16; ++ks)  // 16 positions per step
               tc_mma_f16(tO + (uint32_t)(c * N), smem_desc_mn_sw128(vbase + (uint32_t)ks * 2048u, kDblBytes / 2),
                          desc_sw128_at(dP, ((uint32_t)ks >> 2) * (N * 128u) + ((uint32_t)ks & 3u) * 32u), kIdO,
                          (t | ks) ? 1u : 0u);
@@ -784,7 +800,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     constexpr uint32_t kSmxThreads = kAttnSmx * 32;
     const int qd = warp & 3;                      // TMEM lane quadrant
     const int c0 = ((warp - 2) >> 2) * NC;        // this warp's first query row
-    const int pos = qd * 32 + lane;               // position within a tile; O^T row within a latent chunk
+    // S^T holds position 32 qd + lane of a 128-position tile, or (M = 64)
+    // position 16 qd + lane of a 64-position tile in lanes 0 .. 15; O^T row 32 qd + lane
+    const bool has_pos = kAttnTile == 128 || lane < 16;
+    const int pos = kAttnTile == 128 ? qd * 32 + lane : qd * 16 + (lane & 15);  // position within a tile
+    const int dv = qd * 32 + lane;                // O^T row within a latent chunk
     const int ts = threadIdx.x - 64;              // 0 .. kSmxThreads - 1
     const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);
     const int qG = p.q * p.G;
@@ -839,7 +859,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const long long row = orow_s[c0 + x];
           if (row >= 0)
 #pragma unroll
-            for (int c = 0; c < 4; ++c) p.o[row * kD + 128 * c + pos] = 0;
+            for (int c = 0; c < 4; ++c) p.o[row * kD + 128 * c + dv] = 0;
         }
         arrive_tiles(I);
         continue;
@@ -875,7 +895,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         bool up = false;  // a score of this thread exceeds its column's reference by more than the slack
 #pragma unroll
         for (int x = 0; x < NC; ++x) {
-          sc[x] = (jr < lim[x]) ? __uint_as_float(sr[x]) * p.scale_log2 : kNegInf;
+          sc[x] = (has_pos && jr < lim[x]) ? __uint_as_float(sr[x]) * p.scale_log2 : kNegInf;
           up |= sc[x] > m_ref[x] + kSlack;
         }
         // After an item's first tile a column's reference rarely moves: one
@@ -926,7 +946,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           tc_fence_after();
         }
         // P^T row m, column pos (K-major, 128-byte swizzle, K blocks of 64 positions)
-        {
+        if (has_pos) {
           uint8_t *pb = gbase + L::p_off + (pos >> 6) * (N * 128);
           const int x2 = (pos & 63) * 2;
 #pragma unroll
@@ -939,7 +959,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // a cached row past kv_len (inside the cache tensor) may hold anything:
         // its latent is zeroed (by one warp of the quadrant) so that 0 * it
         // stays 0 in O
-        if (c0 == 0 && I.j0 + jr >= I.Lb && I.j0 + jr < p.Lmax) {
+        if (c0 == 0 && has_pos && I.j0 + jr >= I.Lb && I.j0 + jr < p.Lmax) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint8_t *rowp = gbase + L::dbl_off + (size_t)((4 * T + c) % kAttnDbl) * kDblBytes + pos * 128;
@@ -1008,7 +1028,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
       for (int x = 0; x < NC; ++x) {
         const long long row = orow_s[c0 + x];
-        orow[x] = row >= 0 ? p.o + row * kD + pos : nullptr;
+        orow[x] = row >= 0 ? p.o + row * kD + dv : nullptr;
       }
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -1052,6 +1072,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 int attn_heads_per_cta(int q, int H) { return q * H <= 32 ? H : (32 / q > 0 ? 32 / q : 1); }
 int attn_rows(int q, int H) { return ((q * attn_heads_per_cta(q, H) + 15) / 16) * 16; }
 size_t attn_smem_bytes(int rows) { return 1024 + (rows <= 16 ? AttnLayout<16>::total : AttnLayout<32>::total); }
+int attn_tile_positions(int rows, bool fused) {
+  return fused ? AttnLayout<16, true>::kTile : rows <= 16 ? AttnLayout<16, false>::kTile : AttnLayout<32, false>::kTile;
+}
 int attn_combine_tiles(int S) { return (S + kCmbTile - 1) / kCmbTile; }
 
 template <int N, bool FUSED>
@@ -1081,9 +1104,10 @@ static cudaError_t launch_attn_n(const AttnParams &p, const CUtensorMap &map, co
 cudaError_t launch_attn(const AttnParams &p, const CUtensorMap &map, int num_sms, cudaStream_t stream) {
   const long long items = (long long)p.B * p.spr * p.groups;
   if (items <= 0 || items >= (1LL << 31) || num_sms < 1) return cudaErrorInvalidValue;
-  const unsigned grid = (unsigned)(items < num_sms ? items : num_sms);
   const int rows = ((p.q * p.G + 15) / 16) * 16;  // the host keeps q G <= 32
   if (rows > 32) return cudaErrorInvalidValue;
+  const long long slots = (long long)num_sms * (rows <= 16 ? AttnLayout<16, false>::kCtas : AttnLayout<32, false>::kCtas);
+  const unsigned grid = (unsigned)(items < slots ? items : slots);
   CUtensorMap none;
   std::memset(&none, 0, sizeof none);
   return rows <= 16 ? launch_attn_n<16, false>(p, map, none, none, none, grid, stream)

@@ -46,6 +46,9 @@ cudaError_t launch_pack(const PackParams &p, int grid, cudaStream_t stream);
 int attn_heads_per_cta(int q, int H);  // G
 int attn_rows(int q, int H);           // the MMA's N: q * G rounded up to 16
 size_t attn_smem_bytes(int rows);
+// Cached positions per tile of the attention kernel for `rows` query rows
+// (the TMA box height of the cache tensor's map): 64 or 128.
+int attn_tile_positions(int rows, bool fused);
 cudaError_t launch_attn(const AttnParams &p, const CUtensorMap &map, int num_sms, cudaStream_t stream);
 // The same attention on 2-CTA clusters: each CTA holds half of every cached
 // row's latents (rank 1 also the rope part), the partial scores meet through
