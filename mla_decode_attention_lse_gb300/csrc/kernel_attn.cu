@@ -68,24 +68,25 @@ constexpr uint32_t kWvBytes = 128u * 1024u;  // FUSED: W_V[h], [128 x 512] bf16
 constexpr int kItemRing = 4;        // FUSED: items handed from the TMA lane to the other roles
 constexpr int kItemTakers = 2 + kAttnSmx;  // MMA lane, query warp, softmax warps
 constexpr int kCmbTile = 8;         // FUSED: tokens per combine unit (one merging warp each)
-constexpr int kOpStages = 10;       // FUSED o_proj: stages of a weight box and a core box (16 KiB each)
 constexpr uint32_t kOpBox = 64u * 128u;  // 64 rows x 64 bf16, 128-byte swizzle
 
-// Two tilings.  The attention alone with up to 16 query rows (N = 16) runs
-// two CTAs per SM, each with 64-position tiles (a tile's S^T is an M = 64 MMA,
-// D row i in TMEM lane 32 (i / 16) + i % 16) and one tile's four latent
-// double blocks plus two rope slots: one CTA's copies land while the other
-// computes.  The fused launch (which keeps W_V[h] in shared memory for its
-// combine units) and N = 32 run one CTA per SM with 128-position tiles and a
-// ring of five double blocks.
+// Two tilings.  Up to 16 query rows (N = 16) run two CTAs per SM, each with
+// 64-position tiles (a tile's S^T is an M = 64 MMA, D row i in TMEM lane
+// 32 (i / 16) + i % 16) and one tile's four latent double blocks plus two
+// rope slots: one CTA's copies land while the other computes (the fused
+// launch's combine units then stream W_V[h] through two 32-KiB slots).
+// N = 32 runs one CTA per SM with 128-position tiles and a ring of five
+// double blocks (its combine units keep W_V[h] resident).
 template <int N, bool FUSED = false>
 struct AttnLayout {
-  static constexpr int kCtas = (N == 16 && !FUSED) ? 2 : 1;   // CTAs per SM
+  static constexpr int kCtas = (N == 16) ? 2 : 1;             // CTAs per SM
   static constexpr int kTile = kCtas == 2 ? 64 : 128;          // positions per tile (MMA M of S^T)
   static constexpr uint32_t kDblBytes = 2u * kTile * 128u;     // latents 128 c .. 128 c + 127 of a tile
   static constexpr uint32_t kRopeBytes = kTile * 128u;         // the tile's rope block
   static constexpr int kDbl = kCtas == 2 ? 4 : 5;              // double-block slots (a tile needs 4)
-  static constexpr int kRope = kCtas == 2 ? 2 : (N == 16) ? 2 : 1;  // rope-block slots
+  static constexpr int kRope = kCtas == 2 ? 2 : 1;                // rope-block slots
+  // FUSED o_proj: stages of a weight box and a core box (16 KiB each) below the barriers
+  static constexpr int kOp = kCtas == 2 ? 6 : 10;
   static constexpr uint32_t dbl_off = 0;
   static constexpr uint32_t rope_off = dbl_off + kDbl * kDblBytes;
   static constexpr uint32_t q_off = rope_off + kRope * kRopeBytes;  // 9 K blocks of [N x 128 B]
@@ -98,7 +99,7 @@ struct AttnLayout {
   // s_full, s_free, p_full, o_full, q_full, q_free
   // FUSED adds: item full / empty per ring slot, W_V full, combine MMA done,
   // then the o_proj stages' full / empty and its accumulator's full
-  static constexpr int kBars = 2 * kDbl + 2 * kRope + 6 + (FUSED ? 2 * kItemRing + 2 + 2 * kOpStages + 1 : 0);
+  static constexpr int kBars = 2 * kDbl + 2 * kRope + 6 + (FUSED ? 2 * kItemRing + 5 + 2 * kOp + 1 : 0);
   // misc: [0] TMEM base, [1] abort flag, [2 .. 2 + kItemRing) item ring,
   // [6] the combine unit drawn last
   static constexpr uint32_t misc_off = bar_off + kBars * 8u;
@@ -109,13 +110,19 @@ static_assert(AttnLayout<16, true>::total + 1024 <= 227u * 1024u, "shared memory
 static_assert(AttnLayout<32, true>::total + 1024 <= 227u * 1024u, "shared memory (N = 32)");
 // FUSED: W_V[h] (128 KiB) reuses the first four double-block slots, the
 // latent tile [16 x 512] bf16 (16 KiB) the first rope slot
-static_assert(AttnLayout<16, false>::total + 1024 <= 113u * 1024u, "shared memory (two CTAs per SM)");
-static_assert(AttnLayout<16, true>::kTile == 128 && AttnLayout<32, true>::kTile == 128 &&
-                  4 * AttnLayout<16, true>::kDblBytes == kWvBytes && AttnLayout<16, true>::kRopeBytes >= 16u * 1024u &&
-                  AttnLayout<32, true>::kRopeBytes >= 16u * 1024u,
+static_assert(AttnLayout<16, false>::total + 1024 <= 113u * 1024u && AttnLayout<16, true>::total + 1024 <= 113u * 1024u,
+              "shared memory (two CTAs per SM)");
+// FUSED combine: W_V[h] resident in the first four double slots (one CTA per
+// SM) or streamed in quarters through two 32-KiB slots (two CTAs per SM); the
+// latent tile [16 x 512] bf16 in the rope slots
+static_assert(4 * AttnLayout<32, true>::kDblBytes == kWvBytes && AttnLayout<32, true>::kRope * AttnLayout<32, true>::kRopeBytes >= 16u * 1024u &&
+                  AttnLayout<16, true>::kDbl * AttnLayout<16, true>::kDblBytes >= kWvBytes / 2 &&
+                  AttnLayout<16, true>::kRope * AttnLayout<16, true>::kRopeBytes >= 16u * 1024u,
               "combine tiles");
 // FUSED o_proj: its stage ring reuses the latent double-block slots
-static_assert(kOpStages * 2u * kOpBox <= 5 * AttnLayout<16, true>::kDblBytes, "o_proj stages");
+static_assert(AttnLayout<16, true>::kOp * 2u * kOpBox <= AttnLayout<16, true>::bar_off &&
+                  AttnLayout<32, true>::kOp * 2u * kOpBox <= AttnLayout<32, true>::bar_off,
+              "o_proj stages");
 
 // Bounded wait on an mbarrier phase, shared abort flag (as the combine kernels).
 __device__ __forceinline__ bool attn_wait(uint32_t bar, uint32_t parity, int *err, volatile int *abort_flag) {
@@ -163,8 +170,12 @@ __device__ __forceinline__ float ld_cg_f32(const float *p) {
 template <int N>
 __device__ __forceinline__ void combine_phase(const AttnParams &p, const CUtensorMap &wv_map, uint32_t sbase,
                                               uint8_t *gbase, uint32_t tmem, uint32_t *misc, volatile int *s_abort,
-                                              uint32_t wv_full, uint32_t cmb_mma, int nitems) {
+                                              uint32_t wv_full, uint32_t wv_free, uint32_t cmb_mma, int nitems) {
   using L = AttnLayout<N, true>;
+  // W_V[h] resident (one CTA per SM: reloaded only when the head changes), or
+  // streamed per unit in quarters (kb 2q, 2q + 1) through two 32-KiB slots
+  // (two CTAs per SM): the MMAs of a quarter run while the next one lands
+  constexpr bool kStream = L::kCtas == 2;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = p.B * p.q, H = p.H, n = p.spr;
   const int nunits = p.ntiles * H;
@@ -179,9 +190,18 @@ __device__ __forceinline__ void combine_phase(const AttnParams &p, const CUtenso
   __syncthreads();  // every role is done with its attention items (copies landed, MMAs complete)
   tc_fence_after();
   int cur_h = -1, units = 0;
-  int wv_issued = 0;   // thread 0: W_V loads issued
+  int wv_issued = 0;   // thread 0: W_V loads issued (resident: whole W_V; streamed: quarters)
   int mma_issued = 0;  // MMA lane: units whose MMAs it committed
-  int wv_seen = 0;     // every thread: W_V loads so far
+  int q_done = 0;      // MMA lane (streamed): quarters whose MMAs it committed
+  int wv_seen = 0;     // every thread: W_V loads so far (resident)
+  // streamed quarter q of W_V[h] (8 K blocks of 64, boxes [128 x 64]) into slot q % 2
+  auto load_quarter = [&](int q, int h) {
+    const uint32_t bar = wv_full + 8u * (uint32_t)(q & 1);
+    mbar_arrive_expect_tx(bar, kWvBytes / 4);
+    for (int j = 0; j < 2; ++j)
+      tma_load_3d(sA + (uint32_t)(q & 1) * 32768u + (uint32_t)j * 16384u, &wv_map, 64 * (2 * q + j), 0, h, bar);
+    ++wv_issued;
+  };
   uint32_t unit = misc[6];
   while (!*s_abort && unit != 0xFFFFFFFFu && (int)unit - nitems < nunits) {
     const int u = (int)unit - nitems;
@@ -190,7 +210,10 @@ __device__ __forceinline__ void combine_phase(const AttnParams &p, const CUtenso
     if (threadIdx.x == 0) {
       // W_V[h] first (a weight: it does not wait for the attention), so its
       // copy overlaps the wait for the tile's partials
-      if (new_h) {
+      if constexpr (kStream) {
+        load_quarter(0, h);
+        load_quarter(1, h);
+      } else if (new_h) {
         mbar_arrive_expect_tx(wv_full, kWvBytes);
 #pragma unroll 1
         for (int kb = 0; kb < 8; ++kb) tma_load_3d(sA + (uint32_t)kb * 16384u, &wv_map, 64 * kb, 0, h, wv_full);
@@ -275,7 +298,39 @@ __device__ __forceinline__ void combine_phase(const AttnParams &p, const CUtenso
       fence_proxy_async_smem();
     }
     __syncthreads();
-    if (warp == 1 && lane == 0) {
+    if constexpr (kStream) {
+      if (threadIdx.x == 0) {
+        // quarters 2 and 3 into the slots quarters 0 and 1 free (each slot's
+        // first free of the unit: parity 0)
+        for (int q = 2; q < 4; ++q) {
+          if (!attn_wait(wv_free + 8u * (uint32_t)(q & 1), 0u, p.err, s_abort)) break;
+          load_quarter(q, h);
+        }
+      } else if (warp == 1 && lane == 0) {
+        // D[v, token] = sum_k W_V[h][v][k] lat[token][k]: M = 128, N = 16, K = 512, quarter by quarter
+        bool ok = true;
+        const uint32_t dB = (uint32_t)smem_desc_sw128(sB);
+        constexpr uint32_t kIdesc = idesc_bf16(128, 16);
+        for (int q = 0; q < 4 && ok; ++q) {
+          ok = attn_wait(wv_full + 8u * (uint32_t)(q & 1), (uint32_t)(q >> 1), p.err, s_abort);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t dA = (uint32_t)smem_desc_sw128(sA + (uint32_t)(q & 1) * 32768u);
+#pragma unroll
+          for (int k8 = 0; k8 < 8; ++k8) {
+            const uint32_t j = (uint32_t)k8 >> 2, kk = (uint32_t)k8 & 3u, kb = 2u * q + j;
+            tc_mma_f16(tmem, desc_sw128_at(dA, j * 16384u + kk * 32u), desc_sw128_at(dB, kb * 2048u + kk * 32u), kIdesc,
+                       (q | k8) ? 1u : 0u);
+          }
+          tc_commit(wv_free + 8u * (uint32_t)(q & 1));
+          ++q_done;
+        }
+        if (ok) {
+          tc_commit(cmb_mma);
+          ++mma_issued;
+        }
+      }
+    } else if (warp == 1 && lane == 0) {
       // D[v, token] = sum_k W_V[h][v][k] lat[token][k]: M = 128, N = 16, K = 512
       const bool ok = !new_h || attn_wait(wv_full, (uint32_t)(wv_seen - 1) & 1u, p.err, s_abort);
       if (ok) {
@@ -330,7 +385,16 @@ __device__ __forceinline__ void combine_phase(const AttnParams &p, const CUtenso
     unit = misc[6];
   }
   // after an abort: this CTA's weight copies and MMAs land before it exits
-  if (threadIdx.x == 0 && wv_issued > 0) mbar_wait(wv_full, (uint32_t)(wv_issued - 1) & 1u, p.err, kErrWaitTeardown);
+  if constexpr (kStream) {
+    if (threadIdx.x == 0)  // quarter g of the CTA went to slot g % 2, the (g / 2)-th use of its barrier
+      for (int g = wv_issued - 2 < 0 ? 0 : wv_issued - 2; g < wv_issued; ++g)
+        mbar_wait(wv_full + 8u * (uint32_t)(g & 1), (uint32_t)(g >> 1) & 1u, p.err, kErrWaitTeardown);
+    if (warp == 1 && lane == 0 && q_done > 0)
+      mbar_wait(wv_free + 8u * (uint32_t)((q_done - 1) & 1), (uint32_t)((q_done - 1) >> 1) & 1u, p.err,
+                kErrWaitTeardown);
+  } else if (threadIdx.x == 0 && wv_issued > 0) {
+    mbar_wait(wv_full, (uint32_t)(wv_issued - 1) & 1u, p.err, kErrWaitTeardown);
+  }
   if (warp == 1 && lane == 0 && mma_issued > 0)
     mbar_wait(cmb_mma, (uint32_t)(mma_issued - 1) & 1u, p.err, kErrWaitTeardown);
   // rows S .. S_out - 1 of core are zero (this CTA's slice of them)
@@ -366,8 +430,8 @@ __device__ __forceinline__ void oproj_phase(const AttnParams &p, const CUtensorM
   const int S = p.B * p.q, K = p.H * kV, KB = K / 64, MT = p.n_out / 64;
   const int base = p.B * p.spr * p.groups + p.ntiles * p.H;  // queue index of o_proj unit 0
   auto full = [&](int s) { return obar + 8u * (uint32_t)s; };
-  auto empty = [&](int s) { return obar + 8u * (uint32_t)(kOpStages + s); };
-  const uint32_t acc_full = obar + 8u * (uint32_t)(2 * kOpStages);
+  auto empty = [&](int s) { return obar + 8u * (uint32_t)(L::kOp + s); };
+  const uint32_t acc_full = obar + 8u * (uint32_t)(2 * L::kOp);
   auto sA = [&](int s) { return sbase + L::dbl_off + (uint32_t)s * 2u * kOpBox; };
   auto sB = [&](int s) { return sbase + L::dbl_off + (uint32_t)s * 2u * kOpBox + kOpBox; };
 
@@ -386,7 +450,7 @@ __device__ __forceinline__ void oproj_phase(const AttnParams &p, const CUtensorM
       bool ok = true;
       int pre = 0;
       if (!ready) {  // the CTA's first unit (g == 0): weight boxes first, then the wait
-        pre = KB < kOpStages ? KB : kOpStages;
+        pre = KB < L::kOp ? KB : L::kOp;
         for (int kb = 0; kb < pre; ++kb) {
           mbar_arrive_expect_tx(full(kb), 2u * kOpBox);
           tma_load_3d(sA(kb), &wo_map, 64 * kb, mt * 64, 0, full(kb));
@@ -405,8 +469,8 @@ __device__ __forceinline__ void oproj_phase(const AttnParams &p, const CUtensorM
         issued = pre;
       }
       for (int kb = pre; kb < KB && ok; ++kb, ++g) {
-        const int s = g % kOpStages;
-        if (g >= kOpStages) ok = attn_wait(empty(s), (uint32_t)(g / kOpStages - 1) & 1u, p.err, s_abort);
+        const int s = g % L::kOp;
+        if (g >= L::kOp) ok = attn_wait(empty(s), (uint32_t)(g / L::kOp - 1) & 1u, p.err, s_abort);
         if (!ok) break;
         mbar_arrive_expect_tx(full(s), 2u * kOpBox);
         tma_load_3d(sA(s), &wo_map, 64 * kb, mt * 64, 0, full(s));
@@ -417,8 +481,8 @@ __device__ __forceinline__ void oproj_phase(const AttnParams &p, const CUtensorM
       constexpr uint32_t kId = idesc_bf16(64, 64);
       bool ok = true;
       for (int kb = 0; kb < KB && ok; ++kb, ++g) {
-        const int s = g % kOpStages;
-        ok = attn_wait(full(s), (uint32_t)(g / kOpStages) & 1u, p.err, s_abort);
+        const int s = g % L::kOp;
+        ok = attn_wait(full(s), (uint32_t)(g / L::kOp) & 1u, p.err, s_abort);
         if (!ok) break;
         tc_fence_after();
         const uint32_t dA = (uint32_t)smem_desc_sw128(sA(s)), dB = (uint32_t)smem_desc_sw128(sB(s));
@@ -469,8 +533,8 @@ __device__ __forceinline__ void oproj_phase(const AttnParams &p, const CUtensorM
   }
   // after an abort: this CTA's copies land and its committed MMAs complete
   if (threadIdx.x == 0)
-    for (int q = issued - kOpStages < 0 ? 0 : issued - kOpStages; q < issued; ++q)
-      mbar_wait(full(q % kOpStages), (uint32_t)(q / kOpStages) & 1u, p.err, kErrWaitTeardown);
+    for (int q = issued - L::kOp < 0 ? 0 : issued - L::kOp; q < issued; ++q)
+      mbar_wait(full(q % L::kOp), (uint32_t)(q / L::kOp) & 1u, p.err, kErrWaitTeardown);
   if (warp == 1 && lane == 0 && last_mma >= 0) mbar_wait(acc_full, (uint32_t)last_mma & 1u, p.err, kErrWaitTeardown);
 }
 
@@ -526,8 +590,10 @@ __global__ void __launch_bounds__(kAttnThreads, AttnLayout<N, FUSED>::kCtas)
   // taker has read it), W_V of a combine unit in shared memory, its MMAs done
   auto item_full = [&](int s) { return s_full + 48u + 8u * (uint32_t)s; };
   auto item_empty = [&](int s) { return s_full + 48u + 8u * (uint32_t)(kItemRing + s); };
+  // W_V slots: full / free (a streamed quarter's MMAs are done), two each
   const uint32_t wv_full = s_full + 48u + 8u * (uint32_t)(2 * kItemRing);
-  const uint32_t cmb_mma = wv_full + 8u;
+  const uint32_t wv_free = wv_full + 16u;
+  const uint32_t cmb_mma = wv_free + 16u;
   const uint32_t op_bar = cmb_mma + 8u;  // FUSED o_proj: full / empty per stage, accumulator full
   volatile uint32_t *ring = misc + 2;
 
@@ -552,9 +618,9 @@ __global__ void __launch_bounds__(kAttnThreads, AttnLayout<N, FUSED>::kCtas)
         mbar_init(item_full(s), 1u);
         mbar_init(item_empty(s), (uint32_t)kItemTakers);
       }
-      mbar_init(wv_full, 1u);
+      for (int b = 0; b < 4; ++b) mbar_init(wv_full + 8u * (uint32_t)b, 1u);  // wv_full[2], wv_free[2]
       mbar_init(cmb_mma, 1u);
-      for (int s = 0; s < 2 * kOpStages + 1; ++s) mbar_init(op_bar + 8u * (uint32_t)s, 1u);
+      for (int s = 0; s < 2 * L::kOp + 1; ++s) mbar_init(op_bar + 8u * (uint32_t)s, 1u);
     }
     misc[1] = 0u;
     misc[6] = 0xFFFFFFFFu;
@@ -1055,7 +1121,7 @@ __global__ void __launch_bounds__(kAttnThreads, AttnLayout<N, FUSED>::kCtas)
     grid_launch_dependents();
   }
   if constexpr (FUSED) {
-    combine_phase<N>(p, wv_map, sbase, gbase, tmem, misc, s_abort, wv_full, cmb_mma, nitems);
+    combine_phase<N>(p, wv_map, sbase, gbase, tmem, misc, s_abort, wv_full, wv_free, cmb_mma, nitems);
     if (p.n_out > 0) oproj_phase<N>(p, wo_map, x_map, sbase, tmem, misc, s_abort, op_bar);
     finish_workspace(p);
   }
@@ -1073,7 +1139,8 @@ int attn_heads_per_cta(int q, int H) { return q * H <= 32 ? H : (32 / q > 0 ? 32
 int attn_rows(int q, int H) { return ((q * attn_heads_per_cta(q, H) + 15) / 16) * 16; }
 size_t attn_smem_bytes(int rows) { return 1024 + (rows <= 16 ? AttnLayout<16>::total : AttnLayout<32>::total); }
 int attn_tile_positions(int rows, bool fused) {
-  return fused ? AttnLayout<16, true>::kTile : rows <= 16 ? AttnLayout<16, false>::kTile : AttnLayout<32, false>::kTile;
+  if (fused) return rows <= 16 ? AttnLayout<16, true>::kTile : AttnLayout<32, true>::kTile;
+  return rows <= 16 ? AttnLayout<16, false>::kTile : AttnLayout<32, false>::kTile;
 }
 int attn_combine_tiles(int S) { return (S + kCmbTile - 1) / kCmbTile; }
 
@@ -1114,18 +1181,20 @@ cudaError_t launch_attn(const AttnParams &p, const CUtensorMap &map, int num_sms
                     : launch_attn_n<32, false>(p, map, none, none, none, grid, stream);
 }
 
-// The fused attention + combine (+ o_proj): one CTA per SM over the attention
-// items, then the combine units (ntiles * H), then the o_proj units, all
-// drawn from the workspace queue.
+// The fused attention + combine (+ o_proj): a persistent grid (two CTAs per SM
+// for up to 16 query rows, else one) over the attention items, then the
+// combine units (ntiles * H), then the o_proj units, all drawn from the
+// workspace queue.
 cudaError_t launch_attn_combine(const AttnParams &p, const CUtensorMap &map, const CUtensorMap &wv_map,
                                 const CUtensorMap &wo_map, const CUtensorMap &x_map, int num_sms, cudaStream_t stream) {
   const long long work =
       (long long)p.B * p.spr * p.groups + (long long)p.ntiles * p.H + (p.n_out > 0 ? (long long)p.op_units : 0);
   if (work <= 0 || work >= (1LL << 31) || num_sms < 1 || !p.ws) return cudaErrorInvalidValue;
   if (p.n_out > 0 && (p.n_out % 64 || (p.H * kV) % 64 || !p.y)) return cudaErrorInvalidValue;
-  const unsigned grid = (unsigned)(work < num_sms ? work : num_sms);
   const int rows = ((p.q * p.G + 15) / 16) * 16;
   if (rows > 32 || p.spr > 32) return cudaErrorInvalidValue;
+  const long long slots = (long long)num_sms * (rows <= 16 ? AttnLayout<16, true>::kCtas : AttnLayout<32, true>::kCtas);
+  const unsigned grid = (unsigned)(work < slots ? work : slots);
   return rows <= 16 ? launch_attn_n<16, true>(p, map, wv_map, wo_map, x_map, grid, stream)
                     : launch_attn_n<32, true>(p, map, wv_map, wo_map, x_map, grid, stream);
 }
