@@ -257,11 +257,14 @@ __device__ __forceinline__ void combine_phase(const AttnParams &p, const CUtenso
       for (int x = 0; x < 8; ++x) acc[x] = 0ull;
       const long long pstride = (long long)S * H * kD;
       const uint16_t *row0 = p.o + ((long long)t * H + h) * kD;
-      for (int j0 = 0; j0 < n; j0 += 8) {
-        uint4 buf[8][2];
-        float w[8];
+      // batches of MB partial rows in flight (fewer with two CTAs per SM, whose
+      // threads have 80 registers)
+      constexpr int MB = kStream ? 4 : 8;
+      for (int j0 = 0; j0 < n; j0 += MB) {
+        uint4 buf[MB][2];
+        float w[MB];
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
+        for (int jj = 0; jj < MB; ++jj) {
           w[jj] = __shfl_sync(kFull, wg, (j0 + jj) & 31);  // 0 for partials past n
           if (w[jj] != 0.0f && valid) {
             const uint16_t *r = row0 + (long long)(j0 + jj) * pstride;
@@ -272,7 +275,7 @@ __device__ __forceinline__ void combine_phase(const AttnParams &p, const CUtenso
           }
         }
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
+        for (int jj = 0; jj < MB; ++jj) {
           if (w[jj] == 0.0f) continue;
           const uint64_t w2 = f2_pack(w[jj], w[jj]);
 #pragma unroll
