@@ -72,8 +72,8 @@ constexpr uint32_t kOpBox = 64u * 128u;  // 64 rows x 64 bf16, 128-byte swizzle
 
 // Two tilings.  Up to 16 query rows (N = 16) run two CTAs per SM, each with
 // 64-position tiles (a tile's S^T is an M = 64 MMA, D row i in TMEM lane
-// 32 (i / 16) + i % 16) and one tile's four latent double blocks plus two
-// rope slots: one CTA's copies land while the other computes (the fused
+// 32 (i / 16) + i % 16) and five latent double blocks plus a rope slot: one
+// CTA's copies land while the other computes (the fused
 // launch's combine units then stream W_V[h] through two 32-KiB slots).
 // N = 32 runs one CTA per SM with 128-position tiles and a ring of five
 // double blocks (its combine units keep W_V[h] resident).
@@ -83,8 +83,8 @@ struct AttnLayout {
   static constexpr int kTile = kCtas == 2 ? 64 : 128;          // positions per tile (MMA M of S^T)
   static constexpr uint32_t kDblBytes = 2u * kTile * 128u;     // latents 128 c .. 128 c + 127 of a tile
   static constexpr uint32_t kRopeBytes = kTile * 128u;         // the tile's rope block
-  static constexpr int kDbl = kCtas == 2 ? 4 : 5;              // double-block slots (a tile needs 4)
-  static constexpr int kRope = kCtas == 2 ? 2 : 1;                // rope-block slots
+  static constexpr int kDbl = 5;                               // double-block slots (a tile needs 4)
+  static constexpr int kRope = 1;                              // rope-block slots
   // FUSED o_proj: stages of a weight box and a core box (16 KiB each) below the barriers
   static constexpr int kOp = kCtas == 2 ? 6 : 10;
   static constexpr uint32_t dbl_off = 0;
@@ -117,7 +117,7 @@ static_assert(AttnLayout<16, false>::total + 1024 <= 113u * 1024u && AttnLayout<
 // latent tile [16 x 512] bf16 in the rope slots
 static_assert(4 * AttnLayout<32, true>::kDblBytes == kWvBytes && AttnLayout<32, true>::kRope * AttnLayout<32, true>::kRopeBytes >= 16u * 1024u &&
                   AttnLayout<16, true>::kDbl * AttnLayout<16, true>::kDblBytes >= kWvBytes / 2 &&
-                  AttnLayout<16, true>::kRope * AttnLayout<16, true>::kRopeBytes >= 16u * 1024u,
+                  AttnLayout<16, true>::kRope * AttnLayout<16, true>::kRopeBytes + 9u * 16u * 128u >= 16u * 1024u,
               "combine tiles");
 // FUSED o_proj: its stage ring reuses the latent double-block slots
 static_assert(AttnLayout<16, true>::kOp * 2u * kOpBox <= AttnLayout<16, true>::bar_off &&
