@@ -224,6 +224,7 @@ OPROJ_CASES = [
     (3, 1, 12, 4, 300, [300, 129, 5], 128),           # S = 3, K = 1536
     (4, 2, 3, 3, 260, [128, 256, 1, 0], 64),          # q = 2, a token that sees nothing, K = 384
     (40, 2, 2, 3, 200, [200 - 4 * i for i in range(40)], 192),  # S = 80: two 64-token tiles
+    (3, 2, 12, 2, 300, [300, 150, 7], 128),           # 24 query rows: the one-CTA-per-SM instance (N = 32)
 ]
 
 
