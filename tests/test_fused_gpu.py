@@ -303,3 +303,41 @@ def test_fused_oproj_argument_errors(lib):
         m.mla_attn_combine_uv(inp["qv"], inp["kv"], inp["kv_len"], 1, 2, inp["scale"], part_o, part_lse, inp["w_v"],
                               inp["gate"], out, small)
     assert e.value.status == m.MLA_ERR_SHAPE
+
+
+@pytest.mark.parametrize("case", range(16))
+def test_fused_fuzz(lib, orc, case):
+    """Seeded random decode steps through the one-launch path: requests,
+    queries per request, heads (both tilings: up to 16 query rows and more),
+    splits, lengths (empty, one position, tile edges, long), padded output
+    rows, and (every other case) the o_proj shard in the launch.  core against
+    the oracle chain and bit for bit against mla_combine_uv on the launch's own
+    partials; y bit for bit against mla_o_proj on the same core rows."""
+    import mla_decode_attention_lse_gb300 as m
+
+    rng = np.random.default_rng(5000 + case)
+    q = int(rng.choice([1, 1, 2, 3, 4]))
+    H = int(rng.integers(1, 17))
+    B = int(rng.integers(1, 7))
+    spr = int(rng.choice([1, 2, 3, 5, 16, 32]))
+    Lmax = int(rng.choice([16, 64, 65, 129, 300, 700]))
+    lens = [min(int(rng.choice([0, 1, q, 63, 64, 65, int(rng.integers(1, Lmax + 1)), Lmax])), Lmax) for _ in range(B)]
+    S = B * q
+    S_out = S + int(rng.choice([0, 0, 3]))
+    inp = problem(B, q, H, spr, Lmax, lens, seed=700 + case, S_out=S_out)
+    what = f"fuzz {case}: B={B} q={q} H={H} spr={spr} Lmax={Lmax} lens={lens} S_out={S_out}"
+    got, canary, po, pl = run_fused(inp)
+    assert np.all(canary == CANARY), what
+    ref, zero = oracle_chain(orc, inp)
+    compare(got[:S], ref, zero, what)
+    assert np.all(got[S:] == 0), what
+    assert np.array_equal(got, combine_of(inp, po, pl)), what
+    if case % 2:
+        n_out = 64 * int(rng.integers(1, 4))
+        y, ycan, core, w_o = run_fused_oproj(inp, n_out, seed=case)
+        assert np.all(ycan == CANARY), what
+        assert np.array_equal(to_np16(core), got), what
+        y2 = torch.empty((S, n_out), dtype=torch.bfloat16, device="cuda")
+        m.mla_o_proj(core[:S].contiguous(), w_o, y2)
+        torch.cuda.synchronize()
+        assert np.array_equal(y, to_np16(y2)), what
