@@ -98,8 +98,9 @@ struct AttnLayout {
   // barriers: full/empty per double slot, full/empty per rope slot, then
   // s_full, s_free, p_full, o_full, q_full, q_free
   // FUSED adds: item full / empty per ring slot, W_V full, combine MMA done,
-  // then the o_proj stages' full / empty and its accumulator's full
-  static constexpr int kBars = 2 * kDbl + 2 * kRope + 6 + (FUSED ? 2 * kItemRing + 5 + 2 * kOp + 1 : 0);
+  // then the o_proj stages' full / empty, its accumulators' full and a
+  // drain barrier per o_proj MMA thread
+  static constexpr int kBars = 2 * kDbl + 2 * kRope + 6 + (FUSED ? 2 * kItemRing + 5 + 2 * kOp + 3 : 0);
   // misc: [0] TMEM base, [1] abort flag, [2 .. 2 + kItemRing) item ring,
   // [6] the combine unit drawn last
   static constexpr uint32_t misc_off = bar_off + kBars * 8u;
@@ -435,6 +436,12 @@ __device__ __forceinline__ void oproj_phase(const AttnParams &p, const CUtensorM
   auto full = [&](int s) { return obar + 8u * (uint32_t)s; };
   auto empty = [&](int s) { return obar + 8u * (uint32_t)(L::kOp + s); };
   const uint32_t acc_full = obar + 8u * (uint32_t)(2 * L::kOp);
+  auto drain = [&](int w) { return obar + 8u * (uint32_t)(2 * L::kOp + 1 + w); };
+  // two accumulators, D0 (even K blocks, issued by warp 1) and D1 (odd K
+  // blocks, by the query loader's warp, idle here), summed in fp32 by the
+  // epilogue: the arithmetic of the standalone o_proj kernel, so that both
+  // give the same bits, with the MMAs of two threads overlapping
+  constexpr int kW1 = 2 + kAttnSmx;
   auto sA = [&](int s) { return sbase + L::dbl_off + (uint32_t)s * 2u * kOpBox; };
   auto sB = [&](int s) { return sbase + L::dbl_off + (uint32_t)s * 2u * kOpBox + kOpBox; };
 
@@ -445,7 +452,7 @@ __device__ __forceinline__ void oproj_phase(const AttnParams &p, const CUtensorM
   int issued = 0;      // thread 0: stages whose copies went out
   int nu = 0;          // units done
   bool ready = false;  // thread 0: every combine unit has stored
-  int last_mma = -1;   // MMA lane: the last unit whose MMAs it committed
+  bool issued_mma = false;  // MMA lanes: this thread issued o_proj MMAs
   uint32_t unit = misc[6];
   while (!*s_abort && unit != 0xFFFFFFFFu && (int)unit >= base && (int)unit - base < p.op_units) {
     const int u = (int)unit - base, mt = u % MT, nt = u / MT;
@@ -480,10 +487,14 @@ __device__ __forceinline__ void oproj_phase(const AttnParams &p, const CUtensorM
         tma_load_3d(sB(s), &x_map, 64 * kb, nt * 64, 0, full(s));
         issued = g + 1;
       }
-    } else if (warp == 1 && lane == 0) {
+    } else if ((warp == 1 || warp == kW1) && lane == 0) {
       constexpr uint32_t kId = idesc_bf16(64, 64);
+      const int w = warp == 1 ? 0 : 1;
+      const uint32_t d = tmem + (uint32_t)(64 * w);
       bool ok = true;
+      issued_mma = true;
       for (int kb = 0; kb < KB && ok; ++kb, ++g) {
+        if ((kb & 1) != w) continue;
         const int s = g % L::kOp;
         ok = attn_wait(full(s), (uint32_t)(g / L::kOp) & 1u, p.err, s_abort);
         if (!ok) break;
@@ -491,14 +502,11 @@ __device__ __forceinline__ void oproj_phase(const AttnParams &p, const CUtensorM
         const uint32_t dA = (uint32_t)smem_desc_sw128(sA(s)), dB = (uint32_t)smem_desc_sw128(sB(s));
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4)
-          tc_mma_f16(tmem, desc_sw128_at(dA, (uint32_t)k4 * 32u), desc_sw128_at(dB, (uint32_t)k4 * 32u), kId,
-                     (kb | k4) ? 1u : 0u);
+          tc_mma_f16(d, desc_sw128_at(dA, (uint32_t)k4 * 32u), desc_sw128_at(dB, (uint32_t)k4 * 32u), kId,
+                     (kb >= 2 || k4) ? 1u : 0u);
         tc_commit(empty(s));
       }
-      if (ok) {
-        tc_commit(acc_full);
-        last_mma = nu;
-      }
+      if (ok) tc_commit(acc_full);  // with no K block of this parity (K = 64) it arrives at once
     } else if (warp >= 2 && warp < 6) {
       // quadrant warp % 4: rows 16 qd .. 16 qd + 15 of the M = 64 accumulator in lanes 0..15
       const int qd = warp & 3;
@@ -510,15 +518,17 @@ __device__ __forceinline__ void oproj_phase(const AttnParams &p, const CUtensorM
         const int j = mt * 64 + qd * 16 + (lane & 15);
 #pragma unroll 1
         for (int c = 0; c < 64; c += 16) {
-          uint32_t r[16];
+          uint32_t r[16], r1[16];
           tmem_ld_x16(trow + (uint32_t)c, r);
+          if (KB > 1) tmem_ld_x16(trow + 64u + (uint32_t)c, r1);
           tc_wait_ld();
           if (lane < 16) {
 #pragma unroll
             for (int x = 0; x < 16; ++x) {
               const int t = nt * 64 + c + x;
               if (t < S) {
-                const __nv_bfloat16 hv = __float2bfloat16_rn(__uint_as_float(r[x]));
+                const float v = KB > 1 ? __fadd_rn(__uint_as_float(r[x]), __uint_as_float(r1[x])) : __uint_as_float(r[x]);
+                const __nv_bfloat16 hv = __float2bfloat16_rn(v);
                 p.y[(long long)t * p.y_st + j] = *reinterpret_cast<const uint16_t *>(&hv);
               }
             }
@@ -538,7 +548,11 @@ __device__ __forceinline__ void oproj_phase(const AttnParams &p, const CUtensorM
   if (threadIdx.x == 0)
     for (int q = issued - L::kOp < 0 ? 0 : issued - L::kOp; q < issued; ++q)
       mbar_wait(full(q % L::kOp), (uint32_t)(q / L::kOp) & 1u, p.err, kErrWaitTeardown);
-  if (warp == 1 && lane == 0 && last_mma >= 0) mbar_wait(acc_full, (uint32_t)last_mma & 1u, p.err, kErrWaitTeardown);
+  if (issued_mma) {  // every o_proj MMA of this thread completes before TMEM is freed
+    const int w = warp == 1 ? 0 : 1;
+    tc_commit(drain(w));
+    mbar_wait(drain(w), 0u, p.err, kErrWaitTeardown);
+  }
 }
 
 // The last CTA of the fused launch to finish leaves the workspace zeroed for
@@ -597,7 +611,7 @@ __global__ void __launch_bounds__(kAttnThreads, AttnLayout<N, FUSED>::kCtas)
   const uint32_t wv_full = s_full + 48u + 8u * (uint32_t)(2 * kItemRing);
   const uint32_t wv_free = wv_full + 16u;
   const uint32_t cmb_mma = wv_free + 16u;
-  const uint32_t op_bar = cmb_mma + 8u;  // FUSED o_proj: full / empty per stage, accumulator full
+  const uint32_t op_bar = cmb_mma + 8u;  // FUSED o_proj: full / empty per stage, accumulators full, drain[2]
   volatile uint32_t *ring = misc + 2;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -623,7 +637,8 @@ __global__ void __launch_bounds__(kAttnThreads, AttnLayout<N, FUSED>::kCtas)
       }
       for (int b = 0; b < 4; ++b) mbar_init(wv_full + 8u * (uint32_t)b, 1u);  // wv_full[2], wv_free[2]
       mbar_init(cmb_mma, 1u);
-      for (int s = 0; s < 2 * L::kOp + 1; ++s) mbar_init(op_bar + 8u * (uint32_t)s, 1u);
+      for (int s = 0; s < 2 * L::kOp + 3; ++s)  // the accumulators' full: both MMA threads commit
+        mbar_init(op_bar + 8u * (uint32_t)s, s == 2 * L::kOp ? 2u : 1u);
     }
     misc[1] = 0u;
     misc[6] = 0xFFFFFFFFu;

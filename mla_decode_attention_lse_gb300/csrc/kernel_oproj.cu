@@ -11,11 +11,14 @@
 // Work units are (64 output features, NT tokens); a persistent grid of one
 // CTA per SM walks them.  Warp 0 (one lane) brings, per 64-wide K block, the
 // W box [64 rows x 64] and the core box [NT rows x 64] by TMA into a ring of
-// stages; warp 1 (one lane) issues D[j, t] += W x^T as four kind::f16 MMAs
-// of M = 64, N = NT, K = 16 per stage into one of two TMEM accumulators (D row
-// i of an M = 64 MMA sits in TMEM lane 32 (i / 16) + i % 16); warps 2..5
-// read the accumulator (lanes 0..15 of their quadrant), round to bf16 and
-// store out.  The W copies of the first stages go out before the wait for
+// stages; two MMA warps (one lane each) issue D[j, t] += W x^T as four
+// kind::f16 MMAs of M = 64, N = NT, K = 16 per stage -- warp 1 the even K
+// blocks into accumulator D0, warp 6 the odd ones into D1 (one thread issues
+// an MMA about every 55 cycles whatever its size at these N, and two threads'
+// MMAs overlap) -- with D0 / D1 double-buffered over units where TMEM allows
+// (D row i of an M = 64 MMA sits in TMEM lane 32 (i / 16) + i % 16); warps
+// 2..5 read both (lanes 0..15 of their quadrant), add them in fp32
+// (D = D0 + D1), round to bf16 and store out.  The W copies of the first stages go out before the wait for
 // the previous kernel (a weight no earlier kernel writes); the core rows and
 // every store come after it.  Every wait is bounded.
 #include <cuda.h>
@@ -31,18 +34,22 @@ namespace mla {
 namespace {
 
 constexpr int kOpM = 64;       // output features per unit (MMA M)
-constexpr int kOpThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kOpThreads = 224;  // warp 0 TMA, warps 1 and 6 MMA, warps 2..5 epilogue
 constexpr uint32_t kOpABytes = kOpM * 128u;  // a W box: 64 rows x 128 B
 
 template <int NT>
 struct OpLayout {
   static constexpr uint32_t stage = kOpABytes + (uint32_t)NT * 128u;
   static constexpr int kStages = (NT == 64) ? 12 : (NT == 128) ? 8 : 5;
-  static constexpr uint32_t bar_off = kStages * stage;  // full[ST], empty[ST], acc_full[2], acc_empty[2]
-  static constexpr uint32_t misc_off = bar_off + (2 * kStages + 4) * 8u;
+  // full[ST], empty[ST], acc_full[2], acc_empty[2], drain[2] (one per MMA warp)
+  static constexpr uint32_t bar_off = kStages * stage;
+  static constexpr uint32_t misc_off = bar_off + (2 * kStages + 6) * 8u;
   static constexpr uint32_t total = misc_off + 16u;
-  static constexpr uint32_t tmem_cols = 2u * NT < 32u ? 32u : 2u * NT;
+  static constexpr int kBufs = NT <= 128 ? 2 : 1;  // accumulator pairs (D0, D1) in TMEM
+  static constexpr uint32_t tmem_cols = (uint32_t)(kBufs * 2 * NT);
 };
+static_assert(OpLayout<64>::tmem_cols == 256 && OpLayout<128>::tmem_cols == 512 && OpLayout<256>::tmem_cols == 512,
+              "TMEM columns");
 static_assert(OpLayout<64>::total + 1024 <= 227u * 1024u, "shared memory (NT = 64)");
 static_assert(OpLayout<128>::total + 1024 <= 227u * 1024u, "shared memory (NT = 128)");
 static_assert(OpLayout<256>::total + 1024 <= 227u * 1024u, "shared memory (NT = 256)");
@@ -80,6 +87,10 @@ __global__ void __launch_bounds__(kOpThreads, 1)
   auto empty = [&](int s) { return bar0 + 8u * (uint32_t)(ST + s); };
   auto acc_full = [&](int b) { return bar0 + 8u * (uint32_t)(2 * ST + b); };
   auto acc_empty = [&](int b) { return bar0 + 8u * (uint32_t)(2 * ST + 2 + b); };
+  auto drain = [&](int w) { return bar0 + 8u * (uint32_t)(2 * ST + 4 + w); };
+  constexpr int NB = L::kBufs;
+  // accumulator Dw (w = 0: even K blocks, 1: odd) of buffer b
+  auto acc = [&](uint32_t tmem, int b, int w) { return tmem + (uint32_t)((2 * b + w) * NT); };
   auto sA = [&](int s) { return sbase + (uint32_t)s * L::stage; };
   auto sB = [&](int s) { return sbase + (uint32_t)s * L::stage + kOpABytes; };
 
@@ -90,8 +101,9 @@ __global__ void __launch_bounds__(kOpThreads, 1)
       mbar_init(empty(s), 1u);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(acc_full(b), 1u);
+      mbar_init(acc_full(b), 2u);  // both MMA warps commit
       mbar_init(acc_empty(b), 4u);
+      mbar_init(drain(b), 1u);
     }
     misc[1] = 0u;
     fence_mbar_init();
@@ -144,19 +156,22 @@ __global__ void __launch_bounds__(kOpThreads, 1)
       for (int q = issued - ST < 0 ? 0 : issued - ST; q < issued; ++q)
         mbar_wait(full(q % ST), (uint32_t)(q / ST) & 1u, p.err, kErrWaitTeardown);
     }
-  } else if (warp == 1) {
-    // ---- MMA issuer: D[j, t] += W[j, k] x[t, k], two accumulators ----
+  } else if (warp == 1 || warp == 6) {
+    // ---- MMA issuers: Dw[j, t] += W[j, k] x[t, k] over the K blocks of
+    // parity w; both commit a unit's acc_full ----
     if (lane == 0) {
       constexpr uint32_t kId = idesc_bf16(kOpM, NT);
+      const int w = warp == 1 ? 0 : 1;
       bool ok = true;
-      int g = 0, i = 0, last0 = -1, last1 = -1;
+      int g = 0, i = 0;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++i) {
-        const int b = i & 1;
-        if (i >= 2) ok = op_wait(acc_empty(b), (uint32_t)((i >> 1) - 1) & 1u, p.err, s_abort);
+        const int b = i % NB;
+        if (i >= NB) ok = op_wait(acc_empty(b), (uint32_t)(i / NB - 1) & 1u, p.err, s_abort);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(b * NT);
+        const uint32_t d = acc(tmem, b, w);
         for (int kb = 0; kb < KB; ++kb, ++g) {
+          if ((kb & 1) != w) continue;
           const int s = g % ST;
           ok = op_wait(full(s), (uint32_t)(g / ST) & 1u, p.err, s_abort);
           if (!ok) break;
@@ -165,19 +180,16 @@ __global__ void __launch_bounds__(kOpThreads, 1)
 #pragma unroll
           for (int k4 = 0; k4 < 4; ++k4)
             tc_mma_f16(d, desc_sw128_at(dA, (uint32_t)k4 * 32u), desc_sw128_at(dB, (uint32_t)k4 * 32u), kId,
-                       (kb | k4) ? 1u : 0u);
+                       (kb >= 2 || k4) ? 1u : 0u);
           tc_commit(empty(s));
         }
         if (!ok) break;
-        tc_commit(acc_full(b));
-        if (b == 0)
-          last0 = i;
-        else
-          last1 = i;
+        tc_commit(acc_full(b));  // with no K block of this parity (K = 64) it arrives at once
       }
-      // after an abort: the committed MMAs finish before TMEM is freed
-      if (last0 >= 0) mbar_wait(acc_full(0), (uint32_t)(last0 >> 1) & 1u, p.err, kErrWaitTeardown);
-      if (last1 >= 0) mbar_wait(acc_full(1), (uint32_t)(last1 >> 1) & 1u, p.err, kErrWaitTeardown);
+      // every MMA this thread issued completes before TMEM is freed (after an
+      // abort too)
+      tc_commit(drain(w));
+      mbar_wait(drain(w), 0u, p.err, kErrWaitTeardown);
     }
   } else {
     // ---- epilogue warps 2..5: quadrant warp % 4; an M = 64 accumulator has
@@ -188,23 +200,25 @@ __global__ void __launch_bounds__(kOpThreads, 1)
     grid_dependency_wait();  // out may still be read by the kernel before
     int i = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++i) {
-      const int b = i & 1, mt = u % MT, nt = u / MT;
-      bool ok = op_wait(acc_full(b), (uint32_t)(i >> 1) & 1u, p.err, s_abort);
+      const int b = i % NB, mt = u % MT, nt = u / MT;
+      bool ok = op_wait(acc_full(b), (uint32_t)(i / NB) & 1u, p.err, s_abort);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       const int j = mt * kOpM + qd * 16 + (lane & 15);
 #pragma unroll 1
       for (int c = 0; c < NT; c += 16) {
-        uint32_t r[16];
-        tmem_ld_x16(trow + (uint32_t)(b * NT + c), r);
+        uint32_t r[16], r1[16];
+        tmem_ld_x16(acc(trow, b, 0) + (uint32_t)c, r);
+        if (KB > 1) tmem_ld_x16(acc(trow, b, 1) + (uint32_t)c, r1);
         tc_wait_ld();
         if (act) {
 #pragma unroll
           for (int x = 0; x < 16; ++x) {
             const int t = nt * NT + c + x;
             if (t < p.S) {
-              const __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(r[x]));
+              const float v = KB > 1 ? __fadd_rn(__uint_as_float(r[x]), __uint_as_float(r1[x])) : __uint_as_float(r[x]);
+              const __nv_bfloat16 h = __float2bfloat16_rn(v);
               p.out[(long long)t * p.out_st + j] = *reinterpret_cast<const uint16_t *>(&h);
             }
           }
