@@ -62,11 +62,12 @@ namespace {
 
 constexpr int kAttnK = kD + 64;     // query / cached row width (576)
 constexpr int kAttnSmx = 8;         // softmax warps: two per TMEM lane quadrant, half the query rows each
-constexpr int kAttnThreads = (3 + kAttnSmx) * 32;  // warp 0 TMA, warp 1 MMA, softmax warps, one query warp
+// warp 0 TMA, warp 1 MMAs, softmax warps 2 .. 1 + kAttnSmx, one query warp,
+// and (AttnLayout::kSplitMma) one more warp for the O^T MMAs
+constexpr int kPvWarp = 3 + kAttnSmx;
 constexpr uint32_t kWvBytes = 128u * 1024u;  // FUSED: W_V[h], [128 x 512] bf16
 
 constexpr int kItemRing = 4;        // FUSED: items handed from the TMA lane to the other roles
-constexpr int kItemTakers = 2 + kAttnSmx;  // MMA lane, query warp, softmax warps
 constexpr int kCmbTile = 8;         // FUSED: tokens per combine unit (one merging warp each)
 constexpr uint32_t kOpBox = 64u * 128u;  // 64 rows x 64 bf16, 128-byte swizzle
 
@@ -80,6 +81,14 @@ constexpr uint32_t kOpBox = 64u * 128u;  // 64 rows x 64 bf16, 128-byte swizzle
 template <int N, bool FUSED = false>
 struct AttnLayout {
   static constexpr int kCtas = (N == 16) ? 2 : 1;             // CTAs per SM
+  // The S^T and the O^T MMAs from two threads (one thread issues an MMA about
+  // every 55 cycles at these N whatever its size, and the MMAs of two threads
+  // overlap): S^T of the next tile then goes out while the softmax and the
+  // O^T MMAs of this one run.  Not in the fused step: its 12th warp would cap
+  // two CTAs per SM at 80 registers, and the launch measured slower.
+  static constexpr bool kSplitMma = !FUSED;
+  static constexpr int kThreads = ((kSplitMma ? 4 : 3) + kAttnSmx) * 32;
+  static constexpr int kItemTakers = (kSplitMma ? 3 : 2) + kAttnSmx;  // FUSED: MMA lane(s), query warp, softmax warps
   static constexpr int kTile = kCtas == 2 ? 64 : 128;          // positions per tile (MMA M of S^T)
   static constexpr uint32_t kDblBytes = 2u * kTile * 128u;     // latents 128 c .. 128 c + 127 of a tile
   static constexpr uint32_t kRopeBytes = kTile * 128u;         // the tile's rope block
@@ -99,8 +108,9 @@ struct AttnLayout {
   // s_full, s_free, p_full, o_full, q_full, q_free
   // FUSED adds: item full / empty per ring slot, W_V full, combine MMA done,
   // then the o_proj stages' full / empty, its accumulators' full and a
-  // drain barrier per o_proj MMA thread
-  static constexpr int kBars = 2 * kDbl + 2 * kRope + 6 + (FUSED ? 2 * kItemRing + 5 + 2 * kOp + 3 : 0);
+  // drain barrier per o_proj MMA thread; last, a drain barrier per attention
+  // MMA thread (S^T, O^T)
+  static constexpr int kBars = 2 * kDbl + 2 * kRope + 6 + (FUSED ? 2 * kItemRing + 5 + 2 * kOp + 3 : 0) + 2;
   // misc: [0] TMEM base, [1] abort flag, [2 .. 2 + kItemRing) item ring,
   // [6] the combine unit drawn last
   static constexpr uint32_t misc_off = bar_off + kBars * 8u;
@@ -574,7 +584,7 @@ __device__ __forceinline__ void finish_workspace(const AttnParams &p) {
 }  // namespace
 
 template <int N, bool FUSED>
-__global__ void __launch_bounds__(kAttnThreads, AttnLayout<N, FUSED>::kCtas)
+__global__ void __launch_bounds__(AttnLayout<N, FUSED>::kThreads, AttnLayout<N, FUSED>::kCtas)
     attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap kv_map,
                 const __grid_constant__ CUtensorMap wv_map, const __grid_constant__ CUtensorMap wo_map,
                 const __grid_constant__ CUtensorMap x_map) {
@@ -603,6 +613,8 @@ __global__ void __launch_bounds__(kAttnThreads, AttnLayout<N, FUSED>::kCtas)
   const uint32_t o_full = s_full + 24u;  // a tile's O^T MMAs are complete
   const uint32_t q_full = s_full + 32u;  // an item's query rows are in shared memory
   const uint32_t q_free = s_full + 40u;  // the item's last S^T MMAs are done: Q may be replaced
+  // every MMA of the S^T / O^T thread is complete (its teardown, once)
+  const uint32_t drain_s = bar0 + 8u * (uint32_t)(L::kBars - 2), drain_pv = drain_s + 8u;
   // FUSED: item ring slots (full: published by the TMA lane; empty: every
   // taker has read it), W_V of a combine unit in shared memory, its MMAs done
   auto item_full = [&](int s) { return s_full + 48u + 8u * (uint32_t)s; };
@@ -630,10 +642,12 @@ __global__ void __launch_bounds__(kAttnThreads, AttnLayout<N, FUSED>::kCtas)
     mbar_init(o_full, 1u);
     mbar_init(q_full, 1u);
     mbar_init(q_free, 1u);
+    mbar_init(drain_s, 1u);
+    mbar_init(drain_pv, 1u);
     if constexpr (FUSED) {
       for (int s = 0; s < kItemRing; ++s) {
         mbar_init(item_full(s), 1u);
-        mbar_init(item_empty(s), (uint32_t)kItemTakers);
+        mbar_init(item_empty(s), (uint32_t)L::kItemTakers);
       }
       for (int b = 0; b < 4; ++b) mbar_init(wv_full + 8u * (uint32_t)b, 1u);  // wv_full[2], wv_free[2]
       mbar_init(cmb_mma, 1u);
@@ -755,83 +769,101 @@ __global__ void __launch_bounds__(kAttnThreads, AttnLayout<N, FUSED>::kCtas)
       for (int t = issued_r - NR < 0 ? 0 : issued_r - NR; t < issued_r; ++t)
         mbar_wait(full_r(t % NR), (uint32_t)(t / NR) & 1u, p.err, kErrWaitTeardown);
     }
-  } else if (warp == 1) {
-    // ---- MMA issuer ----
+  } else if (warp == 1 || (L::kSplitMma && warp == kPvWarp)) {
+    // ---- MMA issuers: warp 1 the S^T MMAs (and, one thread for both, the
+    // O^T MMAs), warp kPvWarp the O^T MMAs when they have a thread of their
+    // own ----
     if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_bf16(kAttnTile, N);  // M = the tile's positions
+      constexpr uint32_t kIdS = idesc_bf16(kAttnTile, N);         // M = the tile's positions
       constexpr uint32_t kIdO = idesc_bf16(128, N) | (1u << 15);  // A = V^T, MN-major
       const uint32_t tS = tmem, tO = tmem + (uint32_t)N;
       const uint32_t dQ = (uint32_t)smem_desc_sw128(sbase + L::q_off);
       const uint32_t dP = (uint32_t)smem_desc_sw128(sbase + L::p_off);
-      int last_s = -1, last_o = -1, last_q = -1;  // last committed S^T / O^T tile, Q release
+      // S^T[j, m] = sum_k K[j][k] Q[m][k] of tile T (the t-th of item I)
+      auto s_tile = [&](int T, int t, int ntiles) -> bool {
+        if (T > 0 && !attn_wait(s_free, (uint32_t)(T - 1) & 1u, p.err, s_abort)) return false;
+        // the four latent double blocks ...
+        for (int c = 0; c < 4; ++c) {
+          const int gb = 4 * T + c, s = gb % kAttnDbl;
+          if (!attn_wait(full_db(s), (uint32_t)(gb / kAttnDbl) & 1u, p.err, s_abort)) return false;
+          tc_fence_after();
+          const uint32_t dK = (uint32_t)smem_desc_sw128(sbase + L::dbl_off + (uint32_t)s * kDblBytes);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t box = (uint32_t)kk >> 2, k4 = (uint32_t)kk & 3u;
+            tc_mma_f16(tS, desc_sw128_at(dK, box * (kDblBytes / 2) + k4 * 32u),
+                       desc_sw128_at(dQ, (2u * c + box) * (N * 128u) + k4 * 32u), kIdS, (c | kk) ? 1u : 0u);
+          }
+        }
+        // ... and the rope block
+        const int sr = T % NR;
+        if (!attn_wait(full_r(sr), (uint32_t)(T / NR) & 1u, p.err, s_abort)) return false;
+        tc_fence_after();
+        const uint32_t dR = (uint32_t)smem_desc_sw128(sbase + L::rope_off + (uint32_t)sr * kRopeBytes);
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4)
+          tc_mma_f16(tS, desc_sw128_at(dR, (uint32_t)k4 * 32u),
+                     desc_sw128_at(dQ, 8u * (N * 128u) + (uint32_t)k4 * 32u), kIdS, 1u);
+        tc_commit(s_full);
+        tc_commit(empty_r(sr));
+        if (t == ntiles - 1) tc_commit(q_free);  // the next item's queries may replace these
+        return true;
+      };
+      // O^T[d, m] += sum_j V^T[d][j] P^T[j, m] of tile T, once P(T) is
+      // written and O rescaled (which also orders it after the previous
+      // item's epilogue).  The double-block slots it frees were read by the
+      // tile's S^T MMAs too, which completed before the softmax wrote P(T).
+      auto pv_tile = [&](int T, int t) -> bool {
+        if (!attn_wait(p_full, (uint32_t)T & 1u, p.err, s_abort)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t vbase = sbase + L::dbl_off + (uint32_t)((4 * T + c) % kAttnDbl) * kDblBytes;
+#pragma unroll
+          for (int ks = 0; ks < kAttnTile / 16; ++ks)  // 16 positions per step
+            tc_mma_f16(tO + (uint32_t)(c * N), smem_desc_mn_sw128(vbase + (uint32_t)ks * 2048u, kDblBytes / 2),
+                       desc_sw128_at(dP, ((uint32_t)ks >> 2) * (N * 128u) + ((uint32_t)ks & 3u) * 32u), kIdO,
+                       (t | ks) ? 1u : 0u);
+          tc_commit(empty_db((4 * T + c) % kAttnDbl));  // this latent chunk's slot is free once its MMAs are
+        }
+        tc_commit(o_full);
+        return true;
+      };
       bool ok = true;
       int T = 0, kq = 0;  // tiles, non-empty items
-      for (int k = 0; ok; ++k) {
-        const int it = take(k, ok);
-        if (!ok) break;
-        release(k);
-        if (it >= nitems) break;
-        const Item I = item_of(it);
-        if (I.ntiles == 0) continue;
-        ok = attn_wait(q_full, (uint32_t)kq & 1u, p.err, s_abort);
-        for (int t = 0; t < I.ntiles && ok; ++t, ++T) {
-          if (T > 0) ok = attn_wait(s_free, (uint32_t)(T - 1) & 1u, p.err, s_abort);
-          // S^T[j, m] = sum_k K[j][k] Q[m][k]: the four latent double blocks ...
-          for (int c = 0; c < 4 && ok; ++c) {
-            const int gb = 4 * T + c, s = gb % kAttnDbl;
-            ok = attn_wait(full_db(s), (uint32_t)(gb / kAttnDbl) & 1u, p.err, s_abort);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t dK = (uint32_t)smem_desc_sw128(sbase + L::dbl_off + (uint32_t)s * kDblBytes);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t box = (uint32_t)kk >> 2, k4 = (uint32_t)kk & 3u;
-              tc_mma_f16(tS, desc_sw128_at(dK, box * (kDblBytes / 2) + k4 * 32u),
-                         desc_sw128_at(dQ, (2u * c + box) * (N * 128u) + k4 * 32u), kIdS, (c | kk) ? 1u : 0u);
+      if (!L::kSplitMma || warp == 1) {
+        for (int k = 0; ok; ++k) {
+          const int it = take(k, ok);
+          if (!ok) break;
+          release(k);
+          if (it >= nitems) break;
+          const Item I = item_of(it);
+          if (I.ntiles == 0) continue;
+          ok = attn_wait(q_full, (uint32_t)kq & 1u, p.err, s_abort);
+          for (int t = 0; t < I.ntiles && ok; ++t, ++T) {
+            ok = s_tile(T, t, I.ntiles);
+            if constexpr (!L::kSplitMma) {
+              if (ok) ok = pv_tile(T, t);
             }
           }
-          if (!ok) break;
-          // ... and the rope block
-          const int sr = T % NR;
-          ok = attn_wait(full_r(sr), (uint32_t)(T / NR) & 1u, p.err, s_abort);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t dR = (uint32_t)smem_desc_sw128(sbase + L::rope_off + (uint32_t)sr * kRopeBytes);
-#pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4)
-            tc_mma_f16(tS, desc_sw128_at(dR, (uint32_t)k4 * 32u),
-                       desc_sw128_at(dQ, 8u * (N * 128u) + (uint32_t)k4 * 32u), kIdS, 1u);
-          tc_commit(s_full);
-          tc_commit(empty_r(sr));
-          last_s = T;
-          if (t == I.ntiles - 1) {
-            tc_commit(q_free);  // the next item's queries may replace these
-            last_q = kq;
-          }
-          // O^T[d, m] += sum_j V^T[d][j] P^T[j, m], once P(t) is written and O
-          // rescaled (which also orders it after the previous item's epilogue)
-          ok = attn_wait(p_full, (uint32_t)T & 1u, p.err, s_abort);
-          if (!ok) break;
-          tc_fence_after();
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint32_t vbase = sbase + L::dbl_off + (uint32_t)((4 * T + c) % kAttnDbl) * kDblBytes;
-#pragma unroll
-            for (int ks = 0; ks < kAttnTile / 16; ++ks)  // 16 positions per step
-              tc_mma_f16(tO + (uint32_t)(c * N), smem_desc_mn_sw128(vbase + (uint32_t)ks * 2048u, kDblBytes / 2),
-                         desc_sw128_at(dP, ((uint32_t)ks >> 2) * (N * 128u) + ((uint32_t)ks & 3u) * 32u), kIdO,
-                         (t | ks) ? 1u : 0u);
-            tc_commit(empty_db((4 * T + c) % kAttnDbl));  // this latent chunk's slot is free once its MMAs are
-          }
-          tc_commit(o_full);
-          last_o = T;
+          ++kq;
         }
-        ++kq;
+        // every MMA this thread issued completes before TMEM is freed (after
+        // an abort too)
+        tc_commit(drain_s);
+        mbar_wait(drain_s, 0u, p.err, kErrWaitTeardown);
+      } else {
+        for (int k = 0; ok; ++k) {
+          const int it = take(k, ok);
+          if (!ok) break;
+          release(k);
+          if (it >= nitems) break;
+          const Item I = item_of(it);
+          for (int t = 0; t < I.ntiles && ok; ++t, ++T) ok = pv_tile(T, t);
+        }
+        tc_commit(drain_pv);
+        mbar_wait(drain_pv, 0u, p.err, kErrWaitTeardown);
       }
-      // after an abort: the committed MMAs finish before TMEM is freed
-      if (last_s >= 0) mbar_wait(s_full, (uint32_t)last_s & 1u, p.err, kErrWaitTeardown);
-      if (last_o >= 0) mbar_wait(o_full, (uint32_t)last_o & 1u, p.err, kErrWaitTeardown);
-      if (last_q >= 0) mbar_wait(q_free, (uint32_t)last_q & 1u, p.err, kErrWaitTeardown);
     }
   } else if (warp == 2 + kAttnSmx) {
     // ---- query loader: an item's N rows (row m: token m / G, head g G + m % G;
@@ -1171,7 +1203,7 @@ static cudaError_t launch_attn_n(const AttnParams &p, const CUtensorMap &map, co
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(kAttnThreads, 1, 1);
+  cfg.blockDim = dim3(AttnLayout<N, FUSED>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
