@@ -130,10 +130,13 @@ static_assert(4 * AttnLayout<32, true>::kDblBytes == kWvBytes && AttnLayout<32, 
                   AttnLayout<16, true>::kDbl * AttnLayout<16, true>::kDblBytes >= kWvBytes / 2 &&
                   AttnLayout<16, true>::kRope * AttnLayout<16, true>::kRopeBytes + 9u * 16u * 128u >= 16u * 1024u,
               "combine tiles");
-// FUSED o_proj: its stage ring reuses the latent double-block slots
-static_assert(AttnLayout<16, true>::kOp * 2u * kOpBox <= AttnLayout<16, true>::bar_off &&
-                  AttnLayout<32, true>::kOp * 2u * kOpBox <= AttnLayout<32, true>::bar_off,
-              "o_proj stages");
+// FUSED o_proj: its stage ring reuses the latent double-block slots, its
+// output tile [64 tokens x 64 features] bf16 is staged right after the ring
+template <int N>
+constexpr uint32_t kOpStgOff = AttnLayout<N, true>::kOp * 2u * kOpBox;
+static_assert(kOpStgOff<16> + 64u * 128u <= AttnLayout<16, true>::bar_off &&
+                  kOpStgOff<32> + 64u * 128u <= AttnLayout<32, true>::bar_off,
+              "o_proj stages and output tile");
 
 // Bounded wait on an mbarrier phase, shared abort flag (as the combine kernels).
 __device__ __forceinline__ bool attn_wait(uint32_t bar, uint32_t parity, int *err, volatile int *abort_flag) {
@@ -436,8 +439,8 @@ __device__ __forceinline__ void combine_phase(const AttnParams &p, const CUtenso
 // reads with a proxy fence.
 template <int N>
 __device__ __forceinline__ void oproj_phase(const AttnParams &p, const CUtensorMap &wo_map, const CUtensorMap &x_map,
-                                            uint32_t sbase, uint32_t tmem, uint32_t *misc, volatile int *s_abort,
-                                            uint32_t obar) {
+                                            uint32_t sbase, uint8_t *gbase, uint32_t tmem, uint32_t *misc,
+                                            volatile int *s_abort, uint32_t obar) {
   using L = AttnLayout<N, true>;
   constexpr unsigned kFull = 0xffffffffu;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -518,31 +521,47 @@ __device__ __forceinline__ void oproj_phase(const AttnParams &p, const CUtensorM
       }
       if (ok) tc_commit(acc_full);  // with no K block of this parity (K = 64) it arrives at once
     } else if (warp >= 2 && warp < 6) {
-      // quadrant warp % 4: rows 16 qd .. 16 qd + 15 of the M = 64 accumulator in lanes 0..15
-      const int qd = warp & 3;
+      // quadrant warp % 4: rows 16 qd .. 16 qd + 15 of the M = 64 accumulator
+      // in lanes 0..15; D0 + D1 rounded to bf16 into a staging tile in shared
+      // memory, then copied out row by row with coalesced stores (per-element
+      // stores from the accumulator's layout cost ~2 us per unit)
+      const int qd = warp & 3, et = threadIdx.x - 64;  // et: 0 .. 127
       bool ok = attn_wait(acc_full, (uint32_t)nu & 1u, p.err, s_abort);
-      ok = __all_sync(kFull, ok);
+      ok = named_barrier_and(2, 128, ok);  // the four warps decide together
       if (ok) {
         tc_fence_after();
         const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);
-        const int j = mt * 64 + qd * 16 + (lane & 15);
+        uint16_t *stg = reinterpret_cast<uint16_t *>(gbase + kOpStgOff<N>);  // [64][64]
 #pragma unroll 1
         for (int c = 0; c < 64; c += 16) {
           uint32_t r[16], r1[16];
           tmem_ld_x16(trow + (uint32_t)c, r);
           if (KB > 1) tmem_ld_x16(trow + 64u + (uint32_t)c, r1);
           tc_wait_ld();
-          if (lane < 16) {
+          // lanes l and l + 16 write the even and odd tokens of feature 16 qd + l
+          uint16_t *srow = stg + (c + (lane >> 4)) * 64 + qd * 16 + (lane & 15);
 #pragma unroll
-            for (int x = 0; x < 16; ++x) {
-              const int t = nt * 64 + c + x;
-              if (t < S) {
-                const float v = KB > 1 ? __fadd_rn(__uint_as_float(r[x]), __uint_as_float(r1[x])) : __uint_as_float(r[x]);
-                const __nv_bfloat16 hv = __float2bfloat16_rn(v);
-                p.y[(long long)t * p.y_st + j] = *reinterpret_cast<const uint16_t *>(&hv);
-              }
-            }
+          for (int x = 0; x < 16; x += 2) {
+            const float e =
+                KB > 1 ? __fadd_rn(__uint_as_float(r[x]), __uint_as_float(r1[x])) : __uint_as_float(r[x]);
+            const float o =
+                KB > 1 ? __fadd_rn(__uint_as_float(r[x + 1]), __uint_as_float(r1[x + 1])) : __uint_as_float(r[x + 1]);
+            const float o_hi = __shfl_xor_sync(kFull, o, 16);
+            const __nv_bfloat16 hv = __float2bfloat16_rn(lane < 16 ? e : o_hi);
+            srow[x * 64] = *reinterpret_cast<const uint16_t *>(&hv);
           }
+        }
+        named_barrier(2, 128);  // the tile is staged
+        const int rows = min(64, S - nt * 64);
+        uint16_t *ybase = p.y + (long long)nt * 64 * p.y_st + mt * 64;
+        if ((reinterpret_cast<uintptr_t>(p.y) & 15u) == 0 && (p.y_st & 7) == 0) {
+          for (int ch = et; ch < rows * 8; ch += 128) {
+            const int row = ch >> 3, c16 = ch & 7;
+            *reinterpret_cast<uint4 *>(ybase + (long long)row * p.y_st + c16 * 8) =
+                *reinterpret_cast<const uint4 *>(stg + row * 64 + c16 * 8);
+          }
+        } else {
+          for (int e = et; e < rows * 64; e += 128) ybase[(long long)(e >> 6) * p.y_st + (e & 63)] = stg[e];
         }
       }
     }
@@ -1172,7 +1191,7 @@ __global__ void __launch_bounds__(AttnLayout<N, FUSED>::kThreads, AttnLayout<N, 
   }
   if constexpr (FUSED) {
     combine_phase<N>(p, wv_map, sbase, gbase, tmem, misc, s_abort, wv_full, wv_free, cmb_mma, nitems);
-    if (p.n_out > 0) oproj_phase<N>(p, wo_map, x_map, sbase, tmem, misc, s_abort, op_bar);
+    if (p.n_out > 0) oproj_phase<N>(p, wo_map, x_map, sbase, gbase, tmem, misc, s_abort, op_bar);
     finish_workspace(p);
   }
   tc_fence_before();

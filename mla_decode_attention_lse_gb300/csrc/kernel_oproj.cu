@@ -18,7 +18,9 @@
 // MMAs overlap) -- with D0 / D1 double-buffered over units where TMEM allows
 // (D row i of an M = 64 MMA sits in TMEM lane 32 (i / 16) + i % 16); warps
 // 2..5 read both (lanes 0..15 of their quadrant), add them in fp32
-// (D = D0 + D1), round to bf16 and store out.  The W copies of the first stages go out before the wait for
+// (D = D0 + D1), round to bf16 into a staging tile in shared memory, and copy
+// the tile out row by row with coalesced 16-byte stores (per-element stores
+// straight from the accumulator's layout took ~2.2 us per unit).  The W copies of the first stages go out before the wait for
 // the previous kernel (a weight no earlier kernel writes); the core rows and
 // every store come after it.  Every wait is bounded.
 #include <cuda.h>
@@ -40,9 +42,11 @@ constexpr uint32_t kOpABytes = kOpM * 128u;  // a W box: 64 rows x 128 B
 template <int NT>
 struct OpLayout {
   static constexpr uint32_t stage = kOpABytes + (uint32_t)NT * 128u;
-  static constexpr int kStages = (NT == 64) ? 12 : (NT == 128) ? 8 : 5;
+  static constexpr int kStages = (NT == 64) ? 12 : (NT == 128) ? 8 : 4;
+  // the output tile [NT tokens x 64 features] bf16, staged for the copy out
+  static constexpr uint32_t stg_off = kStages * stage;
   // full[ST], empty[ST], acc_full[2], acc_empty[2], drain[2] (one per MMA warp)
-  static constexpr uint32_t bar_off = kStages * stage;
+  static constexpr uint32_t bar_off = stg_off + (uint32_t)NT * 128u;
   static constexpr uint32_t misc_off = bar_off + (2 * kStages + 6) * 8u;
   static constexpr uint32_t total = misc_off + 16u;
   static constexpr int kBufs = NT <= 128 ? 2 : 1;  // accumulator pairs (D0, D1) in TMEM
@@ -194,39 +198,57 @@ __global__ void __launch_bounds__(kOpThreads, 1)
   } else {
     // ---- epilogue warps 2..5: quadrant warp % 4; an M = 64 accumulator has
     // row 16 q + l in lane l < 16 of quadrant q ----
-    const int qd = warp & 3;
-    const bool act = lane < 16;
+    const int qd = warp & 3, et = threadIdx.x - 64;  // et: 0 .. 127
     const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);
+    uint16_t *stg = reinterpret_cast<uint16_t *>(gbase + L::stg_off);  // [NT][64]
+    // 16-byte stores when every row of out starts on a 16-byte boundary
+    const bool vec = (reinterpret_cast<uintptr_t>(p.out) & 15u) == 0 && (p.out_st & 7) == 0;
     grid_dependency_wait();  // out may still be read by the kernel before
     int i = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++i) {
       const int b = i % NB, mt = u % MT, nt = u / MT;
       bool ok = op_wait(acc_full(b), (uint32_t)(i / NB) & 1u, p.err, s_abort);
-      ok = __all_sync(0xffffffffu, ok);
+      // the four warps take the exit decision together (a warp that left
+      // would leave the others at the staging barriers)
+      ok = named_barrier_and(1, 128, ok);
       if (!ok) break;
       tc_fence_after();
-      const int j = mt * kOpM + qd * 16 + (lane & 15);
 #pragma unroll 1
       for (int c = 0; c < NT; c += 16) {
         uint32_t r[16], r1[16];
         tmem_ld_x16(acc(trow, b, 0) + (uint32_t)c, r);
         if (KB > 1) tmem_ld_x16(acc(trow, b, 1) + (uint32_t)c, r1);
         tc_wait_ld();
-        if (act) {
+        // lane l < 16 holds feature 16 qd + l for tokens c .. c + 15; lanes l
+        // and l + 16 write its even and odd tokens (the odd values by one
+        // shuffle), so the whole warp stores
+        uint16_t *srow = stg + (c + (lane >> 4)) * 64 + qd * 16 + (lane & 15);
 #pragma unroll
-          for (int x = 0; x < 16; ++x) {
-            const int t = nt * NT + c + x;
-            if (t < p.S) {
-              const float v = KB > 1 ? __fadd_rn(__uint_as_float(r[x]), __uint_as_float(r1[x])) : __uint_as_float(r[x]);
-              const __nv_bfloat16 h = __float2bfloat16_rn(v);
-              p.out[(long long)t * p.out_st + j] = *reinterpret_cast<const uint16_t *>(&h);
-            }
-          }
+        for (int x = 0; x < 16; x += 2) {
+          const float e = KB > 1 ? __fadd_rn(__uint_as_float(r[x]), __uint_as_float(r1[x])) : __uint_as_float(r[x]);
+          const float o =
+              KB > 1 ? __fadd_rn(__uint_as_float(r[x + 1]), __uint_as_float(r1[x + 1])) : __uint_as_float(r[x + 1]);
+          const float o_hi = __shfl_xor_sync(0xffffffffu, o, 16);
+          const __nv_bfloat16 h = __float2bfloat16_rn(lane < 16 ? e : o_hi);
+          srow[x * 64] = *reinterpret_cast<const uint16_t *>(&h);
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty(b));
+      named_barrier(1, 128);  // the tile is staged
+      const int rows = min(NT, p.S - nt * NT);
+      uint16_t *obase = p.out + (long long)nt * NT * p.out_st + mt * kOpM;
+      if (vec) {
+        for (int ch = et; ch < rows * 8; ch += 128) {
+          const int row = ch >> 3, c16 = ch & 7;
+          *reinterpret_cast<uint4 *>(obase + (long long)row * p.out_st + c16 * 8) =
+              *reinterpret_cast<const uint4 *>(stg + row * 64 + c16 * 8);
+        }
+      } else {
+        for (int e = et; e < rows * 64; e += 128) obase[(long long)(e >> 6) * p.out_st + (e & 63)] = stg[e];
+      }
+      named_barrier(1, 128);  // the staging tile may be written again
     }
   }
   tc_fence_before();
