@@ -195,9 +195,10 @@ def test_fused_empty_batch_and_errors(lib):
     assert e.value.status == m.MLA_ERR_SHAPE
 
 
-def run_fused_oproj(inp, n_out, seed=5, ws=None):
+def run_fused_oproj(inp, n_out, seed=5, ws=None, ypad=8, yoff=0):
     """The decode step with the o_proj shard in the same launch; returns (y,
-    core, canary columns of y)."""
+    the canary columns around y, core, W_o).  y is columns yoff .. yoff + n_out
+    of a canary-filled buffer of yoff + n_out + ypad columns."""
     import mla_decode_attention_lse_gb300 as m
 
     B, q, H, spr, S, S_out = (inp[k] for k in ("B", "q", "H", "spr", "S", "S_out"))
@@ -207,8 +208,8 @@ def run_fused_oproj(inp, n_out, seed=5, ws=None):
     part_o = torch.empty((spr, S, H, D), dtype=torch.bfloat16, device="cuda")
     part_lse = torch.empty((spr, S, H), dtype=torch.float32, device="cuda")
     out = torch.empty((S_out, H * 128), dtype=torch.bfloat16, device="cuda")
-    ybuf = torch.full((S, n_out + 8), CANARY, dtype=torch.int16, device="cuda")
-    y = ybuf[:, :n_out].view(torch.bfloat16)
+    ybuf = torch.full((S, yoff + n_out + ypad), CANARY, dtype=torch.int16, device="cuda")
+    y = ybuf[:, yoff:yoff + n_out].view(torch.bfloat16)
     if ws is None:
         ws = torch.zeros(m.mla_attn_combine_uv_workspace_words(B, q), dtype=torch.int32, device="cuda")
     m.mla_attn_combine_uv(inp["qv"], inp["kv"], inp["kv_len"], q, spr, inp["scale"], part_o, part_lse, inp["w_v"],
@@ -217,7 +218,8 @@ def run_fused_oproj(inp, n_out, seed=5, ws=None):
     assert m.mla_combine_uv_status() == m.MLA_OK
     assert int(ws.abs().sum()) == 0, "workspace not left zero"
     full = ybuf.cpu().numpy().view(np.uint16)
-    return full[:, :n_out], full[:, n_out:], out, w_o
+    canary = np.concatenate([full[:, :yoff], full[:, yoff + n_out:]], axis=1)
+    return full[:, yoff:yoff + n_out], canary, out, w_o
 
 
 OPROJ_CASES = [
@@ -256,6 +258,23 @@ def test_fused_with_oproj(lib, orc, B, q, H, spr, Lmax, lens, n_out):
     d = np.abs(g32 - r32)
     bad = d > 1e-2 + 1e-2 * np.abs(r32)
     assert not bad.any(), f"o_proj in the launch: {bad.sum()} out of tolerance, max {d.max()}"
+
+
+def test_fused_with_oproj_unaligned_y(lib):
+    """y whose rows do not start on 16-byte boundaries (its base 2 bytes past
+    one, its row stride n_out + 4): the shard's tile is copied out element by
+    element, with the same bits as mla_o_proj and nothing written around y."""
+    import mla_decode_attention_lse_gb300 as m
+
+    inp = problem(3, 2, 12, 2, 300, [300, 150, 7], seed=77)
+    n_out = 128
+    y, canary, core, w_o = run_fused_oproj(inp, n_out, ypad=3, yoff=1)
+    assert np.all(canary == CANARY), "wrote outside y"
+    S = inp["S"]
+    y2 = torch.empty((S, n_out), dtype=torch.bfloat16, device="cuda")
+    m.mla_o_proj(core[:S].contiguous(), w_o, y2)
+    torch.cuda.synchronize()
+    assert np.array_equal(y, to_np16(y2)), "y differs from mla_o_proj on the same core"
 
 
 def test_fused_with_oproj_decode_step(lib, orc):

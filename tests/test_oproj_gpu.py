@@ -45,7 +45,8 @@ def check(got, ref, what):
 
 
 @pytest.mark.parametrize("S,K,Nout", [(1, 64, 64), (5, 128, 192), (64, 1536, 256), (100, 256, 128),
-                                      (130, 192, 64), (300, 128, 128), (64, 1536, 7168)])
+                                      (130, 192, 64), (300, 128, 128), (64, 1536, 7168),
+                                      (64, 256, 10240)])  # 160 units: CTAs that run two
 def test_oproj_matches_oracle(lib, orc, S, K, Nout):
     g = torch.Generator(device="cuda")
     g.manual_seed(S * 7 + K)
@@ -53,6 +54,26 @@ def test_oproj_matches_oracle(lib, orc, S, K, Nout):
     w = (torch.randn((Nout, K), generator=g, device="cuda") / K ** 0.5).to(torch.bfloat16)
     out = run(x, w, out_pad=8 if Nout < 1000 else 0)
     check(out, orc.o_proj(to_np16(x), to_np16(w)), f"S={S} K={K} Nout={Nout}")
+
+
+def test_oproj_unaligned_output(lib, orc):
+    # out's rows start 2 bytes past a 16-byte boundary (base offset by one
+    # element, row stride Nout + 8): the output tile is copied element by
+    # element; the columns around out stay untouched
+    import mla_decode_attention_lse_gb300 as m
+
+    g = torch.Generator(device="cuda")
+    g.manual_seed(3)
+    S, K, Nout = 70, 256, 192
+    x = torch.randn((S, K), generator=g, device="cuda").to(torch.bfloat16)
+    w = (torch.randn((Nout, K), generator=g, device="cuda") / K ** 0.5).to(torch.bfloat16)
+    big = torch.empty((S, Nout + 9), dtype=torch.int16, device="cuda").fill_(CANARY).view(torch.bfloat16)
+    out = big[:, 1:Nout + 1]
+    m.mla_o_proj(x, w, out)
+    torch.cuda.synchronize()
+    assert m.mla_combine_uv_status() == m.MLA_OK
+    assert np.all(to_np16(big[:, :1]) == CANARY) and np.all(to_np16(big[:, Nout + 1:]) == CANARY)
+    check(out, orc.o_proj(to_np16(x), to_np16(w)), "unaligned output")
 
 
 def test_oproj_strided_rows(lib, orc):
