@@ -12,24 +12,28 @@
 // lse = ln sum_j exp(scale q.k_j) and o = sum_j softmax_j * latent_j (bf16);
 // a split with no visible position gives lse -inf and o 0.
 //
-// One CTA per (request, split, group of G heads): its N = roundup16(q G)
-// query rows share every cached row it reads, so a row is read once per
-// group.  Per tile of 128 positions:
-//   * TMA brings the tile as four 32-KiB double blocks (latents 128 c ..
-//     128 c + 127, two [128 x 64] boxes with the 128-byte swizzle) and one
-//     16-KiB rope block, into rings of shared-memory slots;
-//   * one thread issues S^T = K Q^T on the tensor cores (M = 128 positions,
-//     N query rows, K = 576), accumulator in TMEM;
-//   * four softmax warps (one TMEM lane quadrant each, a thread per
-//     position) mask, take the column max, write P^T = exp2(s - max) in bf16
-//     to shared memory and, when a column's max moved, rescale that column
-//     of the O accumulator in TMEM;
-//   * the same thread issues O^T += V^T P^T (four M = 128 latent chunks, K =
-//     128 positions): V^T is the tile's latent read MN-major in place.
-// At the end the softmax warps divide by the column sums, write o (bf16) and
-// lse.  Every wait is bounded; a timeout records an error, the roles stop,
-// and the kernel waits (bounded) for its own copies and MMAs before it frees
-// TMEM and returns.
+// Work items are (request, split, group of G heads): the N = roundup16(q G)
+// query rows of an item share every cached row it reads, so a row is read
+// once per group.  A persistent grid walks the items.  Up to 16 query rows
+// run two CTAs per SM with tiles of 64 positions, 32 rows one CTA per SM with
+// tiles of 128.  Per tile:
+//   * TMA brings the tile as four double blocks (latents 128 c .. 128 c +
+//     127, two [positions x 64] boxes with the 128-byte swizzle) and one rope
+//     block, into rings of shared-memory slots;
+//   * one thread issues S^T = K Q^T on the tensor cores (M = the tile's
+//     positions, N query rows, K = 576), accumulator in TMEM;
+//   * eight softmax warps (two per TMEM lane quadrant, a thread per position,
+//     half the query rows each) mask, take the column max, write P^T =
+//     exp2(s - reference max) in bf16 to shared memory and, when a column's
+//     reference moved, rescale that column of the O accumulator in TMEM;
+//   * O^T += V^T P^T (four M = 128 latent chunks, K = the tile's positions),
+//     V^T being the tile's latent read MN-major in place: issued by the same
+//     thread, or (the attention alone) by a thread of its own, so that the
+//     next tile's S^T goes out while this tile's softmax and O^T run.
+// At the end of an item the softmax warps divide by the column sums, write o
+// (bf16) and lse.  Every wait is bounded; a timeout records an error, the
+// roles stop, and the kernel waits (bounded) for its own copies and MMAs
+// before it frees TMEM and returns.
 //
 // The FUSED instance (mla_attn_combine_uv) runs the combine of the same page
 // behind the attention in the same launch, as the page's M1c + combine pair
@@ -46,7 +50,11 @@
 // combine's LSE weights into bf16 latents in shared memory, W_V[h] arrives by
 // TMA, one thread issues the W_UV GEMM (32 kind::f16 MMAs, M = 128 V rows,
 // N = 16 with 8 tokens) into TMEM, and the same warps apply the gate and
-// store core.  The last CTA to finish zeroes the workspace again.
+// store core.  With an o_proj weight, units of (64 outputs, 64 tokens) of
+// this rank's o_proj shard follow the combine units in the queue: each waits
+// (bounded) until every combine unit has stored its core rows, then runs the
+// GEMM the standalone o_proj kernel runs, with the same arithmetic.  The last
+// CTA to finish zeroes the workspace again.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -1048,7 +1056,7 @@ __global__ void __launch_bounds__(AttnLayout<N, FUSED>::kThreads, AttnLayout<N, 
             l_part[x] = __fmaf_rn(l_part[x], 1.0f, sc[x]);
           }
         } else {
-          // the tile's column max over 128 positions, exchanged through shared memory
+          // the tile's column max over its positions, exchanged through shared memory
           float *rd = red + (T & 1) * 4 * N;
 #pragma unroll
           for (int x = 0; x < NC; ++x) {
@@ -1235,8 +1243,8 @@ static cudaError_t launch_attn_n(const AttnParams &p, const CUtensorMap &map, co
   return cudaGetLastError();
 }
 
-// Persistent: one CTA per SM (the shared-memory plan fills an SM), at most
-// one per work item.
+// Persistent: one or two CTAs per SM (the shared-memory plan fills an SM or
+// half of one), at most one per work item.
 cudaError_t launch_attn(const AttnParams &p, const CUtensorMap &map, int num_sms, cudaStream_t stream) {
   const long long items = (long long)p.B * p.spr * p.groups;
   if (items <= 0 || items >= (1LL << 31) || num_sms < 1) return cudaErrorInvalidValue;
